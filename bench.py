@@ -1,0 +1,424 @@
+"""Benchmark: one training step of sharded causal attention per timed step.
+
+A step is one pass of the whole hot path on device-resident inputs: zigzag
+permute of Q/K/V, P ring steps of per-block (o, lse) partials with
+double-buffered key/value staging, the exact lse merge (fused inverse
+permute), delta, the P ring steps of the backward and the inverse permutes
+of dQ/dK/dV.  Default workload: B=1, H=16, S=32768, D=128 bf16, P=4 zigzag
+shards (the training-step case); --workload picks another of seeded_inputs.
+
+FLOPs: forward 2*B*H*S^2*D, backward 5*B*H*S^2*D (causal; five matmuls in
+the backward including the recompute of S).
+
+Multi-GPU: the path is computed on one GPU per process; with torchrun each
+rank runs an independent replica (no data-path collective) and the rank-0
+line reports the whole job's FLOPs over the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle instead (the deliberately slow
+plain implementation), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import seeded_inputs  # noqa: E402
+from seeded_inputs import WORKLOADS  # noqa: E402
+
+METRIC = "causal attn fwd/bwd TFLOP/s and % of BF16 tensor peak, S=8K–128K, 1×GB300"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+L2_BYTES = 129 * 2 ** 20
+
+
+def flops(w, fwd=True, bwd=True):
+    f = 2.0 * w.B * w.H * w.S * w.S * w.D if fwd else 0.0
+    if bwd and w.backward:
+        f += 5.0 * w.B * w.H * w.S * w.S * w.D
+    return f
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, ws: int, device=None) -> float:
+    """Largest value over all ranks (the slowest rank's time)."""
+    if ws <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "sharded_causal_softmax_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, sources, workload: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken
+    on the current source of the kernel; else None."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash(sources) or rec.get("workload") != workload:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ GPU arm ----
+
+def run_gpu(args):
+    import sharded_causal_softmax_gb300 as sca
+    from sharded_causal_softmax_gb300 import build as sca_build
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    if rank == 0 or ws == 1:
+        sca_build.build()
+    barrier(ws)
+    w = WORKLOADS[args.workload]
+    dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    inputs = seeded_inputs.workload_inputs(w)
+    dev_in = [x.to(device) for x in inputs]
+    plan = sca.ShardedCausalAttention(w.B, w.H, w.S, w.D, w.P, layout=w.layout, dtype=dtype,
+                                      head_groups=w.head_groups, schedule=w.schedule, backward=w.backward)
+    stream = torch.cuda.current_stream(device)
+
+    # per-launch timing of the attention kernels (same stream they run on)
+    timing = {"fwd": [], "bwd": []}
+    orig_fwd, orig_bwd = sca.capi.attn_fwd_shard, sca.capi.attn_bwd_shard
+
+    def timed(kind, fn):
+        def wrapper(*a, **k):
+            if not timing_on[0]:
+                return fn(*a, **k)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            r = fn(*a, **k)
+            e1.record(stream)
+            timing[kind].append((e0, e1))
+            return r
+        return wrapper
+
+    timing_on = [False]
+    sca.sharded.capi.attn_fwd_shard = timed("fwd", orig_fwd)
+    sca.sharded.capi.attn_bwd_shard = timed("bwd", orig_bwd)
+
+    def step():
+        plan.forward(*dev_in[:3])
+        kern = plan.kernels
+        if w.backward:
+            plan.backward(dev_in[3])
+            kern += plan.kernels
+        return kern
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if plan.read_status() != 0:
+        raise RuntimeError("device status word reports a failure")
+
+    # timed region: inputs (> L2) resident in HBM
+    barrier(ws)
+    torch.cuda.synchronize()
+    timing_on[0] = True
+    launches = 0
+    with ClockSampler(local) as clocks:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            launches += step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    timing_on[0] = False
+    barrier(ws)
+    ms = t0.elapsed_time(t1)
+    ms_max = max_over_ranks(ms, ws, device)
+    ms_per_step = ms_max / args.steps
+    step_flops = flops(w)
+    value = step_flops * args.steps * ws / (ms_max * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers
+    pinned = [x.pin_memory() for x in inputs]
+    outs_host = None
+    h2d = sum(x.numel() * x.element_size() for x in pinned)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    e2e_steps = max(1, min(args.steps, 5))
+    for _ in range(e2e_steps):
+        for d, h in zip(dev_in, pinned):
+            d.copy_(h, non_blocking=True)
+        o, lse = plan.forward(*dev_in[:3])
+        res = [o, lse]
+        if w.backward:
+            res += list(plan.backward(dev_in[3]))
+        if outs_host is None:
+            outs_host = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in res]
+        for hst, r in zip(outs_host, res):
+            hst.copy_(r, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    d2h = sum(x.numel() * x.element_size() for x in outs_host)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, device)
+    e2e_value = step_flops * e2e_steps * ws / (e2e_ms * 1e-3) / 1e12
+
+    # dominant kernel and its roofline
+    per = {}
+    for kind, evs in timing.items():
+        if evs:
+            durs = [a.elapsed_time(b) for a, b in evs]
+            per[kind] = (sum(durs), len(durs))
+    peaks, peak_src = load_peaks()
+    kind = max(per, key=lambda k: per[k][0])
+    total_ms, n = per[kind]
+    avg_s = total_ms / n * 1e-3
+    launch_flops = flops(w, fwd=(kind == "fwd"), bwd=(kind == "bwd")) / w.P
+    tc = plan.uses_tensor_cores(kind)
+    if tc:
+        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        bound, unit = "tensor", "TFLOP/s"
+        peak_note = f"{peak_src} bf16 sustained (kernel timed inside a long step)"
+    else:
+        # fp32 FMA issue: 152 SMs x 128 FMA/clk x 2 flop x measured max SM clock
+        mhz = peaks.get("sm_max_mhz", 2070.0)
+        peak = 152 * 128 * 2 * mhz * 1e6 / 1e12
+        bound, unit = "alu", "TFLOP/s"
+        peak_note = "derived fp32 FMA peak (152 SM x 128 FMA/clk x 2 x max SM clock)"
+    achieved = launch_flops / avg_s / 1e12
+    src = plan.kernel_sources(kind)
+    traffic = measured_traffic(plan.kernel_name(kind), src, w.name)
+    roofline = {"kernel": plan.kernel_name(kind), "bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1),
+                "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": peak_note, "launches_timed": n, "avg_launch_ms": round(avg_s * 1e3, 4),
+                "flops_per_launch": launch_flops}
+    other = {k: {"avg_launch_ms": round(v[0] / v[1], 4), "launches": v[1],
+                 "tflops": round(flops(w, fwd=(k == "fwd"), bwd=(k == "bwd")) / w.P / (v[0] / v[1] * 1e-3) / 1e12, 2)}
+             for k, v in per.items()}
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": w.description, "name": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "P": w.P,
+                   "layout": w.layout, "schedule": w.schedule, "head_groups": w.head_groups,
+                   "step": "fwd+bwd" if w.backward else "fwd",
+                   "flops_per_step": step_flops, "l2": "inputs larger than L2 (no flush)"
+                   if sum(x.numel() * x.element_size() for x in inputs) > L2_BYTES else "inputs fit in L2",
+                   "parallelism": f"{ws} independent replica(s), one per GPU"},
+        "clocks": clocks.summary(),
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": launches,
+        "roofline": roofline,
+        "kernels": other,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------ CPU oracle ----
+
+def oracle_sample(w, S_sample):
+    """One head of the workload over its first S_sample positions (a causal
+    prefix is itself a causal attention problem): inputs and FLOPs."""
+    ins = seeded_inputs.workload_inputs(w)
+    head = [x[:1, :1, :S_sample] for x in ins]
+    f = 2.0 * S_sample * S_sample * w.D + (5.0 * S_sample * S_sample * w.D if w.backward else 0.0)
+    return head, f
+
+
+def run_oracle_once(w, head):
+    import oracle
+    scale = 1.0 / math.sqrt(w.D)
+    o, lse = oracle.attention(head[0], head[1], head[2], scale)
+    if w.backward:
+        oracle.attention_backward(head[0], head[1], head[2], head[3], scale, o=o, lse=lse)
+
+
+def pick_sample(w, budget_s):
+    S_sample = min(w.S, 4096)
+    head, f = oracle_sample(w, S_sample)
+    t = time.perf_counter()
+    run_oracle_once(w, head)
+    dt = time.perf_counter() - t
+    # scale the prefix (work ~ S^2) to roughly the budget
+    target = S_sample * math.sqrt(max(1.0, budget_s / max(dt, 1e-3)))
+    S2 = int(min(w.S, max(S_sample, 2 ** int(math.log2(target)))))
+    return S2
+
+
+def cpu_baseline(w, budget_s=15.0):
+    S2 = pick_sample(w, budget_s)
+    head, f = oracle_sample(w, S2)
+    t = time.perf_counter()
+    run_oracle_once(w, head)
+    dt = time.perf_counter() - t
+    return {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle, {'fwd+bwd' if w.backward else 'fwd'} of one head (b=0, h=0) over the "
+                      f"first {S2} positions ({f / 1e9:.1f} GFLOP, {dt:.1f} s)"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    S2 = pick_sample(w, budget_s=min(12.0, 150.0 / max(1, args.steps + args.warmup)))
+    head, f = oracle_sample(w, S2)
+    for _ in range(args.warmup):
+        run_oracle_once(w, head)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        run_oracle_once(w, head)
+    dt = time.perf_counter() - t
+    value = f * args.steps / dt / 1e12
+    sample = (f"fp64 numpy oracle, {'fwd+bwd' if w.backward else 'fwd'} of one head over the first {S2} "
+              f"positions per step ({f / 1e9:.1f} GFLOP)")
+    line = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
+            "impl": "reference",
+            "config": {"workload": w.description, "name": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
+                       "P": w.P, "layout": w.layout},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="train_s32k")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gb300":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

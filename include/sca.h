@@ -1,0 +1,218 @@
+/*
+ * sca.h - C ABI of the sharded causal softmax attention library (libsca.so).
+ *
+ * The library computes causal softmax attention over a sequence split into P
+ * context shards, one (query shard, key/value block) pair at a time, as an
+ * (o, lse) partial, and merges the partials exactly by log-sum-exp
+ * rescaling.  The operation is the unit O = f(A B) C of "METP:
+ * memory-efficient tensor parallelism" (FITEE 10.1631/FITEE.2400602,
+ * abstract) with A B = Q K^T, f = causal row softmax of the scores times
+ * `scale`, C = V:
+ *
+ *     s_ij  = scale * q_i . k_j   if pos(k_j) <= pos(q_i), else -inf
+ *     lse_i = ln sum_j exp(s_ij)                  (natural log)
+ *     o_i   = sum_j exp(s_ij - lse_i) v_j
+ *
+ * A query row that sees no key of the block gives o = 0, lse = -inf.
+ *
+ * Conventions shared by every entry point
+ *   - All pointers are DEVICE pointers unless stated otherwise; the caller
+ *     owns all memory.  No entry point allocates device memory.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and returns an sca_status.  Arguments are validated on
+ *     the host before anything is launched; on a non-OK return nothing was
+ *     launched and sca_last_error() gives a message.
+ *   - `dev_status` (may be NULL) is a device int32 the caller zeroes once;
+ *     kernels record the first device-side failure in it (a bounded wait that
+ *     gave up: SCA_ERR_TIMEOUT).  Kernels never trap.  sca_read_status()
+ *     reads it back.
+ *   - Tensors are [B, H, rows, D] views with D contiguous; element strides
+ *     for batch, head and row are given explicitly (sca_view).  Base pointers
+ *     must be 16-byte aligned and row strides multiples of 8 elements (bf16)
+ *     or 4 elements (fp32).
+ *   - Errors are return codes only; no C++ exception crosses this boundary.
+ */
+#ifndef SCA_H
+#define SCA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SCA_OK = 0,
+  SCA_ERR_ARG = -1,          /* invalid argument (size, pointer, stride, alias) */
+  SCA_ERR_UNSUPPORTED = -2,  /* valid but not implemented (e.g. D not 64/128)  */
+  SCA_ERR_CUDA = -3,         /* a CUDA runtime/driver call failed              */
+  SCA_ERR_TIMEOUT = -4,      /* device-side bounded wait gave up (dev_status)  */
+  SCA_ERR_ALIGN = -5         /* pointer or stride misaligned                   */
+} sca_status;
+
+typedef enum { SCA_BF16 = 0, SCA_F32 = 1 } sca_dtype;
+
+/* Kernel choice for attn_fwd_shard / attn_bwd_shard.  AUTO picks the
+ * tcgen05 tensor-core kernel for bf16 and the fp32 SIMT kernel for fp32.
+ * SIMT forces the fp32-arithmetic kernel for either input dtype (used as an
+ * independent cross-check of the tensor-core kernel). */
+typedef enum { SCA_ALGO_AUTO = 0, SCA_ALGO_SIMT = 1, SCA_ALGO_TC = 2 } sca_algo;
+
+/* Row-position map of a slab of rows (a shard's queries or a key/value
+ * block): n (1 or 2) segments of `len` consecutive global positions; slab
+ * row i (0 <= i < n*len) sits at global position start[i / len] + i % len.
+ * A zigzag shard r of a sequence cut into 2P chunks of c rows is
+ * {n=2, len=c, start={r*c, (2P-1-r)*c}}; a contiguous shard is n=1.
+ * Causal visibility compares these global positions. */
+typedef struct {
+  int32_t n;
+  int32_t reserved;
+  int64_t len;
+  int64_t start[2];
+} sca_segs;
+
+/* Element strides (batch, head, row) of a [B, H, rows, D] tensor view; the
+ * D stride is 1. */
+typedef struct {
+  int64_t b, h, s;
+} sca_view;
+
+/* Shapes and layouts shared by all items of one attention call. */
+typedef struct {
+  int32_t B, H, D;     /* batch, heads, head dim (64 or 128)                 */
+  int32_t dtype;       /* sca_dtype of q, k, v (and dO in the backward)      */
+  int32_t causal;      /* 1: mask pos(k) > pos(q); 0: every key visible       */
+  int32_t algo;        /* sca_algo                                           */
+  float scale;         /* score scale, normally 1/sqrt(D)                    */
+  int32_t accumulate;  /* backward: 1 adds into dq/dk/dv, 0 overwrites them  */
+  sca_view q;          /* q (and dO) view                                    */
+  sca_view kv;         /* k and v view                                       */
+  sca_view o;          /* fp32 o (forward) / dq (backward) view              */
+  sca_view dkv;        /* fp32 dk, dv view (backward only)                   */
+  int64_t lse_b, lse_h;/* fp32 lse (and delta) strides; row stride is 1       */
+} sca_attn_dims;
+
+/* One (query shard, key/value block) work item of the forward. */
+typedef struct {
+  const void* q;       /* [B,H,Sq,D] with Sq = q_pos.n * q_pos.len           */
+  const void* k;       /* [B,H,Skv,D] with Skv = kv_pos.n * kv_pos.len        */
+  const void* v;       /* same view as k                                     */
+  float* o;            /* fp32 [B,H,Sq,D] partial output (normalised)        */
+  float* lse;          /* fp32 [B,H,Sq] partial lse (natural log)            */
+  sca_segs q_pos;
+  sca_segs kv_pos;
+} sca_fwd_item;
+
+#define SCA_MAX_ITEMS 32
+
+/* attn_fwd_shard - (o, lse) partials of causal attention for n_items
+ * independent (query shard, key block) pairs in one launch.
+ * Defined by: the unit O = f(A B) C of the METP abstract (above); the
+ * per-block partial and its lse are what lets a shard's output be built one
+ * ring step at a time ("Avances en la capacitacion de LLMs de secuencia
+ * larga", section "Limitaciones de los Enfoques Existentes").
+ * Items must not share output rows.  o is written (not accumulated), in
+ * fp32, already divided by the row's softmax denominator; lse is natural
+ * log.  Rows with no visible key: o = 0, lse = -inf.
+ * Errors: SCA_ERR_ARG for n_items outside [1, SCA_MAX_ITEMS], segment
+ * counts outside {1, 2}, non-positive sizes; SCA_ERR_UNSUPPORTED for D not
+ * in {64, 128}; SCA_ERR_ALIGN for misaligned bases or strides. */
+int attn_fwd_shard(const sca_fwd_item* items, int n_items, const sca_attn_dims* dims,
+                   int* dev_status, void* stream);
+
+/* attn_merge_lse - exact merge of n (o, lse) partials of the same rows:
+ *   M = max_i lse_i, w_i = exp(lse_i - M),
+ *   lse = M + ln sum_i w_i,  o = sum_i w_i o_i / sum_i w_i.
+ * Rows whose partials are all -inf give o = 0, lse = -inf.
+ * Layout: o_parts[p * o_part_stride + row * D + d] (fp32),
+ * lse_parts[p * lse_part_stride + row] (fp32), rows contiguous.
+ * Outputs: o_out fp32 [rows, D] (may alias partial 0), lse_out fp32 [rows]
+ * (may alias partial 0), o_bf16_out optional bf16 copy (NULL to skip).
+ * If `unpermute_P` > 0 the rows are taken as `rows / S` sequences of S
+ * rows in zigzag shard-major order over unpermute_P shards, and each output
+ * row is written at its natural position (fused inverse zigzag permute; the
+ * outputs must then not alias the inputs).
+ * Errors: SCA_ERR_ARG for n < 1 or n > 64, rows < 0, D not a positive
+ * multiple of 4, S not divisible by 2*unpermute_P; SCA_ERR_ALIGN. */
+int attn_merge_lse(const float* o_parts, const float* lse_parts, int n, int64_t rows, int D,
+                   int64_t o_part_stride, int64_t lse_part_stride,
+                   float* o_out, float* lse_out, void* o_bf16_out,
+                   int unpermute_P, int64_t S, void* stream);
+
+/* zigzag_permute - reorder the sequence axis of a [outer, S, row_bytes]
+ * byte tensor into zigzag shard-major order: the sequence is cut into 2P
+ * chunks of S/(2P) rows and shard r's slab holds chunk r followed by chunk
+ * 2P-1-r (TSP page, "Zyphra presenta el paralelismo de secuencia y tensor
+ * (TSP)", section "Lo que realmente significa plegar": K/V are reordered in
+ * zigzag before FlashAttention to balance causal work).  inverse = 1 undoes
+ * it.  A pure copy (bit exact).  src and dst must not overlap.
+ * Errors: SCA_ERR_ARG for S % (2P) != 0, P < 1, row_bytes not a positive
+ * multiple of 4, overlapping buffers; SCA_ERR_ALIGN if pointers are not
+ * 4-byte aligned. */
+int zigzag_permute(const void* src, void* dst, int64_t outer, int64_t S, int64_t row_bytes,
+                   int P, int inverse, void* stream);
+
+/* ring_stage_block - one ring step's key/value hand-off emulated on one GPU:
+ * copy rows [row0, row0 + rows) of every (b, h) of a [outer, S_src, row]
+ * tensor into a contiguous [outer, rows, row] staging buffer with the copy
+ * engine (one strided 2-D copy), so the next ring step's block is staged
+ * while the current one is computed (double buffering of the METP
+ * abstract; point-to-point passing of key/value blocks, "Avances en la
+ * capacitacion de LLMs de secuencia larga", section "Limitaciones de los
+ * Enfoques Existentes").  Errors: SCA_ERR_ARG for out-of-range rows. */
+int ring_stage_block(const void* src, void* dst, int64_t outer, int64_t S_src, int64_t row0,
+                     int64_t rows, int64_t row_bytes, void* stream);
+
+/* One (query shard, key/value block) work item of the backward.  dq, dk, dv
+ * are fp32: with dims->accumulate = 1 the item ADDS its contribution, with 0
+ * it overwrites them (every row of dq and of dk/dv is written, also rows
+ * that see no key of the block).  lse and delta are the FINAL (merged)
+ * values of the query rows. */
+typedef struct {
+  const void* q;       /* [B,H,Sq,D], dims->q view                           */
+  const void* k;       /* [B,H,Skv,D], dims->kv view                         */
+  const void* v;
+  const void* dout;    /* dO, [B,H,Sq,D], dims->q view                       */
+  const float* lse;    /* fp32 [B,H,Sq], natural log, dims->lse_* strides    */
+  const float* delta;  /* fp32 [B,H,Sq], delta_i = dO_i . O_i                */
+  float* dq;           /* fp32 [B,H,Sq,D], dims->o view                      */
+  float* dk;           /* fp32 [B,H,Skv,D], dims->dkv view                   */
+  float* dv;
+  sca_segs q_pos;
+  sca_segs kv_pos;
+} sca_bwd_item;
+
+/* attn_bwd_shard - gradient contributions of n_items (query shard, key
+ * block) pairs, recomputing P_ij = exp(s_ij - lse_i) from the saved lse:
+ *   dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - delta_i),
+ *   dq_i += scale sum_j dS_ij k_j,  dk_j += scale sum_i dS_ij q_i,
+ *   dv_j += sum_i P_ij dO_i.
+ * (Textbook softmax-attention backward; the pages describe only storing
+ * less and recomputing, "Avances en la capacitacion de LLMs de secuencia
+ * larga", section "Escalabilidad y Gestion de Memoria".)
+ * Items in one call must not share dq rows nor dk/dv rows.
+ * Errors as attn_fwd_shard. */
+int attn_bwd_shard(const sca_bwd_item* items, int n_items, const sca_attn_dims* dims,
+                   int* dev_status, void* stream);
+
+/* attn_bwd_delta - delta_i = sum_d dO_id * O_id for `rows` contiguous rows:
+ * o fp32 [rows, D], dout [rows, D] of dtype `dout_dtype`, delta fp32 [rows].
+ * Errors: SCA_ERR_ARG, SCA_ERR_ALIGN. */
+int attn_bwd_delta(const float* o, const void* dout, int dout_dtype, float* delta,
+                   int64_t rows, int D, void* stream);
+
+/* Message of the last non-OK return on the calling thread ("" if none). */
+const char* sca_last_error(void);
+
+/* Synchronises `stream`, copies *dev_status to the host and returns it
+ * (SCA_OK if no kernel recorded a failure), or SCA_ERR_CUDA. */
+int sca_read_status(const int* dev_status, void* stream);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int sca_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SCA_H */

@@ -1,0 +1,171 @@
+"""ctypes binding of libsca.so: the C ABI of ``include/sca.h``, one Python
+function per entry point with the same name.  Argument marshalling only -
+every step of the computation runs in the library's CUDA kernels.
+
+Loading fails loudly (ImportError) when the library has not been built; there
+is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_char_p, c_float, c_int, c_int32, c_int64, c_void_p
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsca.so")
+
+SCA_OK = 0
+SCA_ERR_ARG = -1
+SCA_ERR_UNSUPPORTED = -2
+SCA_ERR_CUDA = -3
+SCA_ERR_TIMEOUT = -4
+SCA_ERR_ALIGN = -5
+STATUS_NAMES = {0: "SCA_OK", -1: "SCA_ERR_ARG", -2: "SCA_ERR_UNSUPPORTED", -3: "SCA_ERR_CUDA",
+                -4: "SCA_ERR_TIMEOUT", -5: "SCA_ERR_ALIGN"}
+
+SCA_BF16 = 0
+SCA_F32 = 1
+SCA_ALGO_AUTO = 0
+SCA_ALGO_SIMT = 1
+SCA_ALGO_TC = 2
+SCA_MAX_ITEMS = 32
+
+EXPORTED = ("attn_fwd_shard", "attn_merge_lse", "zigzag_permute", "ring_stage_block", "attn_bwd_shard",
+            "attn_bwd_delta", "sca_last_error", "sca_read_status", "sca_version")
+
+
+class ScaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+class sca_segs(ctypes.Structure):
+    _fields_ = [("n", c_int32), ("reserved", c_int32), ("len", c_int64), ("start", c_int64 * 2)]
+
+
+class sca_view(ctypes.Structure):
+    _fields_ = [("b", c_int64), ("h", c_int64), ("s", c_int64)]
+
+
+class sca_attn_dims(ctypes.Structure):
+    _fields_ = [("B", c_int32), ("H", c_int32), ("D", c_int32), ("dtype", c_int32), ("causal", c_int32),
+                ("algo", c_int32), ("scale", c_float), ("accumulate", c_int32), ("q", sca_view), ("kv", sca_view),
+                ("o", sca_view), ("dkv", sca_view), ("lse_b", c_int64), ("lse_h", c_int64)]
+
+
+class sca_fwd_item(ctypes.Structure):
+    _fields_ = [("q", c_void_p), ("k", c_void_p), ("v", c_void_p), ("o", c_void_p), ("lse", c_void_p),
+                ("q_pos", sca_segs), ("kv_pos", sca_segs)]
+
+
+class sca_bwd_item(ctypes.Structure):
+    _fields_ = [("q", c_void_p), ("k", c_void_p), ("v", c_void_p), ("dout", c_void_p), ("lse", c_void_p),
+                ("delta", c_void_p), ("dq", c_void_p), ("dk", c_void_p), ("dv", c_void_p),
+                ("q_pos", sca_segs), ("kv_pos", sca_segs)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libsca.so not built ({LIB_PATH}); run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'` or "
+                          "`python sharded_causal_softmax_gb300/build.py`")
+    lib = ctypes.CDLL(LIB_PATH)
+    sig = {
+        "attn_fwd_shard": (c_int, [POINTER(sca_fwd_item), c_int, POINTER(sca_attn_dims), c_void_p, c_void_p]),
+        "attn_merge_lse": (c_int, [c_void_p, c_void_p, c_int, c_int64, c_int, c_int64, c_int64, c_void_p,
+                                   c_void_p, c_void_p, c_int, c_int64, c_void_p]),
+        "zigzag_permute": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int, c_int, c_void_p]),
+        "ring_stage_block": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_int64, c_void_p]),
+        "attn_bwd_shard": (c_int, [POINTER(sca_bwd_item), c_int, POINTER(sca_attn_dims), c_void_p, c_void_p]),
+        "attn_bwd_delta": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int64, c_int, c_void_p]),
+        "sca_last_error": (c_char_p, []),
+        "sca_read_status": (c_int, [c_void_p, c_void_p]),
+        "sca_version": (c_int, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = _load()
+    return _lib
+
+
+def last_error() -> str:
+    return lib().sca_last_error().decode(errors="replace")
+
+
+def check(rc: int) -> int:
+    if rc != SCA_OK:
+        raise ScaError(rc, last_error())
+    return rc
+
+
+def _items_array(cls, items):
+    arr = (cls * len(items))(*items)
+    return arr
+
+
+# ---- one function per C entry point (same names) -------------------------
+
+def attn_fwd_shard(items, dims: sca_attn_dims, dev_status: int, stream: int) -> int:
+    arr = _items_array(sca_fwd_item, items)
+    return check(lib().attn_fwd_shard(arr, len(items), ctypes.byref(dims), dev_status, stream))
+
+
+def attn_bwd_shard(items, dims: sca_attn_dims, dev_status: int, stream: int) -> int:
+    arr = _items_array(sca_bwd_item, items)
+    return check(lib().attn_bwd_shard(arr, len(items), ctypes.byref(dims), dev_status, stream))
+
+
+def attn_merge_lse(o_parts: int, lse_parts: int, n: int, rows: int, D: int, o_part_stride: int,
+                   lse_part_stride: int, o_out: int, lse_out: int, o_bf16_out: int, unpermute_P: int, S: int,
+                   stream: int) -> int:
+    return check(lib().attn_merge_lse(o_parts, lse_parts, n, rows, D, o_part_stride, lse_part_stride, o_out,
+                                      lse_out, o_bf16_out, unpermute_P, S, stream))
+
+
+def zigzag_permute(src: int, dst: int, outer: int, S: int, row_bytes: int, P: int, inverse: int,
+                   stream: int) -> int:
+    return check(lib().zigzag_permute(src, dst, outer, S, row_bytes, P, inverse, stream))
+
+
+def ring_stage_block(src: int, dst: int, outer: int, S_src: int, row0: int, rows: int, row_bytes: int,
+                     stream: int) -> int:
+    return check(lib().ring_stage_block(src, dst, outer, S_src, row0, rows, row_bytes, stream))
+
+
+def attn_bwd_delta(o: int, dout: int, dout_dtype: int, delta: int, rows: int, D: int, stream: int) -> int:
+    return check(lib().attn_bwd_delta(o, dout, dout_dtype, delta, rows, D, stream))
+
+
+def sca_read_status(dev_status: int, stream: int) -> int:
+    return lib().sca_read_status(dev_status, stream)
+
+
+def sca_version() -> int:
+    return lib().sca_version()
+
+
+def segs(n: int, length: int, starts) -> sca_segs:
+    s = sca_segs()
+    s.n = n
+    s.len = length
+    s.start[0] = starts[0]
+    s.start[1] = starts[1] if n > 1 else 0
+    return s
+
+
+def view(b: int, h: int, s: int) -> sca_view:
+    v = sca_view()
+    v.b, v.h, v.s = b, h, s
+    return v

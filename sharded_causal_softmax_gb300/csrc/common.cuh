@@ -1,0 +1,98 @@
+// Shared device/host definitions of libsca: item parameters passed to the
+// kernels, segment position arithmetic, status reporting.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "sca.h"
+
+#define SCA_INLINE __device__ __forceinline__
+
+namespace sca {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// Segment map of a slab of rows (mirror of sca_segs, device friendly).
+struct Segs {
+  int64_t len;
+  int64_t start0, start1;
+  int32_t n;
+};
+
+inline Segs to_segs(const sca_segs& s) {
+  Segs d;
+  d.len = s.len;
+  d.start0 = s.start[0];
+  d.start1 = s.n > 1 ? s.start[1] : 0;
+  d.n = s.n;
+  return d;
+}
+
+// Global position of slab row i.
+__host__ __device__ __forceinline__ int64_t seg_pos(const Segs& s, int64_t i) {
+  return i < s.len ? s.start0 + i : s.start1 + (i - s.len);
+}
+
+// Positions of a tile of slab rows [r0, r0 + cnt) (cnt >= 1, at most two
+// segment parts): min and max global position.
+__host__ __device__ __forceinline__ void tile_pos_range(const Segs& s, int64_t r0, int64_t cnt,
+                                                        int64_t& pmin, int64_t& pmax) {
+  const int64_t r1 = r0 + cnt - 1;
+  if (r1 < s.len || r0 >= s.len) {           // one part: positions increase
+    pmin = seg_pos(s, r0);
+    pmax = seg_pos(s, r1);
+  } else {                                   // straddles the two segments
+    const int64_t a0 = s.start0 + r0, a1 = s.start0 + s.len - 1;
+    const int64_t b0 = s.start1, b1 = s.start1 + (r1 - s.len);
+    pmin = a0 < b0 ? a0 : b0;
+    pmax = a1 > b1 ? a1 : b1;
+  }
+}
+
+// Per-item data of an attention launch (forward and backward share it).
+struct Item {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* dout;   // backward only
+  float* o;           // forward: o partial; backward: dq
+  float* lse;         // forward: lse out; backward: final lse (read)
+  const float* delta; // backward only
+  float* dk;
+  float* dv;
+  Segs qs, ks;
+  int64_t Sq, Skv;
+};
+
+struct View {
+  int64_t b, h, s;
+};
+
+struct AttnArgs {
+  Item items[SCA_MAX_ITEMS];
+  View q, kv, o, dkv;
+  int64_t lse_b, lse_h;
+  int32_t n_items, B, H, D;
+  int32_t causal;
+  int32_t accumulate; // backward: add into dq/dk/dv (1) or overwrite (0)
+  float scale;        // natural-units score scale
+  float scale_log2;   // scale * log2(e)
+  int32_t max_q_tiles;
+  int32_t max_k_tiles;
+  int* status;
+};
+
+// First device-side failure wins; never traps.
+SCA_INLINE void report(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+SCA_INLINE float to_f32(float x) { return x; }
+SCA_INLINE float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+}  // namespace sca

@@ -1,0 +1,309 @@
+// HBM-bound kernels: zigzag permute, ring staging copy, exact lse merge and
+// the backward's delta = rowsum(dO * O).  All move 16-byte vectors where the
+// layout allows; none allocates.
+#include <cmath>
+
+#include "common.cuh"
+#include "host_common.h"
+
+namespace sca {
+
+// ------------------------------------------------------------ zigzag permute
+//
+// The permute moves whole chunks of c = S/(2P) rows: destination chunk x of
+// sequence o is a contiguous copy of one source chunk.  Forward (natural ->
+// shard-major): destination chunk 2r holds natural chunk r and 2r+1 holds
+// natural chunk 2P-1-r.  Inverse: natural chunk n comes from shard-major
+// chunk 2n (n < P) or 2(2P-1-n)+1.  Each CTA copies a contiguous span of one
+// chunk, so loads and stores are fully coalesced.
+
+constexpr int kPermThreads = 256;
+constexpr int kPermUnroll = 4;
+
+__host__ __device__ __forceinline__ int zz_src_chunk(int ch, int P, int inverse) {
+  if (!inverse) {
+    const int r = ch >> 1;
+    return (ch & 1) ? (2 * P - 1 - r) : r;
+  }
+  return ch < P ? 2 * ch : 2 * (2 * P - 1 - ch) + 1;
+}
+
+template <typename V>
+__global__ void __launch_bounds__(kPermThreads) zigzag_permute_kernel(const V* __restrict__ src,
+                                                                      V* __restrict__ dst, int64_t nseg,
+                                                                      int64_t chunk_vecs, int P,
+                                                                      int inverse) {
+  const int two_p = 2 * P;
+  for (int64_t g = blockIdx.y; g < nseg; g += gridDim.y) {
+    const int64_t o = g / two_p;
+    const int ch = static_cast<int>(g - o * two_p);
+    const V* s = src + (o * two_p + zz_src_chunk(ch, P, inverse)) * chunk_vecs;
+    V* d = dst + (o * two_p + ch) * chunk_vecs;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * kPermThreads * kPermUnroll; base < chunk_vecs;
+         base += static_cast<int64_t>(gridDim.x) * kPermThreads * kPermUnroll) {
+      V tmp[kPermUnroll];
+#pragma unroll
+      for (int u = 0; u < kPermUnroll; ++u) {
+        const int64_t i = base + u * kPermThreads + threadIdx.x;
+        if (i < chunk_vecs) tmp[u] = s[i];
+      }
+#pragma unroll
+      for (int u = 0; u < kPermUnroll; ++u) {
+        const int64_t i = base + u * kPermThreads + threadIdx.x;
+        if (i < chunk_vecs) d[i] = tmp[u];
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- lse merge
+//
+// One group of L = D/4 lanes per row; each lane owns 4 consecutive columns
+// (one 16-byte vector) of every partial.  The lse values are read by the
+// lanes of the group and reduced with shuffles.
+
+constexpr int kMergeThreads = 256;
+
+__device__ __forceinline__ int64_t zz_natural_row(int64_t row, int64_t S, int P) {
+  const int64_t o = row / S;
+  const int64_t x = row - o * S;
+  const int64_t c = S / (2 * P);
+  const int64_t r = x / (2 * c);
+  const int64_t w = x - r * 2 * c;
+  const int64_t nat = w < c ? r * c + w : (2 * P - 1 - r) * c + (w - c);
+  return o * S + nat;
+}
+
+template <int L>
+__global__ void __launch_bounds__(kMergeThreads) merge_lse_kernel(
+    const float* __restrict__ o_parts, const float* __restrict__ lse_parts, int n, int64_t rows,
+    int64_t ops, int64_t lps, float* o_out, float* lse_out, __nv_bfloat16* ob_out, int uP, int64_t S) {
+  constexpr int RPW = 32 / L;  // rows per warp
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / L, li = lane % L;
+  const unsigned gmask = (L == 32) ? 0xffffffffu : (((1u << L) - 1u) << (sub * L));
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kMergeThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kMergeThreads) >> 5;
+  const int D = 4 * L;
+  for (int64_t row0 = warp * RPW; row0 < rows; row0 += nwarps * RPW) {
+    const int64_t row = row0 + sub;
+    const bool active = row < rows;
+    // max lse over partials: lane li reads partials li, li+L, ...
+    float M = -INFINITY;
+    if (active)
+      for (int p = li; p < n; p += L) M = fmaxf(M, lse_parts[p * lps + row]);
+#pragma unroll
+    for (int off = L / 2; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(gmask, M, off));
+    const float M0 = (M == -INFINITY) ? 0.f : M;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    if (active) {
+      int p = 0;
+      for (; p + 4 <= n; p += 4) {
+        float4 v[4];
+        float w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          v[u] = *reinterpret_cast<const float4*>(o_parts + (p + u) * ops + row * D + 4 * li);
+          w[u] = lse_parts[(p + u) * lps + row];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float wu = expf(w[u] - M0);   // exp(-inf) = 0 for empty partials
+          wsum += wu;
+          acc.x += wu * v[u].x; acc.y += wu * v[u].y; acc.z += wu * v[u].z; acc.w += wu * v[u].w;
+        }
+      }
+      for (; p < n; ++p) {
+        const float4 v = *reinterpret_cast<const float4*>(o_parts + p * ops + row * D + 4 * li);
+        const float wu = expf(lse_parts[p * lps + row] - M0);
+        wsum += wu;
+        acc.x += wu * v.x; acc.y += wu * v.y; acc.z += wu * v.z; acc.w += wu * v.w;
+      }
+      const bool empty = (M == -INFINITY);
+      const float inv = empty ? 0.f : 1.f / wsum;
+      acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+      const int64_t orow = uP > 0 ? zz_natural_row(row, S, uP) : row;
+      *reinterpret_cast<float4*>(o_out + orow * D + 4 * li) = acc;
+      if (ob_out) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(ob_out + orow * D + 4 * li) = pk;
+      }
+      if (li == 0) lse_out[orow] = empty ? -INFINITY : M0 + logf(wsum);
+    }
+  }
+}
+
+// -------------------------------------------------------------------- delta
+
+template <int L, typename T>
+__global__ void __launch_bounds__(kMergeThreads) delta_kernel(const float* __restrict__ o,
+                                                              const T* __restrict__ dout,
+                                                              float* __restrict__ delta, int64_t rows) {
+  constexpr int RPW = 32 / L;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / L, li = lane % L;
+  const unsigned gmask = (L == 32) ? 0xffffffffu : (((1u << L) - 1u) << (sub * L));
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kMergeThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kMergeThreads) >> 5;
+  const int D = 4 * L;
+  for (int64_t row0 = warp * RPW; row0 < rows; row0 += nwarps * RPW) {
+    const int64_t row = row0 + sub;
+    float s = 0.f;
+    if (row < rows) {
+      const float4 ov = *reinterpret_cast<const float4*>(o + row * D + 4 * li);
+      const T* dp = dout + row * D + 4 * li;
+      s = ov.x * to_f32(dp[0]) + ov.y * to_f32(dp[1]) + ov.z * to_f32(dp[2]) + ov.w * to_f32(dp[3]);
+    }
+#pragma unroll
+    for (int off = L / 2; off > 0; off >>= 1) s += __shfl_xor_sync(gmask, s, off);
+    if (row < rows && li == 0) delta[row] = s;
+  }
+}
+
+static int grid_for(int64_t work_items, int per_block) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t blocks = (work_items + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(sms) * 16;
+  if (blocks > cap) blocks = cap;
+  return static_cast<int>(blocks < 1 ? 1 : blocks);
+}
+
+static bool overlap(const void* a, const void* b, int64_t bytes) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bytes && y < x + bytes;
+}
+
+}  // namespace sca
+
+using namespace sca;
+
+extern "C" int zigzag_permute(const void* src, void* dst, int64_t outer, int64_t S, int64_t row_bytes, int P,
+                              int inverse, void* stream) {
+  SCA_REQUIRE(src && dst, SCA_ERR_ARG, "zigzag_permute: NULL pointer");
+  SCA_REQUIRE(P >= 1, SCA_ERR_ARG, "zigzag_permute: P=%d must be >= 1", P);
+  SCA_REQUIRE(outer >= 0 && S >= 0, SCA_ERR_ARG, "zigzag_permute: negative size");
+  SCA_REQUIRE(S % (2 * P) == 0, SCA_ERR_ARG, "zigzag_permute: S=%lld not divisible by 2P=%d",
+              static_cast<long long>(S), 2 * P);
+  SCA_REQUIRE(row_bytes > 0 && row_bytes % 4 == 0, SCA_ERR_ARG,
+              "zigzag_permute: row_bytes=%lld must be a positive multiple of 4",
+              static_cast<long long>(row_bytes));
+  SCA_REQUIRE(aligned(src, 4) && aligned(dst, 4), SCA_ERR_ALIGN, "zigzag_permute: pointers not 4-byte aligned");
+  const int64_t total = outer * S * row_bytes;
+  SCA_REQUIRE(!overlap(src, dst, total), SCA_ERR_ARG, "zigzag_permute: src and dst overlap");
+  if (total == 0) return SCA_OK;
+  const int64_t chunk_bytes = (S / (2 * P)) * row_bytes;
+  const int64_t nseg = outer * 2 * P;
+  const bool vec16 = chunk_bytes % 16 == 0 && aligned(src, 16) && aligned(dst, 16);
+  const int64_t vsz = vec16 ? 16 : 4;
+  const int64_t chunk_vecs = chunk_bytes / vsz;
+  const int per_block = kPermThreads * kPermUnroll;
+  int64_t gx = (chunk_vecs + per_block - 1) / per_block;
+  const int gy = static_cast<int>(nseg < 65535 ? nseg : 65535);
+  const int64_t cap = grid_for(1LL << 40, 1) / gy + 1;
+  if (gx > cap) gx = cap;
+  dim3 grid(static_cast<unsigned>(gx < 1 ? 1 : gx), gy);
+  cudaStream_t st = as_stream(stream);
+  if (vec16)
+    zigzag_permute_kernel<uint4><<<grid, kPermThreads, 0, st>>>(static_cast<const uint4*>(src),
+                                                                static_cast<uint4*>(dst), nseg, chunk_vecs,
+                                                                P, inverse);
+  else
+    zigzag_permute_kernel<uint32_t><<<grid, kPermThreads, 0, st>>>(static_cast<const uint32_t*>(src),
+                                                                   static_cast<uint32_t*>(dst), nseg,
+                                                                   chunk_vecs, P, inverse);
+  return cuda_status(cudaGetLastError(), "zigzag_permute launch");
+}
+
+extern "C" int ring_stage_block(const void* src, void* dst, int64_t outer, int64_t S_src, int64_t row0,
+                                int64_t rows, int64_t row_bytes, void* stream) {
+  SCA_REQUIRE(src && dst, SCA_ERR_ARG, "ring_stage_block: NULL pointer");
+  SCA_REQUIRE(outer >= 0 && rows >= 0 && row_bytes > 0 && row0 >= 0 && row0 + rows <= S_src, SCA_ERR_ARG,
+              "ring_stage_block: rows [%lld, %lld) outside [0, %lld)", static_cast<long long>(row0),
+              static_cast<long long>(row0 + rows), static_cast<long long>(S_src));
+  if (outer == 0 || rows == 0) return SCA_OK;
+  const char* s = static_cast<const char*>(src) + row0 * row_bytes;
+  const cudaError_t e =
+      cudaMemcpy2DAsync(dst, static_cast<size_t>(rows * row_bytes), s, static_cast<size_t>(S_src * row_bytes),
+                        static_cast<size_t>(rows * row_bytes), static_cast<size_t>(outer),
+                        cudaMemcpyDeviceToDevice, as_stream(stream));
+  return cuda_status(e, "ring_stage_block copy");
+}
+
+extern "C" int attn_merge_lse(const float* o_parts, const float* lse_parts, int n, int64_t rows, int D,
+                              int64_t o_part_stride, int64_t lse_part_stride, float* o_out, float* lse_out,
+                              void* o_bf16_out, int unpermute_P, int64_t S, void* stream) {
+  SCA_REQUIRE(o_parts && lse_parts && o_out && lse_out, SCA_ERR_ARG, "attn_merge_lse: NULL pointer");
+  SCA_REQUIRE(n >= 1 && n <= 64, SCA_ERR_ARG, "attn_merge_lse: n=%d outside [1, 64]", n);
+  SCA_REQUIRE(rows >= 0, SCA_ERR_ARG, "attn_merge_lse: rows < 0");
+  SCA_REQUIRE(D == 4 || D == 8 || D == 16 || D == 32 || D == 64 || D == 128, SCA_ERR_ARG,
+              "attn_merge_lse: D=%d must be one of 4, 8, 16, 32, 64, 128", D);
+  SCA_REQUIRE(o_part_stride >= rows * D && lse_part_stride >= rows, SCA_ERR_ARG,
+              "attn_merge_lse: partial strides smaller than one partial");
+  SCA_REQUIRE(o_part_stride % 4 == 0, SCA_ERR_ALIGN, "attn_merge_lse: o_part_stride not a multiple of 4");
+  SCA_REQUIRE(aligned(o_parts, 16) && aligned(o_out, 16) && aligned(o_bf16_out, 8), SCA_ERR_ALIGN,
+              "attn_merge_lse: o pointers must be 16-byte aligned (bf16 copy 8-byte)");
+  if (unpermute_P > 0) {
+    SCA_REQUIRE(S > 0 && S % (2 * unpermute_P) == 0 && rows % S == 0, SCA_ERR_ARG,
+                "attn_merge_lse: unpermute needs S %% 2P == 0 and rows %% S == 0");
+    SCA_REQUIRE(!overlap(o_parts, o_out, n * o_part_stride * 4) &&
+                    !overlap(lse_parts, lse_out, n * lse_part_stride * 4),
+                SCA_ERR_ARG, "attn_merge_lse: outputs may not alias inputs when unpermuting");
+  }
+  if (rows == 0) return SCA_OK;
+  const int L = D / 4;
+  const int64_t warps = (rows + (32 / L) - 1) / (32 / L);
+  const int grid = grid_for(warps * 32, kMergeThreads);
+  cudaStream_t st = as_stream(stream);
+  auto* ob = static_cast<__nv_bfloat16*>(o_bf16_out);
+#define SCA_MERGE_CASE(LL)                                                                             \
+  case LL:                                                                                             \
+    merge_lse_kernel<LL><<<grid, kMergeThreads, 0, st>>>(o_parts, lse_parts, n, rows, o_part_stride,   \
+                                                         lse_part_stride, o_out, lse_out, ob,         \
+                                                         unpermute_P, S);                              \
+    break;
+  switch (L) {
+    SCA_MERGE_CASE(1)
+    SCA_MERGE_CASE(2)
+    SCA_MERGE_CASE(4)
+    SCA_MERGE_CASE(8)
+    SCA_MERGE_CASE(16)
+    SCA_MERGE_CASE(32)
+  }
+#undef SCA_MERGE_CASE
+  return cuda_status(cudaGetLastError(), "attn_merge_lse launch");
+}
+
+extern "C" int attn_bwd_delta(const float* o, const void* dout, int dout_dtype, float* delta, int64_t rows,
+                              int D, void* stream) {
+  SCA_REQUIRE(o && dout && delta, SCA_ERR_ARG, "attn_bwd_delta: NULL pointer");
+  SCA_REQUIRE(rows >= 0, SCA_ERR_ARG, "attn_bwd_delta: rows < 0");
+  SCA_REQUIRE(D == 64 || D == 128, SCA_ERR_UNSUPPORTED, "attn_bwd_delta: D=%d not in {64, 128}", D);
+  SCA_REQUIRE(dout_dtype == SCA_BF16 || dout_dtype == SCA_F32, SCA_ERR_ARG, "attn_bwd_delta: bad dtype");
+  SCA_REQUIRE(aligned(o, 16) && aligned(dout, 8), SCA_ERR_ALIGN, "attn_bwd_delta: misaligned pointer");
+  if (rows == 0) return SCA_OK;
+  const int L = D / 4;
+  const int64_t warps = (rows + (32 / L) - 1) / (32 / L);
+  const int grid = grid_for(warps * 32, kMergeThreads);
+  cudaStream_t st = as_stream(stream);
+  if (dout_dtype == SCA_BF16) {
+    if (L == 32)
+      delta_kernel<32, __nv_bfloat16><<<grid, kMergeThreads, 0, st>>>(
+          o, static_cast<const __nv_bfloat16*>(dout), delta, rows);
+    else
+      delta_kernel<16, __nv_bfloat16><<<grid, kMergeThreads, 0, st>>>(
+          o, static_cast<const __nv_bfloat16*>(dout), delta, rows);
+  } else {
+    if (L == 32)
+      delta_kernel<32, float><<<grid, kMergeThreads, 0, st>>>(o, static_cast<const float*>(dout), delta, rows);
+    else
+      delta_kernel<16, float><<<grid, kMergeThreads, 0, st>>>(o, static_cast<const float*>(dout), delta, rows);
+  }
+  return cuda_status(cudaGetLastError(), "attn_bwd_delta launch");
+}

@@ -1,0 +1,353 @@
+"""P virtual context shards of causal softmax attention on one GPU.
+
+The schedule (host logic only; every byte is moved or computed by libsca):
+
+* Partition.  Zigzag (TSP page, "Zyphra presenta el paralelismo de secuencia
+  y tensor (TSP)", section "Lo que realmente significa plegar"): the sequence
+  is cut into 2P chunks of c rows and shard r owns chunks r and 2P-1-r, which
+  balances causal work; ``zigzag_permute`` lays Q, K, V out shard-major so a
+  shard is one contiguous slab of 2c rows per (batch, head).  Contiguous:
+  shard r owns rows [r S/P, (r+1) S/P) and nothing is permuted.
+* 2D split ("Avances en la capacitacion de LLMs de secuencia larga", section
+  "Introduciendo la Atencion 2D"): G head groups x P context shards give
+  G*P virtual ranks; rank (g, r) holds heads [g H/G, (g+1) H/G) of shard r.
+* Ring (same page, section "Limitaciones de los Enfoques Existentes"): at
+  step t rank (g, r) holds key/value block (r - t) mod P and computes the
+  (o, lse) partial of its queries against it.  With the "ring" schedule the
+  blocks move like a ring pass: before step t+1, each rank's staging buffer
+  receives the block its left neighbour holds at step t, copied by the copy
+  engine on a side stream into the spare one of two staging buffers while
+  step t computes (the double buffer of the METP abstract, FITEE
+  10.1631/FITEE.2400602).  The "direct" schedule reads every block from its
+  home slab (the K/V all-gather reading of the TSP page).
+* Merge: the P partials of every row are combined exactly by log-sum-exp
+  rescaling, fused with the inverse zigzag permute (``attn_merge_lse``).
+* Backward: delta = rowsum(dO * O), then the same ring of steps; each step
+  recomputes P from the final lse and adds into dQ of the rank's rows and
+  into dK/dV of the block's home rows (step 0 overwrites, so no zeroing pass
+  is needed); finally the gradients are permuted back to natural order.
+
+PyTorch supplies device memory, streams and events only.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import capi
+
+_DT = {torch.bfloat16: capi.SCA_BF16, torch.float32: capi.SCA_F32}
+
+
+def ring_block(r: int, t: int, P: int) -> int:
+    """Key/value block held by shard r at ring step t."""
+    return (r - t) % P
+
+
+def shard_segs(S: int, P: int, layout: str, r: int) -> capi.sca_segs:
+    """Global positions of shard r's rows, in the shard's row order."""
+    if layout == "zigzag":
+        c = S // (2 * P)
+        return capi.segs(2, c, (r * c, (2 * P - 1 - r) * c))
+    n = S // P
+    return capi.segs(1, n, (r * n, 0))
+
+
+def _ptr(t: torch.Tensor) -> int:
+    return t.data_ptr()
+
+
+class ShardedCausalAttention:
+    """Buffers and launch schedule of one sharded attention configuration.
+
+    Create once, then call ``forward`` (and ``backward``) per step; nothing is
+    allocated per call.  Inputs are [B, H, S, D] tensors in natural order, of
+    ``dtype`` (bf16 or fp32), contiguous, on the current CUDA device.
+    Outputs are fp32 [B, H, S, D] (and lse [B, H, S], natural log).
+    """
+
+    def __init__(self, B, H, S, D, P, layout="zigzag", dtype=torch.bfloat16, head_groups=1,
+                 schedule="ring", scale=None, causal=True, algo=capi.SCA_ALGO_AUTO, backward=False,
+                 bf16_out=False, device=None):
+        if layout not in ("zigzag", "contiguous"):
+            raise ValueError(f"layout {layout!r}")
+        if schedule not in ("ring", "direct"):
+            raise ValueError(f"schedule {schedule!r}")
+        if dtype not in _DT:
+            raise ValueError(f"dtype {dtype}")
+        if S % (2 * P if layout == "zigzag" else P):
+            raise ValueError(f"S={S} not divisible into {P} {layout} shards")
+        if H % head_groups:
+            raise ValueError("head_groups must divide H")
+        if head_groups * P > capi.SCA_MAX_ITEMS:
+            raise ValueError(f"{head_groups * P} virtual ranks > {capi.SCA_MAX_ITEMS}")
+        self.B, self.H, self.S, self.D, self.P = B, H, S, D, P
+        self.G, self.Hg = head_groups, H // head_groups
+        self.layout, self.schedule, self.dtype = layout, schedule, dtype
+        self.scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+        self.causal, self.algo, self.backward_enabled = causal, algo, backward
+        self.n_r = S // P                       # rows per shard
+        self.eb = torch.tensor([], dtype=dtype).element_size()
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        self.device = dev
+        z = lambda *shape, dt=torch.float32: torch.empty(shape, dtype=dt, device=dev)
+        zig = layout == "zigzag"
+        self.qp = z(B, H, S, D, dt=dtype) if zig else None
+        self.kp = z(B, H, S, D, dt=dtype) if zig else None
+        self.vp = z(B, H, S, D, dt=dtype) if zig else None
+        self.o_parts = z(P, B, H, S, D)
+        self.lse_parts = z(P, B, H, S)
+        self.o = z(B, H, S, D)
+        self.lse = z(B, H, S)
+        self.o_bf16 = z(B, H, S, D, dt=torch.bfloat16) if bf16_out else None
+        ring = schedule == "ring" and P > 1
+        self.stage_k = [z(self.G, P, B, self.Hg, self.n_r, D, dt=dtype) for _ in range(2)] if ring else None
+        self.stage_v = [z(self.G, P, B, self.Hg, self.n_r, D, dt=dtype) for _ in range(2)] if ring else None
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        if backward:
+            self.delta = z(B, H, S)
+            self.dq = z(B, H, S, D)
+            self.dk = z(B, H, S, D)
+            self.dv = z(B, H, S, D)
+            self.dop = z(B, H, S, D, dt=dtype) if zig else None
+            self.lse_p = z(B, H, S) if zig else None
+            self.delta_p = z(B, H, S) if zig else None
+            self.dq_p = z(B, H, S, D) if zig else None
+            self.dk_p = z(B, H, S, D) if zig else None
+            self.dv_p = z(B, H, S, D) if zig else None
+        self.copy_stream = torch.cuda.Stream(device=dev) if ring else None
+        self.ev_ready = torch.cuda.Event()
+        self.ev_staged = [torch.cuda.Event() for _ in range(P)]
+        self.ev_done = [torch.cuda.Event() for _ in range(P)]
+        self.launches = 0   # kernels + copies issued by the last forward/backward
+        self.kernels = 0    # kernels alone
+
+    # ------------------------------------------------------------ helpers
+
+    def _permute(self, src, dst, row_bytes, inverse, stream):
+        capi.zigzag_permute(_ptr(src), _ptr(dst), self.B * self.H, self.S, row_bytes, self.P, inverse, stream)
+        self.launches += 1
+        self.kernels += 1
+
+    # ------------------------------------------------- kernel descriptions
+
+    def uses_tensor_cores(self, kind: str) -> bool:
+        if self.dtype != torch.bfloat16 or self.algo == capi.SCA_ALGO_SIMT:
+            return False
+        return kind == "fwd" or self.algo == capi.SCA_ALGO_TC
+
+    def kernel_name(self, kind: str) -> str:
+        tc = self.uses_tensor_cores(kind)
+        if kind == "fwd":
+            return "fwd_tc_kernel" if tc else "fwd_simt_kernel"
+        return "bwd_tc_kernel" if tc else "dq_simt_kernel+dkv_simt_kernel"
+
+    def kernel_sources(self, kind: str):
+        tc = self.uses_tensor_cores(kind)
+        if kind == "fwd":
+            return ["fwd_tc.cu", "ptx.cuh", "common.cuh"] if tc else ["attn_simt.cu", "common.cuh"]
+        return ["bwd_tc.cu", "ptx.cuh", "common.cuh"] if tc else ["attn_simt.cu", "common.cuh"]
+
+    def kernels_per_attn_call(self, kind: str) -> int:
+        return 2 if (kind == "bwd" and not self.uses_tensor_cores("bwd")) else 1
+
+    def _dims(self, kv_view, backward=False, accumulate=0):
+        d = capi.sca_attn_dims()
+        d.B, d.H, d.D = self.B, self.Hg, self.D
+        d.dtype = _DT[self.dtype]
+        d.causal = 1 if self.causal else 0
+        d.algo = self.algo
+        d.scale = self.scale
+        d.accumulate = accumulate
+        S, D, H = self.S, self.D, self.H
+        d.q = capi.view(H * S * D, S * D, D)
+        d.kv = kv_view
+        d.o = capi.view(H * S * D, S * D, D)
+        d.dkv = capi.view(H * S * D, S * D, D)
+        d.lse_b, d.lse_h = H * S, S
+        return d
+
+    def _home_kv_view(self):
+        return capi.view(self.H * self.S * self.D, self.S * self.D, self.D)
+
+    def _stage_kv_view(self):
+        return capi.view(self.Hg * self.n_r * self.D, self.n_r * self.D, self.D)
+
+    def _kv_ptrs(self, k_home, v_home, t, g, r):
+        """(k, v) base pointers of the block rank (g, r) holds at step t."""
+        P = self.P
+        if self.stage_k is None or t == 0:
+            j = ring_block(r, t, P)
+            off = (g * self.Hg * self.S + j * self.n_r) * self.D * self.eb
+            return _ptr(k_home) + off, _ptr(v_home) + off
+        buf = t % 2
+        return _ptr(self.stage_k[buf][g, r]), _ptr(self.stage_v[buf][g, r])
+
+    def _stage(self, k_home, v_home, t_next):
+        """Ring pass into the spare buffer: rank (g, r) receives what rank
+        (g, r-1) holds at step t_next - 1."""
+        P, B, Hg, n_r, D, eb = self.P, self.B, self.Hg, self.n_r, self.D, self.eb
+        cs = self.copy_stream.cuda_stream
+        dst_k, dst_v = self.stage_k[t_next % 2], self.stage_v[t_next % 2]
+        row = D * eb
+        for g in range(self.G):
+            if t_next == 1:   # neighbours' home blocks
+                for r in range(P):
+                    src_r = (r - 1) % P
+                    for b in range(B):
+                        off = ((b * self.H + g * Hg) * self.S) * row
+                        for home, dst in ((k_home, dst_k), (v_home, dst_v)):
+                            capi.ring_stage_block(_ptr(home) + off, _ptr(dst[g, r, b]), Hg, self.S,
+                                                  src_r * n_r, n_r, row, cs)
+                            self.launches += 1
+            else:             # neighbours' staged blocks: a rotation by one rank
+                src_k, src_v = self.stage_k[(t_next - 1) % 2], self.stage_v[(t_next - 1) % 2]
+                blk = B * Hg * n_r
+                for src, dst in ((src_k, dst_k), (src_v, dst_v)):
+                    capi.ring_stage_block(_ptr(src[g, 0]), _ptr(dst[g, 1]), 1, (P - 1) * blk, 0, (P - 1) * blk,
+                                          row, cs)
+                    capi.ring_stage_block(_ptr(src[g, P - 1]), _ptr(dst[g, 0]), 1, blk, 0, blk, row, cs)
+                    self.launches += 2
+
+    def _ring(self, k_home, v_home, launch_step):
+        """Run launch_step(t, kv_ptrs(g, r), kv_view) for t = 0..P-1 with the
+        staging copies of step t+1 overlapped on the copy stream."""
+        cur = torch.cuda.current_stream(self.device)
+        ring = self.stage_k is not None
+        if ring:
+            self.ev_ready.record(cur)
+            self.copy_stream.wait_event(self.ev_ready)
+        for t in range(self.P):
+            if ring and t + 1 < self.P:
+                with torch.cuda.stream(self.copy_stream):
+                    if t >= 1:
+                        self.copy_stream.wait_event(self.ev_done[t - 1])
+                    self._stage(k_home, v_home, t + 1)
+                    self.ev_staged[t + 1].record(self.copy_stream)
+            if ring and t >= 1:
+                cur.wait_event(self.ev_staged[t])
+            view = self._home_kv_view() if (not ring or t == 0) else self._stage_kv_view()
+            launch_step(t, lambda g, r: self._kv_ptrs(k_home, v_home, t, g, r), view)
+            self.ev_done[t].record(cur)
+        if ring:  # the staging buffers are reused by the next call
+            cur.wait_stream(self.copy_stream)
+
+    # ------------------------------------------------------------ forward
+
+    def forward(self, q, k, v):
+        self._check_inputs(q, k, v)
+        self.launches = self.kernels = 0
+        stream = torch.cuda.current_stream(self.device).cuda_stream
+        zig = self.layout == "zigzag"
+        row = self.D * self.eb
+        if zig:
+            self._permute(q, self.qp, row, 0, stream)
+            self._permute(k, self.kp, row, 0, stream)
+            self._permute(v, self.vp, row, 0, stream)
+            qh, kh, vh = self.qp, self.kp, self.vp
+        else:
+            qh, kh, vh = q, k, v
+        S, D, H, P = self.S, self.D, self.H, self.P
+        eb = self.eb
+        st_ptr = _ptr(self.status)
+
+        def step(t, kv_ptrs, kv_view):
+            items = []
+            for g in range(self.G):
+                for r in range(P):
+                    it = capi.sca_fwd_item()
+                    hoff = g * self.Hg * S
+                    it.q = _ptr(qh) + (hoff + r * self.n_r) * D * eb
+                    it.k, it.v = kv_ptrs(g, r)
+                    it.o = _ptr(self.o_parts[t]) + (hoff + r * self.n_r) * D * 4
+                    it.lse = _ptr(self.lse_parts[t]) + (hoff + r * self.n_r) * 4
+                    it.q_pos = shard_segs(S, P, self.layout, r)
+                    it.kv_pos = shard_segs(S, P, self.layout, ring_block(r, t, P))
+                    items.append(it)
+            capi.attn_fwd_shard(items, self._dims(kv_view), st_ptr, stream)
+            self.launches += 1
+            self.kernels += 1
+
+        self._ring(kh, vh, step)
+        rows = self.B * H * S
+        capi.attn_merge_lse(_ptr(self.o_parts), _ptr(self.lse_parts), P, rows, D, rows * D, rows,
+                            _ptr(self.o), _ptr(self.lse), _ptr(self.o_bf16) if self.o_bf16 is not None else 0,
+                            P if zig else 0, S, stream)
+        self.launches += 1
+        self.kernels += 1
+        return self.o, self.lse
+
+    # ----------------------------------------------------------- backward
+
+    def backward(self, do, q=None, k=None, v=None):
+        """Gradients (dq, dk, dv) fp32 natural order, for the inputs of the
+        last ``forward`` (whose permuted copies are reused); for the
+        contiguous layout q, k, v must be passed again."""
+        if not self.backward_enabled:
+            raise RuntimeError("plan built without backward=True")
+        self.launches = self.kernels = 0
+        stream = torch.cuda.current_stream(self.device).cuda_stream
+        zig = self.layout == "zigzag"
+        S, D, H, P, B = self.S, self.D, self.H, self.P, self.B
+        eb = self.eb
+        rows = B * H * S
+        capi.attn_bwd_delta(_ptr(self.o), _ptr(do), _DT[self.dtype], _ptr(self.delta), rows, D, stream)
+        self.launches += 1
+        self.kernels += 1
+        if zig:
+            self._permute(do, self.dop, D * eb, 0, stream)
+            self._permute(self.lse, self.lse_p, 4, 0, stream)
+            self._permute(self.delta, self.delta_p, 4, 0, stream)
+            qh, kh, vh, doh = self.qp, self.kp, self.vp, self.dop
+            lse_h, dl_h = self.lse_p, self.delta_p
+            dq, dk, dv = self.dq_p, self.dk_p, self.dv_p
+        else:
+            if q is None:
+                raise ValueError("contiguous layout: pass q, k, v to backward")
+            qh, kh, vh, doh = q, k, v, do
+            lse_h, dl_h = self.lse, self.delta
+            dq, dk, dv = self.dq, self.dk, self.dv
+        st_ptr = _ptr(self.status)
+
+        def step(t, kv_ptrs, kv_view):
+            items = []
+            for g in range(self.G):
+                for r in range(P):
+                    j = ring_block(r, t, P)
+                    hoff = g * self.Hg * S
+                    qo, ko = hoff + r * self.n_r, hoff + j * self.n_r
+                    it = capi.sca_bwd_item()
+                    it.q = _ptr(qh) + qo * D * eb
+                    it.dout = _ptr(doh) + qo * D * eb
+                    it.k, it.v = kv_ptrs(g, r)
+                    it.lse = _ptr(lse_h) + qo * 4
+                    it.delta = _ptr(dl_h) + qo * 4
+                    it.dq = _ptr(dq) + qo * D * 4
+                    it.dk = _ptr(dk) + ko * D * 4
+                    it.dv = _ptr(dv) + ko * D * 4
+                    it.q_pos = shard_segs(S, P, self.layout, r)
+                    it.kv_pos = shard_segs(S, P, self.layout, j)
+                    items.append(it)
+            capi.attn_bwd_shard(items, self._dims(kv_view, backward=True, accumulate=1 if t > 0 else 0),
+                                st_ptr, stream)
+            self.launches += 1
+            self.kernels += self.kernels_per_attn_call("bwd")
+
+        self._ring(kh, vh, step)
+        if zig:
+            self._permute(dq, self.dq, D * 4, 1, stream)
+            self._permute(dk, self.dk, D * 4, 1, stream)
+            self._permute(dv, self.dv, D * 4, 1, stream)
+        return self.dq, self.dk, self.dv
+
+    def read_status(self) -> int:
+        """Synchronise and return the device status word (0 = OK)."""
+        return capi.sca_read_status(_ptr(self.status), torch.cuda.current_stream(self.device).cuda_stream)
+
+    def _check_inputs(self, *ts):
+        for t in ts:
+            if t.dtype != self.dtype or t.device != self.device or not t.is_contiguous() or \
+                    tuple(t.shape) != (self.B, self.H, self.S, self.D):
+                raise ValueError(f"expected contiguous {self.dtype} [{self.B},{self.H},{self.S},{self.D}] "
+                                 f"on {self.device}, got {t.dtype} {tuple(t.shape)} on {t.device}")
