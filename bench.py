@@ -237,17 +237,12 @@ def run_gpu(args):
     step_flops = flops(w)
     value = step_flops * args.steps * ws / (ms_max * 1e-3) / 1e12
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers: every step copies
+    # its inputs from pinned host memory and reads all results back
     pinned = [x.pin_memory() for x in inputs]
-    outs_host = None
     h2d = sum(x.numel() * x.element_size() for x in pinned)
-    barrier(ws)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    e2e_steps = max(1, min(args.steps, 5))
-    for _ in range(e2e_steps):
+
+    def e2e_step(outs_host):
         for d, h in zip(dev_in, pinned):
             d.copy_(h, non_blocking=True)
         o, lse = plan.forward(*dev_in[:3])
@@ -258,6 +253,17 @@ def run_gpu(args):
             outs_host = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in res]
         for hst, r in zip(outs_host, res):
             hst.copy_(r, non_blocking=True)
+        return outs_host
+
+    outs_host = e2e_step(None)   # untimed: allocates the pinned result buffers
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    e2e_steps = max(1, min(args.steps, 5))
+    for _ in range(e2e_steps):
+        e2e_step(outs_host)
     e1.record(stream)
     torch.cuda.synchronize()
     d2h = sum(x.numel() * x.element_size() for x in outs_host)

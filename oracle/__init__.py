@@ -31,7 +31,7 @@ What it computes, and where that comes from:
 
 Everything is float64 numpy; matmul is the only library primitive used.
 """
-from .attention import (attention, attention_rows, attention_backward,
+from .attention import (attention, attention_rows, attention_backward, attention_backward_block,
                         backward_query_rows, backward_key_columns, merge_lse,
                         softmax_matrix)
 from .shards import (chunk_len, zigzag_order, contiguous_order, shard_order,
@@ -40,7 +40,8 @@ from .shards import (chunk_len, zigzag_order, contiguous_order, shard_order,
                      visible_pairs)
 
 __all__ = [
-    "attention", "attention_rows", "attention_backward", "backward_query_rows",
+    "attention", "attention_rows", "attention_backward", "attention_backward_block",
+    "backward_query_rows",
     "backward_key_columns", "merge_lse", "softmax_matrix", "chunk_len",
     "zigzag_order", "contiguous_order", "shard_order", "shard_positions",
     "permute_rows", "ring_visit_order", "double_ring_visit_order",

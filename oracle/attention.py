@@ -240,3 +240,24 @@ def backward_key_columns(q, k, v, do, o, lse, scale, cols):
         dk[c] = scale * (ds @ q[i])
         dv[c] = p @ do[i]
     return dk, dv
+
+
+def attention_backward_block(q, k, v, do, lse, delta, scale, causal=True, q_pos=None, k_pos=None):
+    """Gradient contributions of one (query slab, key block) pair, float64.
+
+    With the FINAL lse_i and delta_i = dO_i . O_i of the query rows (over
+    the whole sequence), the pair contributes, over its visible (i, j):
+        P_ij = exp(s_ij - lse_i),  dS_ij = P_ij (dO_i . v_j - delta_i)
+        dq_i += scale sum_j dS_ij k_j,  dk_j += scale sum_i dS_ij q_i,
+        dv_j += sum_i P_ij dO_i
+    q, do: [Sq, D]; k, v: [Sk, D] (one head).  Summing the contributions of
+    every block of a partition gives the full gradients.
+    """
+    q, k, v, do, lse, delta = map(_f64, (q, k, v, do, lse, delta))
+    qp, kp = _positions(q_pos, q.shape[0]), _positions(k_pos, k.shape[0])
+    s = scale * (q @ k.T)
+    if causal:
+        s = np.where(kp[None, :] <= qp[:, None], s, NEG_INF)
+    p = _probs(s, lse)
+    ds = p * (do @ v.T - delta[:, None])
+    return scale * (ds @ k), scale * (ds.T @ q), p.T @ do

@@ -175,9 +175,10 @@ static int grid_for(int64_t work_items, int per_block) {
   return static_cast<int>(blocks < 1 ? 1 : blocks);
 }
 
-static bool overlap(const void* a, const void* b, int64_t bytes) {
+// Do [a, a + a_bytes) and [b, b + b_bytes) intersect?
+static bool overlap(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-  return x < y + bytes && y < x + bytes;
+  return x < y + static_cast<uintptr_t>(b_bytes) && y < x + static_cast<uintptr_t>(a_bytes);
 }
 
 }  // namespace sca
@@ -196,7 +197,7 @@ extern "C" int zigzag_permute(const void* src, void* dst, int64_t outer, int64_t
               static_cast<long long>(row_bytes));
   SCA_REQUIRE(aligned(src, 4) && aligned(dst, 4), SCA_ERR_ALIGN, "zigzag_permute: pointers not 4-byte aligned");
   const int64_t total = outer * S * row_bytes;
-  SCA_REQUIRE(!overlap(src, dst, total), SCA_ERR_ARG, "zigzag_permute: src and dst overlap");
+  SCA_REQUIRE(!overlap(src, total, dst, total), SCA_ERR_ARG, "zigzag_permute: src and dst overlap");
   if (total == 0) return SCA_OK;
   const int64_t chunk_bytes = (S / (2 * P)) * row_bytes;
   const int64_t nseg = outer * 2 * P;
@@ -252,8 +253,8 @@ extern "C" int attn_merge_lse(const float* o_parts, const float* lse_parts, int 
   if (unpermute_P > 0) {
     SCA_REQUIRE(S > 0 && S % (2 * unpermute_P) == 0 && rows % S == 0, SCA_ERR_ARG,
                 "attn_merge_lse: unpermute needs S %% 2P == 0 and rows %% S == 0");
-    SCA_REQUIRE(!overlap(o_parts, o_out, n * o_part_stride * 4) &&
-                    !overlap(lse_parts, lse_out, n * lse_part_stride * 4),
+    SCA_REQUIRE(!overlap(o_parts, (n - 1) * o_part_stride * 4 + rows * D * 4, o_out, rows * D * 4) &&
+                    !overlap(lse_parts, (n - 1) * lse_part_stride * 4 + rows * 4, lse_out, rows * 4),
                 SCA_ERR_ARG, "attn_merge_lse: outputs may not alias inputs when unpermuting");
   }
   if (rows == 0) return SCA_OK;

@@ -55,8 +55,11 @@ def test_backward_repeat_overwrites(sca):
     a = [t.clone() for t in plan.backward(do)]
     plan.forward(q, k, v)
     b = plan.backward(do)
-    for x, y in zip(a, b):
-        assert torch.equal(x, y)
+    # dK, dV: each key tile is owned by one CTA, summed over ring steps in a
+    # fixed order -> bitwise equal.  dQ may gather key tiles through fp32
+    # atomics, whose order varies -> equal up to rounding.
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    assert torch.allclose(a[0], b[0], rtol=0, atol=1e-5)
 
 
 def test_training_step_full_size_sampled(sca):

@@ -316,3 +316,25 @@ def test_sampled_rows_match_full():
                                                o[0, h], lse[0, h], 0.5, r)
         np.testing.assert_allclose(sdk, dk[0, h][r], atol=1e-12)
         np.testing.assert_allclose(sdv, dv[0, h][r], atol=1e-12)
+
+
+@pytest.mark.parametrize("layout,P", [("zigzag", 2), ("zigzag", 4), ("contiguous", 3)])
+def test_block_backward_contributions_sum_to_full(layout, P):
+    S, D = 48, 5
+    q, k, v, do = (RNG.standard_normal((S, D)) for _ in range(4))
+    o, lse = oracle.attention(q, k, v, 0.45)
+    delta = (do * o).sum(axis=1)
+    dq, dk, dv = np.zeros((S, D)), np.zeros((S, D)), np.zeros((S, D))
+    pos = oracle.shard_positions(S, P, layout)
+    for r in range(P):
+        for j in range(P):
+            gq, gk, gv = oracle.attention_backward_block(q[pos[r]], k[pos[j]], v[pos[j]], do[pos[r]],
+                                                         lse[pos[r]], delta[pos[r]], 0.45,
+                                                         q_pos=pos[r], k_pos=pos[j])
+            dq[pos[r]] += gq
+            dk[pos[j]] += gk
+            dv[pos[j]] += gv
+    fq, fk, fv = oracle.attention_backward(q, k, v, do, 0.45)
+    np.testing.assert_allclose(dq, fq, atol=1e-12)
+    np.testing.assert_allclose(dk, fk, atol=1e-12)
+    np.testing.assert_allclose(dv, fv, atol=1e-12)
