@@ -157,10 +157,11 @@ extern "C" int attn_bwd_shard(const sca_bwd_item* items, int n_items, const sca_
   if (rows == 0) return SCA_OK;
   cudaStream_t st = as_stream(stream);
   cudaError_t e;
-  if (dims->algo == SCA_ALGO_TC) {
+  if (use_tc(dims)) {
     e = tc_backward(a, st);
     if (e == cudaErrorNotSupported)
-      return fail(SCA_ERR_UNSUPPORTED, "attn_bwd_shard: tensor-core backward unavailable for this layout");
+      return fail(SCA_ERR_ALIGN, "attn_bwd_shard: layout not expressible as a TMA tensor map "
+                                 "(or dq rows not contiguous in overwrite mode)");
   } else {
     e = simt_backward(a, dims->dtype, st);
   }

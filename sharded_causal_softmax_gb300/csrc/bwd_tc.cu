@@ -1,9 +1,456 @@
-// Backward on the tensor cores: not built yet; attn_bwd_shard runs the
-// fp32-arithmetic kernels for every dtype until it is.
+// Backward of one (query shard, key block) item on the 5th-generation
+// tensor cores (sm_103a), recomputing P from the saved lse.
+//
+// One CTA owns a tile of 128 keys of one (item, batch, head), keeps dK and
+// dV for it in tensor memory, and walks the query tiles (128 rows) that can
+// see it.  Per query tile i (all products bf16 x bf16 -> fp32):
+//
+//   dP^T = V dO_i^T        S^T = K Q_i^T          (A = K/V, B = Q/dO; smem)
+//   P^T  = exp(scale S^T - lse_i),  dS^T = P^T (dP^T - delta_i)   (warps 0-7)
+//   dV  += P^T dO_i        dK  += dS^T Q_i         (A = P^T/dS^T in tmem)
+//   dQ_i = dS K            (A = dS from smem, written by warps 0-7)
+//   dq[rows of tile i] += scale * dQ_i             (fp32 vector atomics)
+//
+// Roles: warps 0-7 elementwise (two warpgroups; warpgroup g owns query
+// columns [64g, 64g+64), thread = key row = tensor-memory lane), then read
+// back dQ (thread = query row) and, at the end, dK / dV; warp 8 issues TMA
+// loads (K, V once; Q_i, dO_i double-buffered); warp 9 allocates tensor
+// memory and issues tcgen05.mma from one thread.
+//
+// Tensor memory (512 columns): S^T [0,128), dP^T [128,256), dV [256,256+D),
+// dK [256+D, 256+2D).  Warpgroup g writes its P^T (bf16, 32 columns) over the
+// S^T columns it has already read, [64g, 64g+32), and dS^T over
+// [128+64g, 128+64g+32); after the dV MMAs have read P^T the S^T region is
+// reused for dQ (D columns; MMAs execute in issue order).  dP^T of the next
+// tile is issued before the dQ read-back of the current one finishes; S^T
+// waits for it.
+//
+// Every wait is bounded (ptx.cuh); on expiry the CTA records
+// SCA_ERR_TIMEOUT, drains in-flight copies/MMAs (bounded), frees tensor
+// memory and returns.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "ptx.cuh"
 #include "simt_launch.h"
+#include "tmap.h"
 
 namespace sca {
+namespace bwdtc {
 
-cudaError_t tc_backward(AttnArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int BN = 128;           // keys per CTA
+constexpr int BM = 128;           // query rows per tile
+constexpr int PANEL = 128 * 128;  // bytes: 128 rows x 64 bf16, 128B swizzle
+constexpr int kThreads = 320;
+
+template <int D>
+struct Layout {
+  static constexpr int TILE = (D / 64) * PANEL;  // 128 rows x D bf16
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + TILE;
+  static constexpr int Q_OFF = V_OFF + TILE;          // 2 stages
+  static constexpr int DO_OFF = Q_OFF + 2 * TILE;     // 2 stages
+  static constexpr int DS_OFF = DO_OFF + 2 * TILE;    // dS^T: 128 keys x 128 queries bf16, 2 panels
+  static constexpr int BAR_OFF = DS_OFF + 2 * PANEL;
+  static constexpr int USED = BAR_OFF + 256;
+  static constexpr int SMEM = (USED + 1024 > 120 * 1024 ? USED + 1024 : 120 * 1024);
+};
+
+struct Bars {
+  uint64_t kv_full;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t sdp_full, p_ready, dq_full, tmem_free;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct TcArgs {
+  CUtensorMap maps[SCA_MAX_ITEMS][4];  // q, k, v, dO
+  AttnArgs a;
+};
+
+struct QTile {
+  int64_t q0;
+  int nq;
+  int64_t qmin, qmax;
+  bool visible, full;
+};
+
+SCA_INLINE QTile q_tile(const Item& it, int t, bool causal, int nk, int64_t kmin, int64_t kmax) {
+  QTile q;
+  q.q0 = static_cast<int64_t>(t) * BM;
+  q.nq = static_cast<int>(min64(BM, it.Sq - q.q0));
+  tile_pos_range(it.qs, q.q0, q.nq, q.qmin, q.qmax);
+  q.visible = !causal || kmin <= q.qmax;
+  q.full = q.nq == BM && nk == BN && (!causal || kmax <= q.qmin);
+  return q;
+}
+
+SCA_INLINE void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      SCA_I8(r, 0), SCA_I8(r, 8)
+      : "memory");
+}
+
+SCA_INLINE void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ TcArgs ta) {
+  using L = Layout<D>;
+  const AttnArgs& a = ta.a;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + L::BAR_OFF);
+
+  const int item_idx = blockIdx.z;
+  const Item& it = a.items[item_idx];
+  const int64_t k0 = static_cast<int64_t>(blockIdx.x) * BN;   // early keys (most queries) first
+  if (k0 >= it.Skv) return;
+  const int b = blockIdx.y / a.H, h = blockIdx.y % a.H;
+  const int nk = static_cast<int>(min64(BN, it.Skv - k0));
+  int64_t kmin, kmax;
+  tile_pos_range(it.ks, k0, nk, kmin, kmax);
+  const bool causal = a.causal != 0;
+  const int nqt = static_cast<int>((it.Sq + BM - 1) / BM);
+  int n_vis = 0;
+  for (int t = 0; t < nqt; ++t) n_vis += q_tile(it, t, causal, nk, kmin, kmax).visible ? 1 : 0;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* dk_base = it.dk + b * a.dkv.b + h * a.dkv.h;
+  float* dv_base = it.dv + b * a.dkv.b + h * a.dkv.h;
+
+  if (n_vis == 0) {
+    // no query sees these keys: overwrite mode still owes zeros
+    if (!a.accumulate && threadIdx.x < nk) {
+      float* pk = dk_base + (k0 + threadIdx.x) * a.dkv.s;
+      float* pv = dv_base + (k0 + threadIdx.x) * a.dkv.s;
+      for (int c = 0; c < D; c += 4) {
+        *reinterpret_cast<float4*>(pk + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(pv + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+    }
+    mbar_init(&bars->sdp_full, 1);
+    mbar_init(&bars->p_ready, 256);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->tmem_free, 256);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  volatile int* abort = &bars->abort;
+  int* status = a.status;
+  const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+
+  if (warp == 8) {
+    // ---------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const CUtensorMap* mq = &ta.maps[item_idx][0];
+      const CUtensorMap* mk = &ta.maps[item_idx][1];
+      const CUtensorMap* mv = &ta.maps[item_idx][2];
+      const CUtensorMap* mo = &ta.maps[item_idx][3];
+      tma_prefetch_map(mq);
+      tma_prefetch_map(mo);
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * L::TILE);
+      for (int p = 0; p < D / 64; ++p) {
+        tma_load_4d(smem + L::K_OFF + p * PANEL, mk, &bars->kv_full, 64 * p, static_cast<int>(k0), h, b);
+        tma_load_4d(smem + L::V_OFF + p * PANEL, mv, &bars->kv_full, 64 * p, static_cast<int>(k0), h, b);
+      }
+      int n = 0;
+      for (int t = 0; t < nqt; ++t) {
+        const QTile qt = q_tile(it, t, causal, nk, kmin, kmax);
+        if (!qt.visible) continue;
+        const int st = n & 1;
+        if (!mbar_wait(&bars->q_empty[st], ((n >> 1) & 1) ^ 1, abort, status)) break;
+        mbar_arrive_expect_tx(&bars->q_full[st], 2 * L::TILE);
+        for (int p = 0; p < D / 64; ++p) {
+          tma_load_4d(smem + L::Q_OFF + st * L::TILE + p * PANEL, mq, &bars->q_full[st], 64 * p,
+                      static_cast<int>(qt.q0), h, b);
+          tma_load_4d(smem + L::DO_OFF + st * L::TILE + p * PANEL, mo, &bars->q_full[st], 64 * p,
+                      static_cast<int>(qt.q0), h, b);
+        }
+        ++n;
+      }
+      if (*abort) {
+        mbar_wait_drain(&bars->kv_full, 0);
+        for (int j = (n > 2 ? n - 2 : 0); j < n; ++j) mbar_wait_drain(&bars->q_full[j & 1], (j >> 1) & 1);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_sdp = idesc_bf16_f32(BN, BM, false, false);   // M=keys, N=queries
+      constexpr uint32_t idesc_kv = idesc_bf16_f32(BN, D, false, true);      // dV, dK: M=keys, N=D
+      constexpr uint32_t idesc_dq = idesc_bf16_f32(BM, 64, true, true);      // dQ: M=queries, N=64
+      const uint32_t sK = smem_u32(smem + L::K_OFF), sV = smem_u32(smem + L::V_OFF);
+      const uint32_t sDS = smem_u32(smem + L::DS_OFF);
+      bool ok = mbar_wait(&bars->kv_full, 0, abort, status);
+      int n = 0;
+      for (int t = 0; ok && t < nqt; ++t) {
+        const QTile qt = q_tile(it, t, causal, nk, kmin, kmax);
+        if (!qt.visible) continue;
+        const int st = n & 1;
+        if (!mbar_wait(&bars->q_full[st], (n >> 1) & 1, abort, status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sQ = smem_u32(smem + L::Q_OFF + st * L::TILE);
+        const uint32_t sO = smem_u32(smem + L::DO_OFF + st * L::TILE);
+        // dP^T = V dO^T  (the dP^T columns are free: read by the previous tile's
+        // elementwise step, and its dS^T consumed by MMAs issued earlier)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;
+          umma_ss(tdP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sO + off, 16, 1024), idesc_sdp,
+                  kk > 0 ? 1u : 0u);
+        }
+        // S^T = K Q^T: the S^T columns hold the previous dQ until it is read back
+        if (n > 0 && !mbar_wait(&bars->tmem_free, (n - 1) & 1, abort, status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;
+          umma_ss(tS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idesc_sdp,
+                  kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars->sdp_full);
+        if (!mbar_wait(&bars->p_ready, n & 1, abort, status)) { ok = false; break; }
+        tc_fence_after();
+        // dV += P^T dO, dK += dS^T Q  (A from tensor memory; query K-step kk
+        // lives in warpgroup kk/4's packed columns)
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk) {
+          const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
+          const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
+          umma_ts(tdV, tS + acol, sdesc_sw128(sO + kk * 2048, PANEL, 1024), idesc_kv, acc);
+          umma_ts(tdK, tdP + acol, sdesc_sw128(sQ + kk * 2048, PANEL, 1024), idesc_kv, acc);
+        }
+        // dQ = dS K, in 64-column halves over the (now free) S^T columns
+#pragma unroll
+        for (int hh = 0; hh < D / 64; ++hh) {
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            umma_ss(tS + 64 * hh, sdesc_sw128(sDS + kk * 2048, PANEL, 1024),
+                    sdesc_sw128(sK + hh * PANEL + kk * 2048, PANEL, 1024), idesc_dq, kk > 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(&bars->q_empty[st]);
+        umma_commit(&bars->dq_full);
+        ++n;
+      }
+      if (!ok) {
+        umma_commit(&bars->drain);
+        mbar_wait_drain(&bars->drain, 0);
+      }
+    }
+  } else {
+    // ----------------------------------- elementwise + read-back (warps 0-7)
+    const int wg = warp >> 2;                 // query-column half
+    const int qw = warp & 3;                  // lane quadrant
+    const int row = qw * 32 + lane;           // key row (S^T) / query row (dQ)
+    const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
+    const bool krow_valid = row < nk;
+    const int64_t kpos = krow_valid ? seg_pos(it.ks, k0 + row) : INT64_MAX;
+    const float sl2 = a.scale_log2;
+    const float* lse_base = it.lse + b * a.lse_b + h * a.lse_h;
+    const float* dl_base = it.delta + b * a.lse_b + h * a.lse_h;
+    float* dq_base = it.o + b * a.o.b + h * a.o.h;
+    uint8_t* sds = smem + L::DS_OFF + wg * PANEL + (row >> 3) * 1024 + (row & 7) * 128;
+    int n = 0;
+    bool ok = true;
+    for (int t = 0; t < nqt; ++t) {
+      const QTile qt = q_tile(it, t, causal, nk, kmin, kmax);
+      if (!qt.visible) continue;
+      bool w = mbar_wait(&bars->sdp_full, n & 1, abort, status);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = 64 * wg + 32 * c;    // first query column of this chunk
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tS + lane_off + col0, sr);
+        tmem_ld32(tdP + lane_off + col0, dr);
+        // lse (as log2) and delta of the chunk's 32 query rows
+        float l2[32], dl[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int qi = col0 + i;
+          const bool ok_q = qi < qt.nq;
+          const float lse = ok_q ? lse_base[qt.q0 + qi] : -INFINITY;
+          l2[i] = lse * kLog2e;
+          dl[i] = ok_q ? dl_base[qt.q0 + qi] : 0.f;
+        }
+        tmem_wait_ld32(sr);
+        tmem_wait_ld32(dr);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float p2[2], d2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int qi = col0 + i + u;
+            bool vis = l2[i + u] != -INFINITY;
+            if (!qt.full)
+              vis = vis && krow_valid && qi < qt.nq && (!causal || kpos <= seg_pos(it.qs, qt.q0 + qi));
+            const float s = __uint_as_float(sr[i + u]);
+            const float p = vis ? ex2(fmaf(s, sl2, -l2[i + u])) : 0.f;
+            p2[u] = p;
+            d2[u] = p * (__uint_as_float(dr[i + u]) - dl[i + u]);
+          }
+          pk[i >> 1] = pack_bf16x2(p2[0], p2[1]);
+          dk[i >> 1] = pack_bf16x2(d2[0], d2[1]);
+        }
+        // P^T / dS^T over columns this thread has already read
+        tmem_st16(tS + lane_off + 64 * wg + 16 * c, pk);
+        tmem_st16(tdP + lane_off + 64 * wg + 16 * c, dk);
+        // dS^T row into shared memory (MN-major, 128B swizzle): chunk j of
+        // 16 bytes holds queries 8j..8j+7 of this warpgroup's panel
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = 4 * c + u;
+          uint4 v = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+          *reinterpret_cast<uint4*>(sds + ((j ^ (row & 7)) << 4)) = v;
+        }
+      }
+      tmem_wait_st();
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p_ready);
+      // dQ read-back: thread = query row, warpgroup wg takes columns [wg*D/2, (wg+1)*D/2)
+      w = mbar_wait(&bars->dq_full, n & 1, abort, status);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      tc_fence_after();
+      {
+        const bool qrow_valid = row < qt.nq;
+        float* dq_row = dq_base + (qt.q0 + (qrow_valid ? row : 0)) * a.o.s;
+#pragma unroll
+        for (int c = 0; c < D / 2; c += 32) {
+          const int col = wg * (D / 2) + c;
+          uint32_t r[32];
+          tmem_ld32(tS + lane_off + col, r);
+          tmem_wait_ld32(r);
+          if (qrow_valid) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 v = make_float4(a.scale * __uint_as_float(r[i]), a.scale * __uint_as_float(r[i + 1]),
+                                           a.scale * __uint_as_float(r[i + 2]), a.scale * __uint_as_float(r[i + 3]));
+              atomicAdd(reinterpret_cast<float4*>(dq_row + col + i), v);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->tmem_free);
+      ++n;
+    }
+    // dK (warpgroup 0) and dV (warpgroup 1): thread = key row
+    if (__all_sync(0xffffffffu, ok) && n > 0) {
+      tc_fence_after();
+      const uint32_t src = (wg == 0 ? tdK : tdV) + lane_off;
+      float* dst = (wg == 0 ? dk_base : dv_base) + (k0 + (krow_valid ? row : 0)) * a.dkv.s;
+      const float mul = wg == 0 ? a.scale : 1.f;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(src + c, r);
+        tmem_wait_ld32(r);
+        if (krow_valid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            float4 v = make_float4(mul * __uint_as_float(r[i]), mul * __uint_as_float(r[i + 1]),
+                                   mul * __uint_as_float(r[i + 2]), mul * __uint_as_float(r[i + 3]));
+            float4* p = reinterpret_cast<float4*>(dst + c + i);
+            if (a.accumulate) {
+              const float4 o = *p;
+              v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+            }
+            *p = v;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+static cudaError_t launch(TcArgs& ta, cudaStream_t st) {
+  using L = Layout<D>;
+  static std::once_flag once[64];
+  static cudaError_t attr_err[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::call_once(once[dev & 63], [&] {
+    attr_err[dev & 63] = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+  });
+  if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
+  dim3 grid(ta.a.max_k_tiles, ta.a.B * ta.a.H, ta.a.n_items);
+  bwd_tc_kernel<D><<<grid, kThreads, L::SMEM, st>>>(ta);
+  return cudaGetLastError();
+}
+
+}  // namespace bwdtc
+
+cudaError_t tc_backward(AttnArgs& a, cudaStream_t st) {
+  using namespace bwdtc;
+  static TcArgs ta;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> g(mu);
+  int64_t mt = 0;
+  for (int i = 0; i < a.n_items; ++i) {
+    const Item& it = a.items[i];
+    const int64_t t = (it.Skv + BN - 1) / BN;
+    if (t > mt) mt = t;
+    cudaError_t e;
+    if ((e = make_tmap_bf16(&ta.maps[i][0], it.q, a.D, it.Sq, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&ta.maps[i][1], it.k, a.D, it.Skv, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&ta.maps[i][2], it.v, a.D, it.Skv, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&ta.maps[i][3], it.dout, a.D, it.Sq, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
+  }
+  // dq gathers contributions from every key tile through atomics: in
+  // overwrite mode it starts from zero
+  if (!a.accumulate) {
+    if (a.o.s != a.D) return cudaErrorNotSupported;
+    for (int i = 0; i < a.n_items; ++i) {
+      const Item& it = a.items[i];
+      if (it.Sq == 0) continue;
+      for (int bb = 0; bb < a.B; ++bb) {
+        const size_t width = static_cast<size_t>(it.Sq * a.D) * 4;
+        const size_t pitch = a.H > 1 ? static_cast<size_t>(a.o.h) * 4 : width;   // one head: pitch unused
+        if (pitch < width) return cudaErrorNotSupported;
+        cudaError_t e = cudaMemset2DAsync(it.o + bb * a.o.b, pitch, 0, width, static_cast<size_t>(a.H), st);
+        if (e != cudaSuccess) return e;
+      }
+    }
+  }
+  a.max_k_tiles = static_cast<int>(mt);
+  ta.a = a;
+  return a.D == 64 ? launch<64>(ta, st) : launch<128>(ta, st);
+}
 
 }  // namespace sca

@@ -133,9 +133,7 @@ class ShardedCausalAttention:
     # ------------------------------------------------- kernel descriptions
 
     def uses_tensor_cores(self, kind: str) -> bool:
-        if self.dtype != torch.bfloat16 or self.algo == capi.SCA_ALGO_SIMT:
-            return False
-        return kind == "fwd" or self.algo == capi.SCA_ALGO_TC
+        return self.dtype == torch.bfloat16 and self.algo != capi.SCA_ALGO_SIMT
 
     def kernel_name(self, kind: str) -> str:
         tc = self.uses_tensor_cores(kind)
