@@ -20,6 +20,7 @@ plain implementation), on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -175,6 +176,9 @@ def run_gpu(args):
         sca_build.build()
     barrier(ws)
     w = WORKLOADS[args.workload]
+    if args.heads:   # a smaller case of the same kernels, for profiler captures
+        w = dataclasses.replace(w, H=args.heads, head_groups=1 if args.heads % w.head_groups else w.head_groups,
+                                description=w.description + f" (profiling case: H={args.heads})")
     dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     inputs = seeded_inputs.workload_inputs(w)
     dev_in = [x.to(device) for x in inputs]
@@ -417,6 +421,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="train_s32k")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="override the head count (profiler captures of a smaller case; not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

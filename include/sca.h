@@ -191,6 +191,10 @@ typedef struct {
  * less and recomputing, "Avances en la capacitacion de LLMs de secuencia
  * larga", section "Escalabilidad y Gestion de Memoria".)
  * Items in one call must not share dq rows nor dk/dv rows.
+ * With bf16 inputs the tensor-core kernel computes S, dK and dQ as fp16
+ * products (Q and K are converted to fp16 inside the kernel, dS is rounded
+ * to fp16): |q| and |k| must stay below 65504.  dq is summed over key tiles
+ * with fp32 atomics, so it is reproducible only up to rounding order.
  * Errors as attn_fwd_shard. */
 int attn_bwd_shard(const sca_bwd_item* items, int n_items, const sca_attn_dims* dims,
                    int* dev_status, void* stream);

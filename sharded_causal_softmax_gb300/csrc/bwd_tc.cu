@@ -25,6 +25,13 @@
 // tile is issued before the dQ read-back of the current one finishes; S^T
 // waits for it.
 //
+// Precision: S^T, dK and dQ run as fp16 MMAs.  The elementwise warps convert
+// the K tile (once) and each Q tile in shared memory from bf16 to fp16 (exact
+// for |x| in [2^-14, 65504], so inputs must stay inside the fp16 range), and
+// dS is rounded to fp16 (2^-11 relative) instead of bf16 (2^-8): with few
+// visible keys a query's dQ is a short sum of large dS terms and bf16 dS
+// alone would cost more than 1e-2.  dP^T and dV stay bf16 (V, dO, P^T).
+//
 // Every wait is bounded (ptx.cuh); on expiry the CTA records
 // SCA_ERR_TIMEOUT, drains in-flight copies/MMAs (bounded), frees tensor
 // memory and returns.
@@ -62,6 +69,7 @@ struct Bars {
   uint64_t kv_full;
   uint64_t q_full[2], q_empty[2];
   uint64_t sdp_full, p_ready, dq_full, tmem_free;
+  uint64_t k_conv, q_conv;   // K / the current Q tile converted to fp16
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -147,6 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     mbar_init(&bars->p_ready, 256);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->tmem_free, 256);
+    mbar_init(&bars->k_conv, 256);
+    mbar_init(&bars->q_conv, 256);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -200,9 +210,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   } else if (warp == 9) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_sdp = idesc_bf16_f32(BN, BM, false, false);   // M=keys, N=queries
-      constexpr uint32_t idesc_kv = idesc_bf16_f32(BN, D, false, true);      // dV, dK: M=keys, N=D
-      constexpr uint32_t idesc_dq = idesc_bf16_f32(BM, 64, true, true);      // dQ: M=queries, N=64
+      constexpr uint32_t idesc_dp = idesc_bf16_f32(BN, BM, false, false);    // dP^T: M=keys, N=queries
+      constexpr uint32_t idesc_s = idesc_f16_f32(BN, BM, false, false);      // S^T (fp16 K, Q)
+      constexpr uint32_t idesc_dv = idesc_bf16_f32(BN, D, false, true);      // dV: M=keys, N=D
+      constexpr uint32_t idesc_dk = idesc_f16_f32(BN, D, false, true);       // dK (fp16 dS^T, Q)
+      constexpr uint32_t idesc_dq = idesc_f16_f32(BM, 64, true, true);       // dQ: M=queries, N=64
       const uint32_t sK = smem_u32(smem + L::K_OFF), sV = smem_u32(smem + L::V_OFF);
       const uint32_t sDS = smem_u32(smem + L::DS_OFF);
       bool ok = mbar_wait(&bars->kv_full, 0, abort, status);
@@ -220,16 +232,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;
-          umma_ss(tdP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sO + off, 16, 1024), idesc_sdp,
+          umma_ss(tdP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sO + off, 16, 1024), idesc_dp,
                   kk > 0 ? 1u : 0u);
         }
-        // S^T = K Q^T: the S^T columns hold the previous dQ until it is read back
+        // S^T = K Q^T: the S^T columns hold the previous dQ until it is read
+        // back; K and Q must have been converted to fp16
         if (n > 0 && !mbar_wait(&bars->tmem_free, (n - 1) & 1, abort, status)) { ok = false; break; }
+        if (n == 0 && !mbar_wait(&bars->k_conv, 0, abort, status)) { ok = false; break; }
+        if (!mbar_wait(&bars->q_conv, n & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;
-          umma_ss(tS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idesc_sdp,
+          umma_ss(tS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idesc_s,
                   kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars->sdp_full);
@@ -241,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         for (int kk = 0; kk < BM / 16; ++kk) {
           const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
           const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
-          umma_ts(tdV, tS + acol, sdesc_sw128(sO + kk * 2048, PANEL, 1024), idesc_kv, acc);
-          umma_ts(tdK, tdP + acol, sdesc_sw128(sQ + kk * 2048, PANEL, 1024), idesc_kv, acc);
+          umma_ts(tdV, tS + acol, sdesc_sw128(sO + kk * 2048, PANEL, 1024), idesc_dv, acc);
+          umma_ts(tdK, tdP + acol, sdesc_sw128(sQ + kk * 2048, PANEL, 1024), idesc_dk, acc);
         }
         // dQ = dS K, in 64-column halves over the (now free) S^T columns
 #pragma unroll
@@ -276,11 +291,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     float* dq_base = it.o + b * a.o.b + h * a.o.h;
     uint8_t* sds = smem + L::DS_OFF + wg * PANEL + (row >> 3) * 1024 + (row & 7) * 128;
     int n = 0;
-    bool ok = true;
-    for (int t = 0; t < nqt; ++t) {
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_full, 0, abort, status));
+    if (ok) {
+      smem_bf16_to_f16(smem + L::K_OFF, L::TILE, threadIdx.x, 256);
+      fence_async_smem();
+    }
+    mbar_arrive(&bars->k_conv);
+    for (int t = 0; ok && t < nqt; ++t) {
       const QTile qt = q_tile(it, t, causal, nk, kmin, kmax);
       if (!qt.visible) continue;
-      bool w = mbar_wait(&bars->sdp_full, n & 1, abort, status);
+      // this tile's Q to fp16 (the dP^T MMA, which needs no Q, runs meanwhile)
+      bool w = mbar_wait(&bars->q_full[n & 1], (n >> 1) & 1, abort, status);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      smem_bf16_to_f16(smem + L::Q_OFF + (n & 1) * L::TILE, L::TILE, threadIdx.x, 256);
+      fence_async_smem();
+      mbar_arrive(&bars->q_conv);
+      w = mbar_wait(&bars->sdp_full, n & 1, abort, status);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
@@ -317,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             d2[u] = p * (__uint_as_float(dr[i + u]) - dl[i + u]);
           }
           pk[i >> 1] = pack_bf16x2(p2[0], p2[1]);
-          dk[i >> 1] = pack_bf16x2(d2[0], d2[1]);
+          dk[i >> 1] = pack_f16x2(d2[0], d2[1]);
         }
         // P^T / dS^T over columns this thread has already read
         tmem_st16(tS + lane_off + 64 * wg + 16 * c, pk);

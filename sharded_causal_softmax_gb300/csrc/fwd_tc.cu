@@ -3,25 +3,26 @@
 // One CTA owns a tile of 128 query rows of one (item, batch, head) and walks
 // the item's visible key/value tiles of 128 rows:
 //
-//   warp 4      TMA producer for Q (once) and the K ring (3 stages)
-//   warp 6      TMA producer for the V ring (2 stages)
-//   warp 5      tensor-memory allocation, and one thread issuing tcgen05.mma:
-//                 S[n%2] = Q K_n^T           (A, B from shared memory)
-//                 O     += P_{n-1} V_{n-1}   (A = P from tensor memory)
-//   warps 0-3   softmax: thread t owns query row t (tensor-memory lane t),
-//               reads its S row, keeps the running max/sum in fp32, writes
-//               P (bf16) back over its S row and rescales O when the max
-//               grows by more than 2^8 (lazy rescale; exact after the final
-//               division); then the epilogue o = O / l, lse = m + ln l.
+//   warp 8      TMA producer for Q (once) and the K ring (3 stages)
+//   warp 10     TMA producer for the V ring (2 stages)
+//   warp 9      tensor-memory allocation, and one thread issuing tcgen05.mma:
+//                 S[n%3] = Q K_n^T           (A, B from shared memory)
+//                 O     += P_n V_n           (A = P from tensor memory)
+//               QK^T runs up to three tiles ahead of the softmax.
+//   warps 0-7   softmax, two warpgroups: warpgroup g owns columns
+//               [64g, 64g+64) of every S row, thread t of the warpgroup owns
+//               query row t (tensor-memory lane t).  The row maximum is
+//               combined across the two warpgroups through shared memory;
+//               each keeps its part of the running sum.  P (bf16) is written
+//               back over the S row; O is rescaled when the maximum grows by
+//               more than 2^8 (lazy rescale, exact after the final division).
+//               Epilogue: o = O / l, lse = m + ln l.
 //
-// S is double-buffered in tensor memory so QK^T of tile n+1 runs while the
-// softmax of tile n is computed; K/V stages mirror the ring step's double
-// buffer.  Tiles with no visible (query, key) pair are skipped; tiles that
-// may hold masked pairs or ragged rows are masked elementwise.
-//
-// Tensor memory: S0 cols [0,128), S1 [128,256), O [256, 256+D); 512 columns
-// allocated (one CTA per SM: shared memory use is above half the SM).
-// Every mbarrier wait is bounded (ptx.cuh); on expiry the CTA records
+// Tensor memory: S0, S1, S2 in columns [0,384), O in [384, 384+D); all 512
+// columns are allocated (one CTA per SM: shared memory use is above half
+// the SM).  Tiles with no visible (query, key) pair are skipped; tiles that
+// may hold masked pairs or ragged rows are masked elementwise.  Every
+// mbarrier wait is bounded (ptx.cuh); on expiry the CTA records
 // SCA_ERR_TIMEOUT, drains its in-flight copies and MMAs (bounded), frees
 // its tensor memory and exits.
 #include <cuda.h>
@@ -41,9 +42,26 @@ constexpr int BM = 128;        // query rows per CTA
 constexpr int BN = 128;        // keys per tile
 constexpr int KST = 3;         // K stages
 constexpr int VST = 2;         // V stages
+constexpr int SBUF = 3;        // S buffers in tensor memory
 constexpr int PANEL = 128 * 128;  // bytes of 128 rows x 64 bf16 (one 128B-swizzle panel column)
-constexpr int kThreads = 224;
+constexpr int kThreads = 352;  // 8 softmax warps + 3 role warps
+constexpr int kProdK = 8, kMma = 9, kProdV = 10;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (log2 units)
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[KST], k_empty[KST];
+  uint64_t v_full[VST], v_empty[VST];
+  uint64_t s_full[SBUF], p_full[SBUF];
+  uint64_t pv_done[2];   // PV_j completes phase j/2 of pv_done[j%2]
+  uint64_t red_full[2];  // both warpgroups published their row maxima (per tile parity)
+  uint64_t lsum_full;    // both warpgroups published their row sums
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  float red[2][2][BM];   // row-max exchange [tile parity][warpgroup][row]
+  float lsum[2][BM];     // final row sums of the two warpgroups
+};
 
 template <int D>
 struct Layout {
@@ -52,20 +70,9 @@ struct Layout {
   static constexpr int K_OFF = Q_OFF + TILE;
   static constexpr int V_OFF = K_OFF + KST * TILE;
   static constexpr int BAR_OFF = V_OFF + VST * TILE;
-  static constexpr int BAR_BYTES = 256;
-  static constexpr int USED = BAR_OFF + BAR_BYTES;
+  static constexpr int USED = BAR_OFF + static_cast<int>(sizeof(Bars));
   // keep one CTA per SM (tensor memory is allocated whole): above half the SM
   static constexpr int SMEM = (USED + 1024 > 120 * 1024 ? USED + 1024 : 120 * 1024);
-};
-
-struct Bars {
-  uint64_t q_full;
-  uint64_t k_full[KST], k_empty[KST];
-  uint64_t v_full[VST], v_empty[VST];
-  uint64_t s_full[2], p_full[2], pv_done[2];
-  uint64_t drain;
-  uint32_t tmem_base;
-  int abort;
 };
 
 struct TcArgs {
@@ -88,6 +95,12 @@ SCA_INLINE TileInfo tile_info(const Item& it, int kt, bool causal, int64_t qmin,
   t.visible = !causal || kmin <= qmax;
   t.full = t.nk == BN && (!causal || kmax <= qmin);
   return t;
+}
+
+// First visible key tile at or after kt (nkt if none).
+SCA_INLINE int next_visible(const Item& it, int kt, int nkt, bool causal, int64_t qmin, int64_t qmax) {
+  while (kt < nkt && !tile_info(it, kt, causal, qmin, qmax).visible) ++kt;
+  return kt;
 }
 
 template <int D>
@@ -115,12 +128,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (n_vis == 0) {
     // no visible key: the empty partial
-    if (warp < 4) {
-      const int row = threadIdx.x;
+    if (warp < 8) {
+      const int row = (warp & 3) * 32 + lane, g = warp >> 2;
       if (row < nq) {
-        float* op = it.o + b * a.o.b + h * a.o.h + (q0 + row) * a.o.s;
-        for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(op + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-        it.lse[b * a.lse_b + h * a.lse_h + q0 + row] = -INFINITY;
+        float* op = it.o + b * a.o.b + h * a.o.h + (q0 + row) * a.o.s + g * (D / 2);
+        for (int c = 0; c < D / 2; c += 4) *reinterpret_cast<float4*>(op + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (g == 0) it.lse[b * a.lse_b + h * a.lse_h + q0 + row] = -INFINITY;
       }
     }
     return;
@@ -136,16 +149,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < SBUF; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], BM);
-      mbar_init(&bars->pv_done[i], 1);
+      mbar_init(&bars->p_full[i], 2 * BM);
     }
+    mbar_init(&bars->pv_done[0], 1);
+    mbar_init(&bars->pv_done[1], 1);
+    mbar_init(&bars->red_full[0], 2 * BM);
+    mbar_init(&bars->red_full[1], 2 * BM);
+    mbar_init(&bars->lsum_full, 2 * BM);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMma) {
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
@@ -153,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  const uint32_t tO = tmem + SBUF * 128;
   volatile int* abort = &bars->abort;
   int* status = a.status;
 
@@ -160,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   const uint32_t sK = smem_u32(smem + L::K_OFF);
   const uint32_t sV = smem_u32(smem + L::V_OFF);
 
-  if (warp == 4) {
+  if (warp == kProdK) {
     // ------------------------------------------------ Q + K producer
     if (lane == 0) {
       const CUtensorMap* mq = &ta.maps[item_idx][0];
@@ -171,74 +189,50 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       for (int p = 0; p < D / 64; ++p)
         tma_load_4d(smem + L::Q_OFF + p * PANEL, mq, &bars->q_full, 64 * p, static_cast<int>(q0), h, b);
       int n = 0;
-      for (int kt = 0; kt < nkt; ++kt) {
-        const TileInfo ti = tile_info(it, kt, causal, qmin, qmax);
-        if (!ti.visible) continue;
+      for (int kt = next_visible(it, 0, nkt, causal, qmin, qmax); kt < nkt;
+           kt = next_visible(it, kt + 1, nkt, causal, qmin, qmax)) {
         const int st = n % KST;
         if (!mbar_wait(&bars->k_empty[st], ((n / KST) & 1) ^ 1, abort, status)) break;
         mbar_arrive_expect_tx(&bars->k_full[st], L::TILE);
         for (int p = 0; p < D / 64; ++p)
-          tma_load_4d(smem + L::K_OFF + st * L::TILE + p * PANEL, mk, &bars->k_full[st], 64 * p,
-                      static_cast<int>(ti.k0), h, b);
+          tma_load_4d(smem + L::K_OFF + st * L::TILE + p * PANEL, mk, &bars->k_full[st], 64 * p, kt * BN, h, b);
         ++n;
       }
       if (*abort) {  // let issued copies land before the CTA goes away
+        mbar_wait_drain(&bars->q_full, 0);
         for (int j = (n > KST ? n - KST : 0); j < n; ++j) mbar_wait_drain(&bars->k_full[j % KST], (j / KST) & 1);
       }
     }
-  } else if (warp == 6) {
+  } else if (warp == kProdV) {
     // ------------------------------------------------------ V producer
     if (lane == 0) {
       const CUtensorMap* mv = &ta.maps[item_idx][2];
       tma_prefetch_map(mv);
       int n = 0;
-      for (int kt = 0; kt < nkt; ++kt) {
-        const TileInfo ti = tile_info(it, kt, causal, qmin, qmax);
-        if (!ti.visible) continue;
+      for (int kt = next_visible(it, 0, nkt, causal, qmin, qmax); kt < nkt;
+           kt = next_visible(it, kt + 1, nkt, causal, qmin, qmax)) {
         const int st = n % VST;
         if (!mbar_wait(&bars->v_empty[st], ((n / VST) & 1) ^ 1, abort, status)) break;
         mbar_arrive_expect_tx(&bars->v_full[st], L::TILE);
         for (int p = 0; p < D / 64; ++p)
-          tma_load_4d(smem + L::V_OFF + st * L::TILE + p * PANEL, mv, &bars->v_full[st], 64 * p,
-                      static_cast<int>(ti.k0), h, b);
+          tma_load_4d(smem + L::V_OFF + st * L::TILE + p * PANEL, mv, &bars->v_full[st], 64 * p, kt * BN, h, b);
         ++n;
       }
       if (*abort) {
         for (int j = (n > VST ? n - VST : 0); j < n; ++j) mbar_wait_drain(&bars->v_full[j % VST], (j / VST) & 1);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMma) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
-      const uint32_t tO = tmem + 256;
       bool ok = mbar_wait(&bars->q_full, 0, abort, status);
-      auto issue_pv = [&](int j) -> bool {
-        const int vs = j % VST;
-        if (!mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, abort, status)) return false;
-        if (!mbar_wait(&bars->v_full[vs], (j / VST) & 1, abort, status)) return false;
+      auto issue_qk = [&](int j) -> bool {   // S[j%3] = Q K_j^T
+        const int ks = j % KST;
+        if (!mbar_wait(&bars->k_full[ks], (j / KST) & 1, abort, status)) return false;
         tc_fence_after();
-        const uint32_t tP = tmem + (j & 1) * 128;
-        const uint32_t vbase = sV + vs * L::TILE;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // B = V tile, MN-major: 64-column panels LBO apart, 8-key groups 1024 B apart
-          const uint64_t bdesc = sdesc_sw128(vbase + kk * 2048, PANEL, 1024);
-          umma_ts(tO, tP + kk * 8, bdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&bars->v_empty[vs]);
-        umma_commit(&bars->pv_done[j & 1]);
-        return true;
-      };
-      int n = 0;
-      for (int kt = 0; ok && kt < nkt; ++kt) {
-        const TileInfo ti = tile_info(it, kt, causal, qmin, qmax);
-        if (!ti.visible) continue;
-        const int ks = n % KST;
-        if (!mbar_wait(&bars->k_full[ks], (n / KST) & 1, abort, status)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t tS = tmem + (n & 1) * 128;
+        const uint32_t tS = tmem + (j % SBUF) * 128;
         const uint32_t kbase = sK + ks * L::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -246,56 +240,85 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           umma_ss(tS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), idesc_qk,
                   kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars->s_full[n & 1]);
+        umma_commit(&bars->s_full[j % SBUF]);
         umma_commit(&bars->k_empty[ks]);
-        if (n > 0 && !issue_pv(n - 1)) { ok = false; break; }
-        ++n;
+        return true;
+      };
+      for (int j = 0; ok && j < n_vis && j < SBUF; ++j) ok = issue_qk(j);
+      for (int j = 0; ok && j < n_vis; ++j) {
+        // O += P_j V_j  (B = V tile, MN-major: 64-column panels LBO apart, 8-key groups 1024 B apart)
+        const int vs = j % VST;
+        if (!mbar_wait(&bars->p_full[j % SBUF], (j / SBUF) & 1, abort, status)) { ok = false; break; }
+        if (!mbar_wait(&bars->v_full[vs], (j / VST) & 1, abort, status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tP = tmem + (j % SBUF) * 128;
+        const uint32_t vbase = sV + vs * L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_ts(tO, tP + kk * 8, sdesc_sw128(vbase + kk * 2048, PANEL, 1024), idesc_pv,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars->v_empty[vs]);
+        umma_commit(&bars->pv_done[j & 1]);
+        // S[j%3] is free once PV_j has read P_j (MMAs execute in order)
+        if (j + SBUF < n_vis) ok = issue_qk(j + SBUF);
       }
-      if (ok && n > 0) ok = issue_pv(n - 1);
       if (!ok) {  // make sure no MMA still writes tensor memory
         umma_commit(&bars->drain);
         mbar_wait_drain(&bars->drain, 0);
       }
     }
   } else {
-    // -------------------------------------------- softmax (warps 0..3)
-    const int row = threadIdx.x;  // == tensor-memory lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // -------------------------------------------- softmax (warps 0..7)
+    const int g = warp >> 2;                 // column half
+    const int qw = warp & 3;                 // lane quadrant
+    const int row = qw * 32 + lane;          // query row == tensor-memory lane
+    const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
     const bool row_valid = row < nq;
     const int64_t qpos = row_valid ? seg_pos(it.qs, q0 + row) : INT64_MIN;
     const float sl2 = a.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     int n = 0;
     bool ok = true;
-    for (int kt = 0; kt < nkt; ++kt) {
+    for (int kt = next_visible(it, 0, nkt, causal, qmin, qmax); kt < nkt;
+         kt = next_visible(it, kt + 1, nkt, causal, qmin, qmax)) {
       const TileInfo ti = tile_info(it, kt, causal, qmin, qmax);
-      if (!ti.visible) continue;
-      const int sb = n & 1;
-      bool w = n < 2 || mbar_wait(&bars->pv_done[sb], ((n - 2) >> 1) & 1, abort, status);
-      w = w && mbar_wait(&bars->s_full[sb], (n >> 1) & 1, abort, status);
+      const int sb = n % SBUF;
+      // observe PV_{n-2}: each pv_done barrier is then at most one phase ahead
+      // of the phase this thread waits for next (a parity wait needs that)
+      bool w = n < 2 || mbar_wait(&bars->pv_done[n & 1], ((n - 2) >> 1) & 1, abort, status);
+      w = w && mbar_wait(&bars->s_full[sb], (n / SBUF) & 1, abort, status);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sr[BN];
+      uint32_t sr[64];
       const uint32_t tS = tmem + lane_off + sb * 128;
-#pragma unroll
-      for (int c = 0; c < BN; c += 32) tmem_ld32(tS + c, sr + c);
-#pragma unroll
-      for (int c = 0; c < BN; c += 32) tmem_wait_ld32(sr + c);
+      tmem_ld32(tS + 64 * g, sr);
+      tmem_ld32(tS + 64 * g + 32, sr + 32);
+      tmem_wait_ld32(sr);
+      tmem_wait_ld32(sr + 32);
       float* s = reinterpret_cast<float*>(sr);
       if (!ti.full) {
 #pragma unroll
-        for (int c = 0; c < BN; ++c) {
+        for (int i = 0; i < 64; ++i) {
+          const int c = 64 * g + i;
           const bool vis = c < ti.nk && (!causal || seg_pos(it.ks, ti.k0 + c) <= qpos);
-          if (!vis) s[c] = -INFINITY;
+          if (!vis) s[i] = -INFINITY;
         }
       }
       float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-      for (int c = 4; c < BN; c += 4) {
+      for (int c = 4; c < 64; c += 4) {
         mx0 = fmaxf(mx0, s[c]); mx1 = fmaxf(mx1, s[c + 1]);
         mx2 = fmaxf(mx2, s[c + 2]); mx3 = fmaxf(mx3, s[c + 3]);
       }
-      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float mine = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      bars->red[n & 1][g][row] = mine;
+      // both halves have read their S columns: P may now overwrite them
+      tc_fence_before();
+      mbar_arrive(&bars->red_full[n & 1]);
+      w = mbar_wait(&bars->red_full[n & 1], (n >> 1) & 1, abort, status);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      tc_fence_after();
+      const float mt = fmaxf(mine, bars->red[n & 1][g ^ 1][row]) * sl2;
       const float m_new = fmaxf(m_used, mt);
       const bool need = m_new > m_used + kRescaleLog2;
       if (__any_sync(0xffffffffu, need)) {
@@ -306,51 +329,51 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           const bool w1 = mbar_wait(&bars->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort, status);
           if (!__all_sync(0xffffffffu, w1)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t tO = tmem + lane_off + 256;
 #pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
+          for (int c = 0; c < D / 2; c += 32) {
             uint32_t r[32];
-            tmem_ld32(tO + c, r);
+            const uint32_t ta_o = tO + lane_off + g * (D / 2) + c;
+            tmem_ld32(ta_o, r);
             tmem_wait_ld32(r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(tO + c, r);
+            tmem_st32(ta_o, r);
           }
         }
       }
       const float msub = (m_used == -INFINITY) ? 0.f : m_used;
       float sum0 = 0.f, sum1 = 0.f;
+      uint32_t pk[32];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = half * 64 + 2 * i;
-          const float p0 = ex2(fmaf(s[c], sl2, -msub));
-          const float p1 = ex2(fmaf(s[c + 1], sl2, -msub));
-          sum0 += p0;
-          sum1 += p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(tS + half * 32, pk);
+      for (int i = 0; i < 32; ++i) {
+        const float p0 = ex2(fmaf(s[2 * i], sl2, -msub));
+        const float p1 = ex2(fmaf(s[2 * i + 1], sl2, -msub));
+        sum0 += p0;
+        sum1 += p1;
+        pk[i] = pack_bf16x2(p0, p1);
       }
+      tmem_st32(tS + 32 * g, pk);
       l += sum0 + sum1;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[sb]);
       ++n;
     }
-    // epilogue
-    if (ok && n > 0) ok = mbar_wait(&bars->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort, status);
+    // epilogue: observe PV_{n-2}, then PV_{n-1}
+    if (ok && n >= 2) ok = mbar_wait(&bars->pv_done[n & 1], ((n - 2) >> 1) & 1, abort, status);
+    if (ok && n >= 1) ok = mbar_wait(&bars->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort, status);
+    bars->lsum[g][row] = l;
+    mbar_arrive(&bars->lsum_full);
+    if (ok) ok = mbar_wait(&bars->lsum_full, 0, abort, status);
+    const float l_tot = l + bars->lsum[g ^ 1][row];
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      float* op = it.o + b * a.o.b + h * a.o.h + (q0 + (row_valid ? row : 0)) * a.o.s;
-      const uint32_t tO = tmem + lane_off + 256;
+      const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+      float* op = it.o + b * a.o.b + h * a.o.h + (q0 + (row_valid ? row : 0)) * a.o.s + g * (D / 2);
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
+      for (int c = 0; c < D / 2; c += 32) {
         uint32_t r[32];
-        tmem_ld32(tO + c, r);
+        tmem_ld32(tO + lane_off + g * (D / 2) + c, r);
         tmem_wait_ld32(r);
         if (row_valid) {
 #pragma unroll
@@ -361,14 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           }
         }
       }
-      if (row_valid)
-        it.lse[b * a.lse_b + h * a.lse_h + q0 + row] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      if (row_valid && g == 0)
+        it.lse[b * a.lse_b + h * a.lse_h + q0 + row] = l_tot > 0.f ? (m_used + log2f(l_tot)) * kLn2 : -INFINITY;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -394,7 +417,7 @@ static cudaError_t launch(TcArgs& ta, cudaStream_t st) {
 
 cudaError_t tc_forward(AttnArgs& a, cudaStream_t st) {
   using namespace fwdtc;
-  static TcArgs ta;  // large; filled per call on the host (calls are host-serialised per thread)
+  static TcArgs ta;  // large; filled per call on the host (the launch copies it)
   static std::mutex mu;
   std::lock_guard<std::mutex> g(mu);
   int64_t mt = 0;

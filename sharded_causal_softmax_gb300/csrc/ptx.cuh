@@ -6,6 +6,7 @@
 
 #include <stdint.h>
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 
@@ -157,6 +158,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
+// Instruction descriptor, kind::f16 with fp16 A/B and fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4)                                  // D format: f32 (A, B format 0: f16)
+         | ((a_mn_major ? 1u : 0u) << 15)
+         | ((b_mn_major ? 1u : 0u) << 16)
+         | (static_cast<uint32_t>(N >> 3) << 17)
+         | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (the layout TMA writes
 // with CU_TENSOR_MAP_SWIZZLE_128B).  lbo/sbo in bytes.
 SCA_INLINE uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -217,6 +227,27 @@ SCA_INLINE float ex2(float x) {
 SCA_INLINE uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+SCA_INLINE uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// In-place bf16 -> fp16 conversion of `bytes` bytes of shared memory (a
+// multiple of 16) by `nthreads` cooperating threads.  Every bf16 value with
+// magnitude in [2^-14, 65504] converts exactly (fp16 has more mantissa bits);
+// smaller ones become fp16 subnormals, larger ones overflow.  The element
+// positions, and so any swizzled layout, are unchanged.
+SCA_INLINE void smem_bf16_to_f16(uint8_t* base, int bytes, int tid, int nthreads) {
+  for (int off = tid * 16; off < bytes; off += nthreads * 16) {
+    uint4 v = *reinterpret_cast<const uint4*>(base + off);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = pack_f16x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+    *reinterpret_cast<uint4*>(base + off) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
 }
 
 }  // namespace sca
