@@ -59,10 +59,15 @@ struct Layout {
   static constexpr int V_OFF = K_OFF + TILE;
   static constexpr int Q_OFF = V_OFF + TILE;          // 2 stages
   static constexpr int DO_OFF = Q_OFF + 2 * TILE;     // 2 stages
-  static constexpr int DS_OFF = DO_OFF + 2 * TILE;    // dS^T: 128 keys x 128 queries bf16, 2 panels
-  static constexpr int BAR_OFF = DS_OFF + 2 * PANEL;
+  static constexpr int DS_OFF = DO_OFF + 2 * TILE;    // dS^T: 128 keys x 128 queries, 2 panels
+  static constexpr int LSE_OFF = DS_OFF + 2 * PANEL;  // 2 stages x (lse*log2e, delta) x 128 rows, fp32
+  static constexpr int BAR_OFF = LSE_OFF + 2 * 2 * BM * 4;
   static constexpr int USED = BAR_OFF + 256;
-  static constexpr int SMEM = (USED + 1024 > 120 * 1024 ? USED + 1024 : 120 * 1024);
+  static constexpr int kMaxSmem = 232448;              // per-CTA limit (227 KB)
+  // room to align the base to 1024 B when it fits; otherwise the kernel
+  // checks at run time that the base is already aligned
+  static constexpr int SMEM = USED + 1024 <= kMaxSmem ? (USED + 1024 > 120 * 1024 ? USED + 1024 : 120 * 1024)
+                                                       : USED;
 };
 
 struct Bars {
@@ -112,8 +117,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   using L = Layout<D>;
   const AttnArgs& a = ta.a;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  if (pad + L::USED > L::SMEM) {   // 128B-swizzled tiles need a 1024-aligned base
+    if (threadIdx.x == 0) report(a.status, SCA_ERR_ALIGN);
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
   Bars* bars = reinterpret_cast<Bars*>(smem + L::BAR_OFF);
+  float* lse_sm = reinterpret_cast<float*>(smem + L::LSE_OFF);   // [stage][lse2 | delta][row]
 
   const int item_idx = blockIdx.z;
   const Item& it = a.items[item_idx];
@@ -148,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_full[i], 1 + 32);   // TMA transaction + the producer warp's lse/delta stores
       mbar_init(&bars->q_empty[i], 1);
     }
     mbar_init(&bars->sdp_full, 1);
@@ -174,12 +185,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
 
   if (warp == 8) {
-    // ---------------------------------------------------- TMA producer
+    // ------------------------------------ TMA producer (lane 0) + lse/delta
+    const CUtensorMap* mq = &ta.maps[item_idx][0];
+    const CUtensorMap* mo = &ta.maps[item_idx][3];
     if (lane == 0) {
-      const CUtensorMap* mq = &ta.maps[item_idx][0];
       const CUtensorMap* mk = &ta.maps[item_idx][1];
       const CUtensorMap* mv = &ta.maps[item_idx][2];
-      const CUtensorMap* mo = &ta.maps[item_idx][3];
       tma_prefetch_map(mq);
       tma_prefetch_map(mo);
       mbar_arrive_expect_tx(&bars->kv_full, 2 * L::TILE);
@@ -187,12 +198,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         tma_load_4d(smem + L::K_OFF + p * PANEL, mk, &bars->kv_full, 64 * p, static_cast<int>(k0), h, b);
         tma_load_4d(smem + L::V_OFF + p * PANEL, mv, &bars->kv_full, 64 * p, static_cast<int>(k0), h, b);
       }
-      int n = 0;
-      for (int t = 0; t < nqt; ++t) {
-        const QTile qt = q_tile(it, t, causal, nk, kmin, kmax);
-        if (!qt.visible) continue;
-        const int st = n & 1;
-        if (!mbar_wait(&bars->q_empty[st], ((n >> 1) & 1) ^ 1, abort, status)) break;
+    }
+    const float* lse_base = it.lse + b * a.lse_b + h * a.lse_h;
+    const float* dl_base = it.delta + b * a.lse_b + h * a.lse_h;
+    int n = 0;
+    for (int t = 0; t < nqt; ++t) {
+      const QTile qt = q_tile(it, t, causal, nk, kmin, kmax);
+      if (!qt.visible) continue;
+      const int st = n & 1;
+      // stage st is free once the MMAs of tile n-2 completed; its lse/delta
+      // were read by the elementwise warps before those MMAs were issued
+      const bool w = mbar_wait(&bars->q_empty[st], ((n >> 1) & 1) ^ 1, abort, status);
+      if (!__all_sync(0xffffffffu, w)) break;
+      if (lane == 0) {
         mbar_arrive_expect_tx(&bars->q_full[st], 2 * L::TILE);
         for (int p = 0; p < D / 64; ++p) {
           tma_load_4d(smem + L::Q_OFF + st * L::TILE + p * PANEL, mq, &bars->q_full[st], 64 * p,
@@ -200,12 +218,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           tma_load_4d(smem + L::DO_OFF + st * L::TILE + p * PANEL, mo, &bars->q_full[st], 64 * p,
                       static_cast<int>(qt.q0), h, b);
         }
-        ++n;
       }
-      if (*abort) {
-        mbar_wait_drain(&bars->kv_full, 0);
-        for (int j = (n > 2 ? n - 2 : 0); j < n; ++j) mbar_wait_drain(&bars->q_full[j & 1], (j >> 1) & 1);
+      float* l2s = lse_sm + st * 2 * BM;
+#pragma unroll
+      for (int k = 0; k < BM / 32; ++k) {
+        // -lse*log2(e), or -inf where P must be 0 (row past the slab, or a
+        // row that sees no key at all), so exp2(s*scale*log2e + it) is P
+        const int i = lane + 32 * k;
+        const bool ok_q = i < qt.nq;
+        const float lse = ok_q ? lse_base[qt.q0 + i] : -INFINITY;
+        l2s[i] = lse == -INFINITY ? -INFINITY : -lse * kLog2e;
+        l2s[BM + i] = ok_q ? dl_base[qt.q0 + i] : 0.f;
       }
+      mbar_arrive(&bars->q_full[st]);
+      ++n;
+    }
+    if (lane == 0 && *abort) {
+      mbar_wait_drain(&bars->kv_full, 0);
+      for (int j = (n > 2 ? n - 2 : 0); j < n; ++j) mbar_wait_drain(&bars->q_full[j & 1], (j >> 1) & 1);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------ MMA issuer
@@ -286,8 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const bool krow_valid = row < nk;
     const int64_t kpos = krow_valid ? seg_pos(it.ks, k0 + row) : INT64_MAX;
     const float sl2 = a.scale_log2;
-    const float* lse_base = it.lse + b * a.lse_b + h * a.lse_h;
-    const float* dl_base = it.delta + b * a.lse_b + h * a.lse_h;
     float* dq_base = it.o + b * a.o.b + h * a.o.h;
     uint8_t* sds = smem + L::DS_OFF + wg * PANEL + (row >> 3) * 1024 + (row & 7) * 128;
     int n = 0;
@@ -297,16 +325,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       fence_async_smem();
     }
     mbar_arrive(&bars->k_conv);
+    // Q of the j-th visible tile to fp16, once its TMA load has landed
+    auto convert_q = [&](int j) -> bool {
+      const bool w = __all_sync(0xffffffffu, mbar_wait(&bars->q_full[j & 1], (j >> 1) & 1, abort, status));
+      if (w) {
+        smem_bf16_to_f16(smem + L::Q_OFF + (j & 1) * L::TILE, L::TILE, threadIdx.x, 256);
+        fence_async_smem();
+      }
+      mbar_arrive(&bars->q_conv);
+      return w;
+    };
+    if (ok) ok = convert_q(0);
     for (int t = 0; ok && t < nqt; ++t) {
       const QTile qt = q_tile(it, t, causal, nk, kmin, kmax);
       if (!qt.visible) continue;
-      // this tile's Q to fp16 (the dP^T MMA, which needs no Q, runs meanwhile)
-      bool w = mbar_wait(&bars->q_full[n & 1], (n >> 1) & 1, abort, status);
-      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-      smem_bf16_to_f16(smem + L::Q_OFF + (n & 1) * L::TILE, L::TILE, threadIdx.x, 256);
-      fence_async_smem();
-      mbar_arrive(&bars->q_conv);
-      w = mbar_wait(&bars->sdp_full, n & 1, abort, status);
+      bool w = mbar_wait(&bars->sdp_full, n & 1, abort, status);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
@@ -315,35 +348,36 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         uint32_t sr[32], dr[32];
         tmem_ld32(tS + lane_off + col0, sr);
         tmem_ld32(tdP + lane_off + col0, dr);
-        // lse (as log2) and delta of the chunk's 32 query rows
-        float l2[32], dl[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int qi = col0 + i;
-          const bool ok_q = qi < qt.nq;
-          const float lse = ok_q ? lse_base[qt.q0 + qi] : -INFINITY;
-          l2[i] = lse * kLog2e;
-          dl[i] = ok_q ? dl_base[qt.q0 + qi] : 0.f;
-        }
+        // -lse*log2e and delta of the chunk's 32 query rows (staged by warp 8)
+        const float* nl2 = lse_sm + (n & 1) * 2 * BM + col0;
+        const float* dls = nl2 + BM;
         tmem_wait_ld32(sr);
         tmem_wait_ld32(dr);
         uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float p2[2], d2[2];
+        for (int i = 0; i < 32; i += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(nl2 + i);   // broadcast reads
+          const float4 d4 = *reinterpret_cast<const float4*>(dls + i);
+          const float2 lp[2] = {make_float2(l4.x, l4.y), make_float2(l4.z, l4.w)};
+          const float2 dp[2] = {make_float2(d4.x, d4.y), make_float2(d4.z, d4.w)};
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int qi = col0 + i + u;
-            bool vis = l2[i + u] != -INFINITY;
-            if (!qt.full)
-              vis = vis && krow_valid && qi < qt.nq && (!causal || kpos <= seg_pos(it.qs, qt.q0 + qi));
-            const float s = __uint_as_float(sr[i + u]);
-            const float p = vis ? ex2(fmaf(s, sl2, -l2[i + u])) : 0.f;
-            p2[u] = p;
-            d2[u] = p * (__uint_as_float(dr[i + u]) - dl[i + u]);
+            const int j = i + 2 * u;
+            // two columns at a time: x = s * scale * log2(e) - lse * log2(e)
+            const float2 x = ffma2(make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])),
+                                   make_float2(sl2, sl2), lp[u]);
+            float p0 = ex2(x.x), p1 = ex2(x.y);
+            if (!qt.full) {
+              const int q0c = col0 + j;
+              if (!(krow_valid && q0c < qt.nq && (!causal || kpos <= seg_pos(it.qs, qt.q0 + q0c)))) p0 = 0.f;
+              if (!(krow_valid && q0c + 1 < qt.nq && (!causal || kpos <= seg_pos(it.qs, qt.q0 + q0c + 1))))
+                p1 = 0.f;
+            }
+            const float2 pp = make_float2(p0, p1);
+            const float2 d = fmul2(pp, fsub2(make_float2(__uint_as_float(dr[j]), __uint_as_float(dr[j + 1])), dp[u]));
+            pk[j >> 1] = pack_bf16x2(p0, p1);
+            dk[j >> 1] = pack_f16x2(d.x, d.y);
           }
-          pk[i >> 1] = pack_bf16x2(p2[0], p2[1]);
-          dk[i >> 1] = pack_f16x2(d2[0], d2[1]);
         }
         // P^T / dS^T over columns this thread has already read
         tmem_st16(tS + lane_off + 64 * wg + 16 * c, pk);
@@ -361,31 +395,30 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->p_ready);
-      // dQ read-back: thread = query row, warpgroup wg takes columns [wg*D/2, (wg+1)*D/2)
+      // the next tile's Q conversion overlaps this tile's dV/dK/dQ MMAs
+      if (n + 1 < n_vis && !convert_q(n + 1)) { ok = false; break; }
+      // dQ read-back: thread = query row, warpgroup wg takes columns
+      // [wg*D/2, (wg+1)*D/2).  Tensor memory is released before the atomics
+      // are issued, so the next tile's S^T never waits on them.
       w = mbar_wait(&bars->dq_full, n & 1, abort, status);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
-      {
-        const bool qrow_valid = row < qt.nq;
-        float* dq_row = dq_base + (qt.q0 + (qrow_valid ? row : 0)) * a.o.s;
+      uint32_t r[D / 2];
 #pragma unroll
-        for (int c = 0; c < D / 2; c += 32) {
-          const int col = wg * (D / 2) + c;
-          uint32_t r[32];
-          tmem_ld32(tS + lane_off + col, r);
-          tmem_wait_ld32(r);
-          if (qrow_valid) {
+      for (int c = 0; c < D / 2; c += 32) tmem_ld32(tS + lane_off + wg * (D / 2) + c, r + c);
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const float4 v = make_float4(a.scale * __uint_as_float(r[i]), a.scale * __uint_as_float(r[i + 1]),
-                                           a.scale * __uint_as_float(r[i + 2]), a.scale * __uint_as_float(r[i + 3]));
-              atomicAdd(reinterpret_cast<float4*>(dq_row + col + i), v);
-            }
-          }
-        }
-      }
+      for (int c = 0; c < D / 2; c += 32) tmem_wait_ld32(r + c);
       tc_fence_before();
       mbar_arrive(&bars->tmem_free);
+      if (row < qt.nq) {
+        float* dq_row = dq_base + (qt.q0 + row) * a.o.s + wg * (D / 2);
+#pragma unroll
+        for (int i = 0; i < D / 2; i += 4) {
+          const float4 v = make_float4(a.scale * __uint_as_float(r[i]), a.scale * __uint_as_float(r[i + 1]),
+                                       a.scale * __uint_as_float(r[i + 2]), a.scale * __uint_as_float(r[i + 3]));
+          atomicAdd(reinterpret_cast<float4*>(dq_row + i), v);
+        }
+      }
       ++n;
     }
     // dK (warpgroup 0) and dV (warpgroup 1): thread = key row

@@ -342,18 +342,19 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         }
       }
       const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-      float sum0 = 0.f, sum1 = 0.f;
+      const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-msub, -msub);
+      float2 sum = make_float2(0.f, 0.f);
       uint32_t pk[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float p0 = ex2(fmaf(s[2 * i], sl2, -msub));
-        const float p1 = ex2(fmaf(s[2 * i + 1], sl2, -msub));
-        sum0 += p0;
-        sum1 += p1;
-        pk[i] = pack_bf16x2(p0, p1);
+        // two columns per packed instruction: p = 2^(s * scale * log2e - m)
+        const float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), sc2, nm2);
+        const float2 p = make_float2(ex2(x.x), ex2(x.y));
+        sum = fadd2(sum, p);
+        pk[i] = pack_bf16x2(p.x, p.y);
       }
       tmem_st32(tS + 32 * g, pk);
-      l += sum0 + sum1;
+      l += sum.x + sum.y;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[sb]);

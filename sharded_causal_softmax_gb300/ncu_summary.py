@@ -74,6 +74,48 @@ def counters(path: str) -> str:
     return "\n".join(out)
 
 
+def traffic(path: str, kernel: str, workload: str, scale: float, sources) -> dict:
+    """Record dram read+write bytes of the captured launch of `kernel`,
+    scaled by `scale` (units of the bench launch / units of the captured
+    launch), with a hash of the kernel's sources (the bench reports the
+    figure only while the sources are unchanged)."""
+    import hashlib
+    import json
+    import os
+    raw = subprocess.run(["ncu", "-i", path, "--page", "raw", "--csv"], capture_output=True, text=True).stdout
+    rows = list(csv.reader(io.StringIO(raw)))
+    hdr, units, vals = rows[0], rows[1], rows[2]
+    mult = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+
+    def get(name):
+        i = hdr.index(name)
+        return float(vals[i].replace(",", "")) * mult.get(units[i], 1)
+
+    bytes_ = get("dram__bytes_read.sum") + get("dram__bytes_write.sum")
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc")
+    h = hashlib.sha256()
+    for n in sources:
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(f.read())
+    rec = {"workload": workload, "dram_bytes_per_launch": bytes_ * scale, "captured_bytes": bytes_,
+           "scale": scale, "source_hash": h.hexdigest()[:16], "report": os.path.basename(path)}
+    out = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "profiles", "traffic.json")
+    data = {}
+    if os.path.exists(out):
+        with open(out) as f:
+            data = json.load(f)
+    data[kernel] = rec
+    with open(out, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+    return rec
+
+
 if __name__ == "__main__":
     what, path = sys.argv[1], sys.argv[2]
-    print(launches(path) if what == "launches" else counters(path))
+    if what == "launches":
+        print(launches(path))
+    elif what == "counters":
+        print(counters(path))
+    elif what == "traffic":
+        # traffic <report> <kernel> <workload> <scale> <source files...>
+        print(traffic(path, sys.argv[3], sys.argv[4], float(sys.argv[5]), sys.argv[6:]))
