@@ -75,13 +75,15 @@ struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t sdp_full, p_ready, dq_full, tmem_free;
   uint64_t k_conv, q_conv;   // K / the current Q tile converted to fp16
+  uint64_t stage_full[2];    // warpgroup g staged a dQ sub-tile in its dS panel
+  uint64_t stage_free[2];    // the TMA reduce of that sub-tile has read it
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 
 struct TcArgs {
-  CUtensorMap maps[SCA_MAX_ITEMS][4];  // q, k, v, dO
+  CUtensorMap maps[SCA_MAX_ITEMS][5];  // q, k, v, dO (bf16), dq (fp32, reduce-add target)
   AttnArgs a;
 };
 
@@ -168,6 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     mbar_init(&bars->tmem_free, 256);
     mbar_init(&bars->k_conv, 256);
     mbar_init(&bars->q_conv, 256);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->stage_full[i], 128);
+      mbar_init(&bars->stage_free[i], 1);
+    }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -244,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       constexpr uint32_t idesc_s = idesc_f16_f32(BN, BM, false, false);      // S^T (fp16 K, Q)
       constexpr uint32_t idesc_dv = idesc_bf16_f32(BN, D, false, true);      // dV: M=keys, N=D
       constexpr uint32_t idesc_dk = idesc_f16_f32(BN, D, false, true);       // dK (fp16 dS^T, Q)
-      constexpr uint32_t idesc_dq = idesc_f16_f32(BM, 64, true, true);       // dQ: M=queries, N=64
+      constexpr uint32_t idesc_dq = idesc_f16_f32(BM, D, true, true);        // dQ: M=queries, N=D
       const uint32_t sK = smem_u32(smem + L::K_OFF), sV = smem_u32(smem + L::V_OFF);
       const uint32_t sDS = smem_u32(smem + L::DS_OFF);
       bool ok = mbar_wait(&bars->kv_full, 0, abort, status);
@@ -289,14 +295,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           umma_ts(tdV, tS + acol, sdesc_sw128(sO + kk * 2048, PANEL, 1024), idesc_dv, acc);
           umma_ts(tdK, tdP + acol, sdesc_sw128(sQ + kk * 2048, PANEL, 1024), idesc_dk, acc);
         }
-        // dQ = dS K, in 64-column halves over the (now free) S^T columns
+        // dQ = dS K over the (now free) S^T columns, N = D: B = K tile,
+        // MN-major, its 64-column panels LBO apart
 #pragma unroll
-        for (int hh = 0; hh < D / 64; ++hh) {
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            umma_ss(tS + 64 * hh, sdesc_sw128(sDS + kk * 2048, PANEL, 1024),
-                    sdesc_sw128(sK + hh * PANEL + kk * 2048, PANEL, 1024), idesc_dq, kk > 0 ? 1u : 0u);
-          }
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          umma_ss(tS, sdesc_sw128(sDS + kk * 2048, PANEL, 1024), sdesc_sw128(sK + kk * 2048, PANEL, 1024), idesc_dq,
+                  kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars->q_empty[st]);
         umma_commit(&bars->dq_full);
@@ -316,9 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const bool krow_valid = row < nk;
     const int64_t kpos = krow_valid ? seg_pos(it.ks, k0 + row) : INT64_MAX;
     const float sl2 = a.scale_log2;
-    float* dq_base = it.o + b * a.o.b + h * a.o.h;
     uint8_t* sds = smem + L::DS_OFF + wg * PANEL + (row >> 3) * 1024 + (row & 7) * 128;
     int n = 0;
+    int s_cnt = 0;   // uses of this warpgroup's dQ staging buffer so far
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_full, 0, abort, status));
     if (ok) {
       smem_bf16_to_f16(smem + L::K_OFF, L::TILE, threadIdx.x, 256);
@@ -340,6 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       const QTile qt = q_tile(it, t, causal, nk, kmin, kmax);
       if (!qt.visible) continue;
       bool w = mbar_wait(&bars->sdp_full, n & 1, abort, status);
+      // this warpgroup's dS panel doubles as its dQ staging buffer: the last
+      // TMA reduce must have read it
+      if (w && s_cnt > 0) w = mbar_wait(&bars->stage_free[wg], (s_cnt - 1) & 1, abort, status);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
@@ -410,17 +417,40 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       for (int c = 0; c < D / 2; c += 32) tmem_wait_ld32(r + c);
       tc_fence_before();
       mbar_arrive(&bars->tmem_free);
-      if (row < qt.nq) {
-        float* dq_row = dq_base + (qt.q0 + row) * a.o.s + wg * (D / 2);
+      // dq += scale * dQ: 32-column sub-tiles staged (128B-swizzled, the
+      // layout the reduce's tensor map reads) in this warpgroup's dS panel,
+      // which the dQ MMA has finished with, and added by one TMA reduce each
+      uint8_t* stg = smem + L::DS_OFF + wg * PANEL + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-        for (int i = 0; i < D / 2; i += 4) {
-          const float4 v = make_float4(a.scale * __uint_as_float(r[i]), a.scale * __uint_as_float(r[i + 1]),
-                                       a.scale * __uint_as_float(r[i + 2]), a.scale * __uint_as_float(r[i + 3]));
-          atomicAdd(reinterpret_cast<float4*>(dq_row + i), v);
+      for (int sub = 0; sub < D / 64; ++sub) {
+        if (sub > 0) {
+          w = mbar_wait(&bars->stage_free[wg], (s_cnt - 1) & 1, abort, status);
+          if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t* x = r + 32 * sub + 4 * j;
+          const float4 v = make_float4(a.scale * __uint_as_float(x[0]), a.scale * __uint_as_float(x[1]),
+                                       a.scale * __uint_as_float(x[2]), a.scale * __uint_as_float(x[3]));
+          *reinterpret_cast<float4*>(stg + ((j ^ (row & 7)) << 4)) = v;
+        }
+        fence_async_smem();
+        mbar_arrive(&bars->stage_full[wg]);
+        if ((threadIdx.x & 127) == 0) {   // one thread per warpgroup drives the TMA
+          if (mbar_wait(&bars->stage_full[wg], s_cnt & 1, abort, status)) {
+            tma_reduce_add_4d(&ta.maps[item_idx][4], smem + L::DS_OFF + wg * PANEL, wg * (D / 2) + 32 * sub,
+                              static_cast<int>(qt.q0), h, b);
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(&bars->stage_free[wg]);
+        }
+        ++s_cnt;
       }
+      if (!ok) break;
       ++n;
     }
+    if ((threadIdx.x & 127) == 0) bulk_wait_all();   // every reduce has landed in dq
     // dK (warpgroup 0) and dV (warpgroup 1): thread = key row
     if (__all_sync(0xffffffffu, ok) && n > 0) {
       tc_fence_after();
@@ -490,6 +520,7 @@ cudaError_t tc_backward(AttnArgs& a, cudaStream_t st) {
     if ((e = make_tmap_bf16(&ta.maps[i][1], it.k, a.D, it.Skv, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16(&ta.maps[i][2], it.v, a.D, it.Skv, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16(&ta.maps[i][3], it.dout, a.D, it.Sq, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
+    if ((e = make_tmap_f32(&ta.maps[i][4], it.o, a.D, it.Sq, a.H, a.B, a.o, 32, BM)) != cudaSuccess) return e;
   }
   // dq gathers contributions from every key tile through atomics: in
   // overwrite mode it starts from zero

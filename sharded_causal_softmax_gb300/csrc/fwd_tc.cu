@@ -12,10 +12,13 @@
 //   warps 0-7   softmax, two warpgroups: warpgroup g owns columns
 //               [64g, 64g+64) of every S row, thread t of the warpgroup owns
 //               query row t (tensor-memory lane t).  The row maximum is
-//               combined across the two warpgroups through shared memory;
-//               each keeps its part of the running sum.  P (bf16) is written
-//               back over the S row; O is rescaled when the maximum grows by
-//               more than 2^8 (lazy rescale, exact after the final division).
+//               combined across the two warpgroups through shared memory
+//               while the exponentials are already computed against the
+//               current reference maximum (redone only when it moves); each
+//               warpgroup keeps its part of the running sum and writes its
+//               half of P (bf16) over its own S columns.  O is rescaled when
+//               the maximum grows by more than 2^8 (lazy rescale, exact
+//               after the final division).
 //               Epilogue: o = O / l, lse = m + ln l.
 //
 // Tensor memory: S0, S1, S2 in columns [0,384), O in [384, 384+D); all 512
@@ -253,9 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         tc_fence_after();
         const uint32_t tP = tmem + (j % SBUF) * 128;
         const uint32_t vbase = sV + vs * L::TILE;
+        // keys [16kk, 16kk+16) of P live in warpgroup kk/4's packed columns
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          umma_ts(tO, tP + kk * 8, sdesc_sw128(vbase + kk * 2048, PANEL, 1024), idesc_pv,
+          umma_ts(tO, tP + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_sw128(vbase + kk * 2048, PANEL, 1024), idesc_pv,
                   (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bars->v_empty[vs]);
         umma_commit(&bars->pv_done[j & 1]);
@@ -312,12 +316,29 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       }
       const float mine = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       bars->red[n & 1][g][row] = mine;
-      // both halves have read their S columns: P may now overwrite them
-      tc_fence_before();
       mbar_arrive(&bars->red_full[n & 1]);
+      // Optimistic exponentials against the current reference maximum while
+      // the other half's maximum arrives; redone only when the reference
+      // has to move (rare after the first tile).
+      const float2 sc2 = make_float2(sl2, sl2);
+      float2 sum = make_float2(0.f, 0.f);
+      uint32_t pk[32];
+      auto exps = [&](float m_ref) {
+        const float msub = (m_ref == -INFINITY) ? 0.f : m_ref;
+        const float2 nm2 = make_float2(-msub, -msub);
+        sum = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          // two columns per packed instruction: p = 2^(s * scale * log2e - m)
+          const float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), sc2, nm2);
+          const float2 p = make_float2(ex2(x.x), ex2(x.y));
+          sum = fadd2(sum, p);
+          pk[i] = pack_bf16x2(p.x, p.y);
+        }
+      };
+      exps(m_used);
       w = mbar_wait(&bars->red_full[n & 1], (n >> 1) & 1, abort, status);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-      tc_fence_after();
       const float mt = fmaxf(mine, bars->red[n & 1][g ^ 1][row]) * sl2;
       const float m_new = fmaxf(m_used, mt);
       const bool need = m_new > m_used + kRescaleLog2;
@@ -340,20 +361,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             tmem_st32(ta_o, r);
           }
         }
+        exps(m_used);   // against the moved reference
       }
-      const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-      const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-msub, -msub);
-      float2 sum = make_float2(0.f, 0.f);
-      uint32_t pk[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        // two columns per packed instruction: p = 2^(s * scale * log2e - m)
-        const float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), sc2, nm2);
-        const float2 p = make_float2(ex2(x.x), ex2(x.y));
-        sum = fadd2(sum, p);
-        pk[i] = pack_bf16x2(p.x, p.y);
-      }
-      tmem_st32(tS + 32 * g, pk);
+      // P (bf16) over this half's own S columns [64g, 64g+32): no other
+      // warpgroup reads them, so no ordering with the other half is needed
+      tmem_st32(tS + 64 * g, pk);
       l += sum.x + sum.y;
       tmem_wait_st();
       tc_fence_before();

@@ -100,6 +100,21 @@ SCA_INLINE void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, in
       : "memory");
 }
 
+// 4-D tiled reduce-add of a shared-memory box into global memory (fp32 add
+// per element, done by the TMA unit; rows outside the tensor are skipped).
+SCA_INLINE void tma_reduce_add_4d(const CUtensorMap* map, const void* src, int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4, %5}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+SCA_INLINE void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until every committed bulk operation of this thread has read its source
+SCA_INLINE void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// wait until every committed bulk operation of this thread has completed
+SCA_INLINE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ------------------------------------------------------------------ tcgen05
 
 SCA_INLINE void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {

@@ -20,12 +20,11 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, int D, int64_t rows, int H, int B,
-                           const View& v, int box_d, int box_rows) {
+static cudaError_t make_tmap(CUtensorMap* map, CUtensorMapDataType type, int64_t eb, const void* base, int D,
+                             int64_t rows, int H, int B, const View& v, int box_d, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   if (reinterpret_cast<uintptr_t>(base) % 16) return cudaErrorNotSupported;
-  const int64_t eb = 2;
   // strides of size-1 dimensions are never used; keep them legal
   int64_t ss = v.s, sh = v.h, sb = v.b;
   if (H == 1) sh = ss * (rows > 0 ? rows : 1);
@@ -38,10 +37,19 @@ cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, int D, int64_t ro
                            static_cast<cuuint64_t>(sb * eb)};
   cuuint32_t box[4] = {static_cast<cuuint32_t>(box_d), static_cast<cuuint32_t>(box_rows), 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(map, type, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorNotSupported;
+}
+
+cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, int D, int64_t rows, int H, int B,
+                           const View& v, int box_d, int box_rows) {
+  return make_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, D, rows, H, B, v, box_d, box_rows);
+}
+
+cudaError_t make_tmap_f32(CUtensorMap* map, const void* base, int D, int64_t rows, int H, int B,
+                          const View& v, int box_d, int box_rows) {
+  return make_tmap(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, D, rows, H, B, v, box_d, box_rows);
 }
 
 }  // namespace sca

@@ -16,4 +16,8 @@ namespace sca {
 cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, int D, int64_t rows, int H, int B,
                            const View& v, int box_d, int box_rows);
 
+// Same for fp32 tensors (box_d * 4 bytes must be 128 for the swizzle).
+cudaError_t make_tmap_f32(CUtensorMap* map, const void* base, int D, int64_t rows, int H, int B,
+                          const View& v, int box_d, int box_rows);
+
 }  // namespace sca
