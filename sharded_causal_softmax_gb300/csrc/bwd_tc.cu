@@ -104,14 +104,6 @@ SCA_INLINE QTile q_tile(const Item& it, int t, bool causal, int nk, int64_t kmin
   return q;
 }
 
-SCA_INLINE void tmem_st16(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      SCA_I8(r, 0), SCA_I8(r, 8)
-      : "memory");
-}
-
 SCA_INLINE void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 template <int D>

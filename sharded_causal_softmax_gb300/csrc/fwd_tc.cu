@@ -6,9 +6,11 @@
 //   warp 8      TMA producer for Q (once) and the K ring (3 stages)
 //   warp 10     TMA producer for the V ring (2 stages)
 //   warp 9      tensor-memory allocation, and one thread issuing tcgen05.mma:
-//                 S[n%3] = Q K_n^T           (A, B from shared memory)
+//                 S[n%2] = Q K_n^T           (A = Q from tensor memory)
 //                 O     += P_n V_n           (A = P from tensor memory)
-//               QK^T runs up to three tiles ahead of the softmax.
+//               QK^T runs up to two tiles ahead of the softmax.  Keeping Q
+//               in tensor memory halves the shared-memory operand traffic of
+//               QK^T, which bounds the MMA rate at N = 128.
 //   warps 0-7   softmax, two warpgroups: warpgroup g owns columns
 //               [64g, 64g+64) of every S row, thread t of the warpgroup owns
 //               query row t (tensor-memory lane t).  The row maximum is
@@ -21,8 +23,8 @@
 //               after the final division).
 //               Epilogue: o = O / l, lse = m + ln l.
 //
-// Tensor memory: S0, S1, S2 in columns [0,384), O in [384, 384+D); all 512
-// columns are allocated (one CTA per SM: shared memory use is above half
+// Tensor memory: S0, S1 in columns [0,256), O in [256, 256+D), Q in
+// [256+D, 256+D+D/2); all 512 columns are allocated (one CTA per SM: shared memory use is above half
 // the SM).  Tiles with no visible (query, key) pair are skipped; tiles that
 // may hold masked pairs or ragged rows are masked elementwise.  Every
 // mbarrier wait is bounded (ptx.cuh); on expiry the CTA records
@@ -45,7 +47,7 @@ constexpr int BM = 128;        // query rows per CTA
 constexpr int BN = 128;        // keys per tile
 constexpr int KST = 3;         // K stages
 constexpr int VST = 2;         // V stages
-constexpr int SBUF = 3;        // S buffers in tensor memory
+constexpr int SBUF = 2;        // S buffers in tensor memory
 constexpr int PANEL = 128 * 128;  // bytes of 128 rows x 64 bf16 (one 128B-swizzle panel column)
 constexpr int kThreads = 352;  // 8 softmax warps + 3 role warps
 constexpr int kProdK = 8, kMma = 9, kProdV = 10;
@@ -53,6 +55,7 @@ constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (log2 units)
 
 struct Bars {
   uint64_t q_full;
+  uint64_t q_tmem;       // Q copied into tensor memory by the softmax warps
   uint64_t k_full[KST], k_empty[KST];
   uint64_t v_full[VST], v_empty[VST];
   uint64_t s_full[SBUF], p_full[SBUF];
@@ -144,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_tmem, 2 * BM);
     for (int i = 0; i < KST; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
@@ -174,10 +178,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   const uint32_t tO = tmem + SBUF * 128;
+  const uint32_t tQ = tO + D;   // Q as the A operand of QK^T (bf16, 2 per column)
   volatile int* abort = &bars->abort;
   int* status = a.status;
 
-  const uint32_t sQ = smem_u32(smem + L::Q_OFF);
   const uint32_t sK = smem_u32(smem + L::K_OFF);
   const uint32_t sV = smem_u32(smem + L::V_OFF);
 
@@ -230,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
-      bool ok = mbar_wait(&bars->q_full, 0, abort, status);
-      auto issue_qk = [&](int j) -> bool {   // S[j%3] = Q K_j^T
+      bool ok = mbar_wait(&bars->q_tmem, 0, abort, status);
+      auto issue_qk = [&](int j) -> bool {   // S[j%2] = Q K_j^T, Q from tensor memory
         const int ks = j % KST;
         if (!mbar_wait(&bars->k_full[ks], (j / KST) & 1, abort, status)) return false;
         tc_fence_after();
@@ -240,8 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;   // K-major: panel, then 32 B steps
-          umma_ss(tS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), idesc_qk,
-                  kk > 0 ? 1u : 0u);
+          umma_ts(tS, tQ + kk * 8, sdesc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars->s_full[j % SBUF]);
         umma_commit(&bars->k_empty[ks]);
@@ -282,8 +285,27 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     const float sl2 = a.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     int n = 0;
-    bool ok = true;
-    for (int kt = next_visible(it, 0, nkt, causal, qmin, qmax); kt < nkt;
+    // Q into tensor memory (the A operand of QK^T, so the MMAs read only K
+    // from shared memory): warpgroup g copies dims [g*D/2, (g+1)*D/2) of its
+    // row out of the 128B-swizzled TMA panels, two bf16 per column.
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, abort, status));
+    if (ok) {
+      constexpr int W = D / 4;                 // 32-bit words per half row
+      uint32_t qr[W];
+#pragma unroll
+      for (int c = 0; c < W / 4; ++c) {        // 16-byte chunks of 8 dims
+        const int d0 = g * (D / 2) + 8 * c;
+        const uint8_t* src = smem + L::Q_OFF + (d0 / 64) * PANEL + (row >> 3) * 1024 + (row & 7) * 128;
+        const uint4 v = *reinterpret_cast<const uint4*>(src + ((((d0 % 64) / 8) ^ (row & 7)) << 4));
+        qr[4 * c] = v.x; qr[4 * c + 1] = v.y; qr[4 * c + 2] = v.z; qr[4 * c + 3] = v.w;
+      }
+      if constexpr (W == 32) tmem_st32(tQ + lane_off + g * (D / 4), qr);
+      else tmem_st16(tQ + lane_off + g * (D / 4), qr);
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    mbar_arrive(&bars->q_tmem);
+    for (int kt = next_visible(it, 0, nkt, causal, qmin, qmax); ok && kt < nkt;
          kt = next_visible(it, kt + 1, nkt, causal, qmin, qmax)) {
       const TileInfo ti = tile_info(it, kt, causal, qmin, qmax);
       const int sb = n % SBUF;

@@ -230,6 +230,14 @@ SCA_INLINE void tmem_st32(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
+SCA_INLINE void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      SCA_I8(r, 0), SCA_I8(r, 8)
+      : "memory");
+}
+
 SCA_INLINE void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 2^x on the SFU (hardware ex2.approx instruction).
