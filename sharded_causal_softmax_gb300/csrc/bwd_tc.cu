@@ -3,27 +3,30 @@
 //
 // One CTA owns a tile of 128 keys of one (item, batch, head), keeps dK and
 // dV for it in tensor memory, and walks the query tiles (128 rows) that can
-// see it.  Per query tile i (all products bf16 x bf16 -> fp32):
+// see it.  Per query tile i:
 //
-//   dP^T = V dO_i^T        S^T = K Q_i^T          (A = K/V, B = Q/dO; smem)
-//   P^T  = exp(scale S^T - lse_i),  dS^T = P^T (dP^T - delta_i)   (warps 0-7)
-//   dV  += P^T dO_i        dK  += dS^T Q_i         (A = P^T/dS^T in tmem)
-//   dQ_i = dS K            (A = dS from smem, written by warps 0-7)
-//   dq[rows of tile i] += scale * dQ_i             (fp32 vector atomics)
+//   S^T = K Q_i^T          dP^T = V dO_i^T        (A = K/V, B = Q/dO; smem)
+//   P^T = exp(scale S^T - lse_i)                   (warps 0-7, phase 1)
+//   dV += P^T dO_i                                 (A = P^T in tmem)
+//   dS^T = P^T (dP^T - delta_i)                    (warps 0-7, phase 2)
+//   dK += dS^T Q_i         dQ_i = dS K             (A = dS^T in tmem / dS in smem)
+//   dq[rows of tile i] += scale * dQ_i             (TMA reduce-add, fp32)
+//
+// The MMAs run in that order, so phase 1 overlaps dP^T, phase 2 overlaps
+// dV, and the next tile's S^T overlaps the read-back of dQ_i.
 //
 // Roles: warps 0-7 elementwise (two warpgroups; warpgroup g owns query
 // columns [64g, 64g+64), thread = key row = tensor-memory lane), then read
 // back dQ (thread = query row) and, at the end, dK / dV; warp 8 issues TMA
-// loads (K, V once; Q_i, dO_i double-buffered); warp 9 allocates tensor
-// memory and issues tcgen05.mma from one thread.
+// loads (K, V once; Q_i, dO_i double-buffered) and stages lse / delta; warp
+// 9 allocates tensor memory and issues tcgen05.mma from one thread.
 //
 // Tensor memory (512 columns): S^T [0,128), dP^T [128,256), dV [256,256+D),
 // dK [256+D, 256+2D).  Warpgroup g writes its P^T (bf16, 32 columns) over the
 // S^T columns it has already read, [64g, 64g+32), and dS^T over
-// [128+64g, 128+64g+32); after the dV MMAs have read P^T the S^T region is
-// reused for dQ (D columns; MMAs execute in issue order).  dP^T of the next
-// tile is issued before the dQ read-back of the current one finishes; S^T
-// waits for it.
+// [128+64g, 128+64g+32).  dQ_i (D columns) goes over the dP^T columns once
+// dK has read dS^T (MMAs execute in issue order); the next tile's dP^T waits
+// until dQ_i has been read back, its S^T only for dV to have read P^T.
 //
 // Precision: S^T, dK and dQ run as fp16 MMAs.  The elementwise warps convert
 // the K tile (once) and each Q tile in shared memory from bf16 to fp16 (exact
@@ -38,6 +41,7 @@
 #include <cuda.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -72,11 +76,12 @@ struct Layout {
 
 struct Bars {
   uint64_t kv_full;
-  uint64_t q_full[2], q_empty[2];
-  uint64_t sdp_full, p_ready, dq_full, tmem_free;
+  uint64_t q_full[2];
+  uint64_t dq_staged[2];     // dQ of the stage's tile written over its Q/dO for the reduce
+  uint64_t s_full, dp_full;   // S^T / dP^T of the current tile in tensor memory
+  uint64_t p_ready, ds_ready; // P^T / dS^T written by warps 0-7 (dS also to smem)
+  uint64_t dq_full, tmem_free;
   uint64_t k_conv, q_conv;   // K / the current Q tile converted to fp16
-  uint64_t stage_full[2];    // warpgroup g staged a dQ sub-tile in its dS panel
-  uint64_t stage_free[2];    // the TMA reduce of that sub-tile has read it
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -154,18 +159,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     mbar_init(&bars->kv_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->q_full[i], 1 + 32);   // TMA transaction + the producer warp's lse/delta stores
-      mbar_init(&bars->q_empty[i], 1);
+      mbar_init(&bars->dq_staged[i], 256);
     }
-    mbar_init(&bars->sdp_full, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_ready, 256);
+    mbar_init(&bars->ds_ready, 256);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->tmem_free, 256);
     mbar_init(&bars->k_conv, 256);
     mbar_init(&bars->q_conv, 256);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->stage_full[i], 128);
-      mbar_init(&bars->stage_free[i], 1);
-    }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -183,14 +186,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
 
   if (warp == 8) {
-    // ------------------------------------ TMA producer (lane 0) + lse/delta
+    // ---------------- TMA producer (lane 0), lse/delta staging, dq reduce-add
     const CUtensorMap* mq = &ta.maps[item_idx][0];
     const CUtensorMap* mo = &ta.maps[item_idx][3];
+    const CUtensorMap* mdq = &ta.maps[item_idx][4];
     if (lane == 0) {
       const CUtensorMap* mk = &ta.maps[item_idx][1];
       const CUtensorMap* mv = &ta.maps[item_idx][2];
       tma_prefetch_map(mq);
       tma_prefetch_map(mo);
+      tma_prefetch_map(mdq);
       mbar_arrive_expect_tx(&bars->kv_full, 2 * L::TILE);
       for (int p = 0; p < D / 64; ++p) {
         tma_load_4d(smem + L::K_OFF + p * PANEL, mk, &bars->kv_full, 64 * p, static_cast<int>(k0), h, b);
@@ -199,15 +204,36 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     }
     const float* lse_base = it.lse + b * a.lse_b + h * a.lse_h;
     const float* dl_base = it.delta + b * a.lse_b + h * a.lse_h;
+    int q0_st0 = 0, q0_st1 = 0;   // first query row of the tile each stage holds
+    // dq[rows of the j-th visible tile] += its staged dQ: D/32 boxes of 32
+    // fp32 columns, the first D/64 over the stage's Q tile, the rest over its dO
+    auto reduce_tile = [&](int j) -> bool {
+      const int sj = j & 1;
+      const bool w = __all_sync(0xffffffffu, mbar_wait(&bars->dq_staged[sj], (j >> 1) & 1, abort, status));
+      if (w && lane == 0) {
+#pragma unroll
+        for (int bx = 0; bx < D / 32; ++bx) {
+          const uint8_t* src = smem + (bx < D / 64 ? L::Q_OFF + bx * PANEL : L::DO_OFF + (bx - D / 64) * PANEL) +
+                               sj * L::TILE;
+          tma_reduce_add_4d(mdq, src, 32 * bx, sj ? q0_st1 : q0_st0, h, b);
+        }
+        bulk_commit();
+      }
+      return w;
+    };
     int n = 0;
+    bool ok = true;
     for (int t = 0; t < nqt; ++t) {
       const QTile qt = q_tile(it, t, causal, nk, kmin, kmax);
       if (!qt.visible) continue;
       const int st = n & 1;
-      // stage st is free once the MMAs of tile n-2 completed; its lse/delta
-      // were read by the elementwise warps before those MMAs were issued
-      const bool w = mbar_wait(&bars->q_empty[st], ((n >> 1) & 1) ^ 1, abort, status);
-      if (!__all_sync(0xffffffffu, w)) break;
+      // stage st is free once the reduce of tile n-2's dQ, staged over it,
+      // has read it; its lse/delta were read before that dQ was computed
+      if (n >= 2) {
+        if (!reduce_tile(n - 2)) { ok = false; break; }
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+      }
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars->q_full[st], 2 * L::TILE);
         for (int p = 0; p < D / 64; ++p) {
@@ -217,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                       static_cast<int>(qt.q0), h, b);
         }
       }
+      if (st) q0_st1 = static_cast<int>(qt.q0); else q0_st0 = static_cast<int>(qt.q0);
       float* l2s = lse_sm + st * 2 * BM;
 #pragma unroll
       for (int k = 0; k < BM / 32; ++k) {
@@ -231,9 +258,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       mbar_arrive(&bars->q_full[st]);
       ++n;
     }
-    if (lane == 0 && *abort) {
-      mbar_wait_drain(&bars->kv_full, 0);
-      for (int j = (n > 2 ? n - 2 : 0); j < n; ++j) mbar_wait_drain(&bars->q_full[j & 1], (j >> 1) & 1);
+    // the last two tiles' reduces
+    for (int j = (n > 2 ? n - 2 : 0); ok && j < n; ++j) ok = reduce_tile(j);
+    if (lane == 0) {
+      bulk_wait_all();   // every reduce has read shared memory and landed in dq
+      if (*abort) {
+        mbar_wait_drain(&bars->kv_full, 0);
+        for (int j = (n > 2 ? n - 2 : 0); j < n; ++j) mbar_wait_drain(&bars->q_full[j & 1], (j >> 1) & 1);
+      }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------ MMA issuer
@@ -255,17 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         tc_fence_after();
         const uint32_t sQ = smem_u32(smem + L::Q_OFF + st * L::TILE);
         const uint32_t sO = smem_u32(smem + L::DO_OFF + st * L::TILE);
-        // dP^T = V dO^T  (the dP^T columns are free: read by the previous tile's
-        // elementwise step, and its dS^T consumed by MMAs issued earlier)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;
-          umma_ss(tdP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sO + off, 16, 1024), idesc_dp,
-                  kk > 0 ? 1u : 0u);
-        }
-        // S^T = K Q^T: the S^T columns hold the previous dQ until it is read
-        // back; K and Q must have been converted to fp16
-        if (n > 0 && !mbar_wait(&bars->tmem_free, (n - 1) & 1, abort, status)) { ok = false; break; }
+        // S^T = K Q^T over the S^T columns (the previous dV has read P^T);
+        // K and Q must have been converted to fp16
         if (n == 0 && !mbar_wait(&bars->k_conv, 0, abort, status)) { ok = false; break; }
         if (!mbar_wait(&bars->q_conv, n & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
@@ -275,26 +298,41 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           umma_ss(tS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idesc_s,
                   kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars->sdp_full);
+        umma_commit(&bars->s_full);
+        // dP^T = V dO^T over the dP^T columns, which hold the previous dQ
+        // until it is read back
+        if (n > 0 && !mbar_wait(&bars->tmem_free, (n - 1) & 1, abort, status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;
+          umma_ss(tdP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sO + off, 16, 1024), idesc_dp,
+                  kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars->dp_full);
+        // dV += P^T dO  (A from tensor memory; query K-step kk lives in
+        // warpgroup kk/4's packed columns)
         if (!mbar_wait(&bars->p_ready, n & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
-        // dV += P^T dO, dK += dS^T Q  (A from tensor memory; query K-step kk
-        // lives in warpgroup kk/4's packed columns)
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk) {
           const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
-          const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
-          umma_ts(tdV, tS + acol, sdesc_sw128(sO + kk * 2048, PANEL, 1024), idesc_dv, acc);
-          umma_ts(tdK, tdP + acol, sdesc_sw128(sQ + kk * 2048, PANEL, 1024), idesc_dk, acc);
+          umma_ts(tdV, tS + acol, sdesc_sw128(sO + kk * 2048, PANEL, 1024), idesc_dv, (n > 0 || kk > 0) ? 1u : 0u);
         }
-        // dQ = dS K over the (now free) S^T columns, N = D: B = K tile,
-        // MN-major, its 64-column panels LBO apart
+        // dK += dS^T Q, then dQ = dS K over the dP^T columns, N = D: B = K
+        // tile, MN-major, its 64-column panels LBO apart
+        if (!mbar_wait(&bars->ds_ready, n & 1, abort, status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk) {
+          const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
+          umma_ts(tdK, tdP + acol, sdesc_sw128(sQ + kk * 2048, PANEL, 1024), idesc_dk, (n > 0 || kk > 0) ? 1u : 0u);
+        }
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          umma_ss(tS, sdesc_sw128(sDS + kk * 2048, PANEL, 1024), sdesc_sw128(sK + kk * 2048, PANEL, 1024), idesc_dq,
+          umma_ss(tdP, sdesc_sw128(sDS + kk * 2048, PANEL, 1024), sdesc_sw128(sK + kk * 2048, PANEL, 1024), idesc_dq,
                   kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars->q_empty[st]);
         umma_commit(&bars->dq_full);
         ++n;
       }
@@ -314,10 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const float sl2 = a.scale_log2;
     uint8_t* sds = smem + L::DS_OFF + wg * PANEL + (row >> 3) * 1024 + (row & 7) * 128;
     int n = 0;
-    int s_cnt = 0;   // uses of this warpgroup's dQ staging buffer so far
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_full, 0, abort, status));
     if (ok) {
-      smem_bf16_to_f16(smem + L::K_OFF, L::TILE, threadIdx.x, 256);
+      smem_bf16_to_f16<L::TILE, 256>(smem + L::K_OFF, threadIdx.x);
       fence_async_smem();
     }
     mbar_arrive(&bars->k_conv);
@@ -325,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     auto convert_q = [&](int j) -> bool {
       const bool w = __all_sync(0xffffffffu, mbar_wait(&bars->q_full[j & 1], (j >> 1) & 1, abort, status));
       if (w) {
-        smem_bf16_to_f16(smem + L::Q_OFF + (j & 1) * L::TILE, L::TILE, threadIdx.x, 256);
+        smem_bf16_to_f16<L::TILE, 256>(smem + L::Q_OFF + (j & 1) * L::TILE, threadIdx.x);
         fence_async_smem();
       }
       mbar_arrive(&bars->q_conv);
@@ -335,51 +372,89 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     for (int t = 0; ok && t < nqt; ++t) {
       const QTile qt = q_tile(it, t, causal, nk, kmin, kmax);
       if (!qt.visible) continue;
-      bool w = mbar_wait(&bars->sdp_full, n & 1, abort, status);
-      // this warpgroup's dS panel doubles as its dQ staging buffer: the last
-      // TMA reduce must have read it
-      if (w && s_cnt > 0) w = mbar_wait(&bars->stage_free[wg], (s_cnt - 1) & 1, abort, status);
+      // -lse*log2e and delta of this warpgroup's 64 query columns (staged by warp 8)
+      const float* nl2 = lse_sm + (n & 1) * 2 * BM + 64 * wg;
+      const float* dls = nl2 + BM;
+      // phase 1: P^T = exp2(s * scale * log2(e) - lse * log2(e)), kept in fp32
+      // for phase 2 and written to tensor memory as bf16 for the dV MMAs
+      bool w = mbar_wait(&bars->s_full, n & 1, abort, status);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
+      uint32_t pr[64];   // S^T, then P^T (fp32 bits)
+      tmem_ld32(tS + lane_off + 64 * wg, pr);
+      tmem_ld32(tS + lane_off + 64 * wg + 32, pr + 32);
+      // tiles that may hold masked pairs or ragged rows: bit j set when query
+      // column 64*wg + j is visible to this thread's key (rows past the slab
+      // already have lse = -inf, so P = 0 there)
+      uint64_t vis = ~0ull;
+      if (!qt.full) {
+        vis = 0;
 #pragma unroll 1
+        for (int j = 0; j < 64; ++j) {
+          const int qc = 64 * wg + j;
+          const bool v = krow_valid && qc < qt.nq && (!causal || kpos <= seg_pos(it.qs, qt.q0 + qc));
+          vis |= static_cast<uint64_t>(v) << j;
+        }
+      }
+      tmem_wait_ld32(pr);
+      tmem_wait_ld32(pr + 32);
+      auto exps = [&](auto masked) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(nl2 + 32 * c + i);   // broadcast reads
+            const float2 lp[2] = {make_float2(l4.x, l4.y), make_float2(l4.z, l4.w)};
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int j = 32 * c + i + 2 * u;
+              const float2 x = ffma2(make_float2(__uint_as_float(pr[j]), __uint_as_float(pr[j + 1])),
+                                     make_float2(sl2, sl2), lp[u]);
+              float p0 = ex2(x.x), p1 = ex2(x.y);
+              if (decltype(masked)::value) {
+                p0 = (vis >> j) & 1 ? p0 : 0.f;
+                p1 = (vis >> (j + 1)) & 1 ? p1 : 0.f;
+              }
+              pr[j] = __float_as_uint(p0);
+              pr[j + 1] = __float_as_uint(p1);
+              pk[(i + 2 * u) >> 1] = pack_bf16x2(p0, p1);
+            }
+          }
+          // over S^T columns this thread has already read
+          tmem_st16(tS + lane_off + 64 * wg + 16 * c, pk);
+        }
+      };
+      if (qt.full)
+        exps(std::false_type{});
+      else
+        exps(std::true_type{});
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_ready);
+      // phase 2: dS^T = P^T (dP^T - delta), fp16, to tensor memory (A of the
+      // dK MMAs) and to this warpgroup's dS panel (A of the dQ MMAs)
+      w = mbar_wait(&bars->dp_full, n & 1, abort, status);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
       for (int c = 0; c < 2; ++c) {
-        const int col0 = 64 * wg + 32 * c;    // first query column of this chunk
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tS + lane_off + col0, sr);
-        tmem_ld32(tdP + lane_off + col0, dr);
-        // -lse*log2e and delta of the chunk's 32 query rows (staged by warp 8)
-        const float* nl2 = lse_sm + (n & 1) * 2 * BM + col0;
-        const float* dls = nl2 + BM;
-        tmem_wait_ld32(sr);
+        uint32_t dr[32];
+        tmem_ld32(tdP + lane_off + 64 * wg + 32 * c, dr);
         tmem_wait_ld32(dr);
-        uint32_t pk[16], dk[16];
+        uint32_t dk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(nl2 + i);   // broadcast reads
-          const float4 d4 = *reinterpret_cast<const float4*>(dls + i);
-          const float2 lp[2] = {make_float2(l4.x, l4.y), make_float2(l4.z, l4.w)};
+          const float4 d4 = *reinterpret_cast<const float4*>(dls + 32 * c + i);
           const float2 dp[2] = {make_float2(d4.x, d4.y), make_float2(d4.z, d4.w)};
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int j = i + 2 * u;
-            // two columns at a time: x = s * scale * log2(e) - lse * log2(e)
-            const float2 x = ffma2(make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])),
-                                   make_float2(sl2, sl2), lp[u]);
-            float p0 = ex2(x.x), p1 = ex2(x.y);
-            if (!qt.full) {
-              const int q0c = col0 + j;
-              if (!(krow_valid && q0c < qt.nq && (!causal || kpos <= seg_pos(it.qs, qt.q0 + q0c)))) p0 = 0.f;
-              if (!(krow_valid && q0c + 1 < qt.nq && (!causal || kpos <= seg_pos(it.qs, qt.q0 + q0c + 1))))
-                p1 = 0.f;
-            }
-            const float2 pp = make_float2(p0, p1);
+            const float2 pp = make_float2(__uint_as_float(pr[32 * c + j]), __uint_as_float(pr[32 * c + j + 1]));
             const float2 d = fmul2(pp, fsub2(make_float2(__uint_as_float(dr[j]), __uint_as_float(dr[j + 1])), dp[u]));
-            pk[j >> 1] = pack_bf16x2(p0, p1);
             dk[j >> 1] = pack_f16x2(d.x, d.y);
           }
         }
-        // P^T / dS^T over columns this thread has already read
-        tmem_st16(tS + lane_off + 64 * wg + 16 * c, pk);
         tmem_st16(tdP + lane_off + 64 * wg + 16 * c, dk);
         // dS^T row into shared memory (MN-major, 128B swizzle): chunk j of
         // 16 bytes holds queries 8j..8j+7 of this warpgroup's panel
@@ -393,56 +468,40 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       tmem_wait_st();
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars->p_ready);
-      // the next tile's Q conversion overlaps this tile's dV/dK/dQ MMAs
+      mbar_arrive(&bars->ds_ready);
+      // the next tile's Q conversion overlaps this tile's dK/dQ MMAs
       if (n + 1 < n_vis && !convert_q(n + 1)) { ok = false; break; }
-      // dQ read-back: thread = query row, warpgroup wg takes columns
-      // [wg*D/2, (wg+1)*D/2).  Tensor memory is released before the atomics
-      // are issued, so the next tile's S^T never waits on them.
+      // dQ read-back from the dP^T columns: thread = query row, warpgroup wg
+      // takes columns [wg*D/2, (wg+1)*D/2).  Tensor memory is released before
+      // the reduces are issued, so the next tile's dP^T never waits on them.
       w = mbar_wait(&bars->dq_full, n & 1, abort, status);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
       uint32_t r[D / 2];
 #pragma unroll
-      for (int c = 0; c < D / 2; c += 32) tmem_ld32(tS + lane_off + wg * (D / 2) + c, r + c);
+      for (int c = 0; c < D / 2; c += 32) tmem_ld32(tdP + lane_off + wg * (D / 2) + c, r + c);
 #pragma unroll
       for (int c = 0; c < D / 2; c += 32) tmem_wait_ld32(r + c);
       tc_fence_before();
       mbar_arrive(&bars->tmem_free);
-      // dq += scale * dQ: 32-column sub-tiles staged (128B-swizzled, the
-      // layout the reduce's tensor map reads) in this warpgroup's dS panel,
-      // which the dQ MMA has finished with, and added by one TMA reduce each
-      uint8_t* stg = smem + L::DS_OFF + wg * PANEL + (row >> 3) * 1024 + (row & 7) * 128;
+      // scale * dQ staged for the producer's TMA reduce-add over this tile's
+      // Q (warpgroup 0) or dO (warpgroup 1) tile, free since the dQ MMA ran:
+      // 32-column boxes of 128 rows, 128B-swizzled like the reduce's map
+      uint8_t* stg = smem + (wg == 0 ? L::Q_OFF : L::DO_OFF) + (n & 1) * L::TILE + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
       for (int sub = 0; sub < D / 64; ++sub) {
-        if (sub > 0) {
-          w = mbar_wait(&bars->stage_free[wg], (s_cnt - 1) & 1, abort, status);
-          if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t* x = r + 32 * sub + 4 * j;
           const float4 v = make_float4(a.scale * __uint_as_float(x[0]), a.scale * __uint_as_float(x[1]),
                                        a.scale * __uint_as_float(x[2]), a.scale * __uint_as_float(x[3]));
-          *reinterpret_cast<float4*>(stg + ((j ^ (row & 7)) << 4)) = v;
+          *reinterpret_cast<float4*>(stg + sub * PANEL + ((j ^ (row & 7)) << 4)) = v;
         }
-        fence_async_smem();
-        mbar_arrive(&bars->stage_full[wg]);
-        if ((threadIdx.x & 127) == 0) {   // one thread per warpgroup drives the TMA
-          if (mbar_wait(&bars->stage_full[wg], s_cnt & 1, abort, status)) {
-            tma_reduce_add_4d(&ta.maps[item_idx][4], smem + L::DS_OFF + wg * PANEL, wg * (D / 2) + 32 * sub,
-                              static_cast<int>(qt.q0), h, b);
-            bulk_commit();
-            bulk_wait_read_all();
-          }
-          mbar_arrive(&bars->stage_free[wg]);
-        }
-        ++s_cnt;
       }
-      if (!ok) break;
+      fence_async_smem();
+      mbar_arrive(&bars->dq_staged[n & 1]);
       ++n;
     }
-    if ((threadIdx.x & 127) == 0) bulk_wait_all();   // every reduce has landed in dq
     // dK (warpgroup 0) and dV (warpgroup 1): thread = key row
     if (__all_sync(0xffffffffu, ok) && n > 0) {
       tc_fence_after();
