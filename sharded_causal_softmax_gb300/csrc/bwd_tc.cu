@@ -76,8 +76,11 @@ struct Layout {
 
 struct Bars {
   uint64_t kv_full;
-  uint64_t q_full[2];
-  uint64_t dq_staged[2];     // dQ of the stage's tile written over its Q/dO for the reduce
+  uint64_t q_full[2];        // Q tile landed, lse/delta staged
+  uint64_t do_full[2];       // dO tile landed
+  uint64_t q_empty[2];       // the MMAs of the stage's tile have completed
+  uint64_t dq_staged[2];     // dQ of the stage's tile staged (dS panels + its dO) for the reduce
+  uint64_t ds_free;          // the reduce has read the dQ half staged in the dS panels
   uint64_t s_full, dp_full;   // S^T / dP^T of the current tile in tensor memory
   uint64_t p_ready, ds_ready; // P^T / dS^T written by warps 0-7 (dS also to smem)
   uint64_t dq_full, tmem_free;
@@ -159,8 +162,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     mbar_init(&bars->kv_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->q_full[i], 1 + 32);   // TMA transaction + the producer warp's lse/delta stores
+      mbar_init(&bars->do_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
       mbar_init(&bars->dq_staged[i], 256);
     }
+    mbar_init(&bars->ds_free, 1);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_ready, 256);
@@ -205,19 +211,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const float* lse_base = it.lse + b * a.lse_b + h * a.lse_h;
     const float* dl_base = it.delta + b * a.lse_b + h * a.lse_h;
     int q0_st0 = 0, q0_st1 = 0;   // first query row of the tile each stage holds
-    // dq[rows of the j-th visible tile] += its staged dQ: D/32 boxes of 32
-    // fp32 columns, the first D/64 over the stage's Q tile, the rest over its dO
+    // dq[rows of the j-th visible tile] += its staged dQ, D/32 boxes of 32
+    // fp32 columns: the first D/64 (warpgroup 0's half) from the dS panels,
+    // the rest from the tile's dO stage.  Two bulk groups; once the first is
+    // read the dS panels are released.
     auto reduce_tile = [&](int j) -> bool {
       const int sj = j & 1;
       const bool w = __all_sync(0xffffffffu, mbar_wait(&bars->dq_staged[sj], (j >> 1) & 1, abort, status));
       if (w && lane == 0) {
+        const int row0 = sj ? q0_st1 : q0_st0;
 #pragma unroll
-        for (int bx = 0; bx < D / 32; ++bx) {
-          const uint8_t* src = smem + (bx < D / 64 ? L::Q_OFF + bx * PANEL : L::DO_OFF + (bx - D / 64) * PANEL) +
-                               sj * L::TILE;
-          tma_reduce_add_4d(mdq, src, 32 * bx, sj ? q0_st1 : q0_st0, h, b);
-        }
+        for (int bx = 0; bx < D / 64; ++bx) tma_reduce_add_4d(mdq, smem + L::DS_OFF + bx * PANEL, 32 * bx, row0, h, b);
         bulk_commit();
+#pragma unroll
+        for (int bx = 0; bx < D / 64; ++bx)
+          tma_reduce_add_4d(mdq, smem + L::DO_OFF + sj * L::TILE + bx * PANEL, D / 2 + 32 * bx, row0, h, b);
+        bulk_commit();
+        bulk_wait_read<1>();
+        mbar_arrive(&bars->ds_free);
       }
       return w;
     };
@@ -227,35 +238,50 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       const QTile qt = q_tile(it, t, causal, nk, kmin, kmax);
       if (!qt.visible) continue;
       const int st = n & 1;
-      // stage st is free once the reduce of tile n-2's dQ, staged over it,
-      // has read it; its lse/delta were read before that dQ was computed
-      if (n >= 2) {
-        if (!reduce_tile(n - 2)) { ok = false; break; }
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
+      // lse/delta of this tile into registers while the stage drains
+      float lse_r[BM / 32], dl_r[BM / 32];
+#pragma unroll
+      for (int k = 0; k < BM / 32; ++k) {
+        const int i = lane + 32 * k;
+        lse_r[k] = i < qt.nq ? lse_base[qt.q0 + i] : -INFINITY;
+        dl_r[k] = i < qt.nq ? dl_base[qt.q0 + i] : 0.f;
+      }
+      // Q stage st (and its lse/delta slot) is free once the MMAs of tile
+      // n-2 have completed
+      if (n >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bars->q_empty[st], ((n - 2) >> 1) & 1, abort, status))) {
+        ok = false;
+        break;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->q_full[st], 2 * L::TILE);
-        for (int p = 0; p < D / 64; ++p) {
+        mbar_arrive_expect_tx(&bars->q_full[st], L::TILE);
+        for (int p = 0; p < D / 64; ++p)
           tma_load_4d(smem + L::Q_OFF + st * L::TILE + p * PANEL, mq, &bars->q_full[st], 64 * p,
                       static_cast<int>(qt.q0), h, b);
-          tma_load_4d(smem + L::DO_OFF + st * L::TILE + p * PANEL, mo, &bars->q_full[st], 64 * p,
-                      static_cast<int>(qt.q0), h, b);
-        }
       }
-      if (st) q0_st1 = static_cast<int>(qt.q0); else q0_st0 = static_cast<int>(qt.q0);
       float* l2s = lse_sm + st * 2 * BM;
 #pragma unroll
       for (int k = 0; k < BM / 32; ++k) {
         // -lse*log2(e), or -inf where P must be 0 (row past the slab, or a
         // row that sees no key at all), so exp2(s*scale*log2e + it) is P
         const int i = lane + 32 * k;
-        const bool ok_q = i < qt.nq;
-        const float lse = ok_q ? lse_base[qt.q0 + i] : -INFINITY;
-        l2s[i] = lse == -INFINITY ? -INFINITY : -lse * kLog2e;
-        l2s[BM + i] = ok_q ? dl_base[qt.q0 + i] : 0.f;
+        l2s[i] = lse_r[k] == -INFINITY ? -INFINITY : -lse_r[k] * kLog2e;
+        l2s[BM + i] = dl_r[k];
       }
       mbar_arrive(&bars->q_full[st]);
+      // dO stage st still holds half of tile n-2's dQ until its reduce has
+      // read it
+      if (n >= 2) {
+        if (!reduce_tile(n - 2)) { ok = false; break; }
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+      }
+      if (st) q0_st1 = static_cast<int>(qt.q0); else q0_st0 = static_cast<int>(qt.q0);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->do_full[st], L::TILE);
+        for (int p = 0; p < D / 64; ++p)
+          tma_load_4d(smem + L::DO_OFF + st * L::TILE + p * PANEL, mo, &bars->do_full[st], 64 * p,
+                      static_cast<int>(qt.q0), h, b);
+      }
       ++n;
     }
     // the last two tiles' reduces
@@ -264,7 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       bulk_wait_all();   // every reduce has read shared memory and landed in dq
       if (*abort) {
         mbar_wait_drain(&bars->kv_full, 0);
-        for (int j = (n > 2 ? n - 2 : 0); j < n; ++j) mbar_wait_drain(&bars->q_full[j & 1], (j >> 1) & 1);
+        for (int j = (n > 2 ? n - 2 : 0); j < n; ++j) {
+          mbar_wait_drain(&bars->q_full[j & 1], (j >> 1) & 1);
+          mbar_wait_drain(&bars->do_full[j & 1], (j >> 1) & 1);
+        }
       }
     }
   } else if (warp == 9) {
@@ -302,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         // dP^T = V dO^T over the dP^T columns, which hold the previous dQ
         // until it is read back
         if (n > 0 && !mbar_wait(&bars->tmem_free, (n - 1) & 1, abort, status)) { ok = false; break; }
+        if (!mbar_wait(&bars->do_full[st], (n >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -333,6 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           umma_ss(tdP, sdesc_sw128(sDS + kk * 2048, PANEL, 1024), sdesc_sw128(sK + kk * 2048, PANEL, 1024), idesc_dq,
                   kk > 0 ? 1u : 0u);
         }
+        umma_commit(&bars->q_empty[st]);
         umma_commit(&bars->dq_full);
         ++n;
       }
@@ -434,7 +465,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       mbar_arrive(&bars->p_ready);
       // phase 2: dS^T = P^T (dP^T - delta), fp16, to tensor memory (A of the
       // dK MMAs) and to this warpgroup's dS panel (A of the dQ MMAs)
+      // the dS panels hold half of the previous tile's dQ until its reduce
+      // has read them
       w = mbar_wait(&bars->dp_full, n & 1, abort, status);
+      if (w && n > 0) w = mbar_wait(&bars->ds_free, (n - 1) & 1, abort, status);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
@@ -484,10 +518,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       for (int c = 0; c < D / 2; c += 32) tmem_wait_ld32(r + c);
       tc_fence_before();
       mbar_arrive(&bars->tmem_free);
-      // scale * dQ staged for the producer's TMA reduce-add over this tile's
-      // Q (warpgroup 0) or dO (warpgroup 1) tile, free since the dQ MMA ran:
-      // 32-column boxes of 128 rows, 128B-swizzled like the reduce's map
-      uint8_t* stg = smem + (wg == 0 ? L::Q_OFF : L::DO_OFF) + (n & 1) * L::TILE + (row >> 3) * 1024 + (row & 7) * 128;
+      // scale * dQ staged for the producer's TMA reduce-add over the dS panels
+      // (warpgroup 0) or this tile's dO (warpgroup 1), both free since the
+      // dQ MMA ran: 32-column boxes of 128 rows, 128B-swizzled like the
+      // reduce's map
+      uint8_t* stg = smem + (wg == 0 ? L::DS_OFF : L::DO_OFF + (n & 1) * L::TILE) + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
       for (int sub = 0; sub < D / 64; ++sub) {
 #pragma unroll

@@ -110,8 +110,10 @@ SCA_INLINE void tma_reduce_add_4d(const CUtensorMap* map, const void* src, int c
       : "memory");
 }
 SCA_INLINE void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// wait until every committed bulk operation of this thread has read its source
-SCA_INLINE void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// wait until at most N of this thread's committed bulk groups have not yet
+// read their source
+template <int N>
+SCA_INLINE void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 // wait until every committed bulk operation of this thread has completed
 SCA_INLINE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
