@@ -81,6 +81,7 @@ struct Bars {
   uint64_t q_empty[2];       // the MMAs of the stage's tile have completed
   uint64_t dq_staged[2];     // dQ of the stage's tile staged (dS panels + its dO) for the reduce
   uint64_t ds_free;          // the reduce has read the dQ half staged in the dS panels
+  uint64_t epi_staged[2];    // warpgroup g staged dK (g=0) / dV (g=1) for the final TMA write
   uint64_t s_full, dp_full;   // S^T / dP^T of the current tile in tensor memory
   uint64_t p_ready, ds_ready; // P^T / dS^T written by warps 0-7 (dS also to smem)
   uint64_t dq_full, tmem_free;
@@ -90,10 +91,16 @@ struct Bars {
   int abort;
 };
 
+// Items per launch: seven tensor maps per item must fit, with the rest of the
+// arguments, in the 32764 bytes of kernel parameters.
+constexpr int kItemsPerLaunch = 28;
+
 struct TcArgs {
-  CUtensorMap maps[SCA_MAX_ITEMS][5];  // q, k, v, dO (bf16), dq (fp32, reduce-add target)
+  // q, k, v, dO (bf16); dq, dk, dv (fp32, TMA reduce-add / store targets)
+  CUtensorMap maps[kItemsPerLaunch][7];
   AttnArgs a;
 };
+static_assert(sizeof(TcArgs) <= 32764, "kernel parameters");
 
 struct QTile {
   int64_t q0;
@@ -102,11 +109,11 @@ struct QTile {
   bool visible, full;
 };
 
-SCA_INLINE QTile q_tile(const Item& it, int t, bool causal, int nk, int64_t kmin, int64_t kmax) {
+SCA_INLINE QTile q_tile(const ItemGeom& g, int t, bool causal, int nk, int64_t kmin, int64_t kmax) {
   QTile q;
   q.q0 = static_cast<int64_t>(t) * BM;
-  q.nq = static_cast<int>(min64(BM, it.Sq - q.q0));
-  tile_pos_range(it.qs, q.q0, q.nq, q.qmin, q.qmax);
+  q.nq = static_cast<int>(min64(BM, g.Sq - q.q0));
+  tile_pos_range(g.qs, q.q0, q.nq, q.qmin, q.qmax);
   q.visible = !causal || kmin <= q.qmax;
   q.full = q.nq == BM && nk == BN && (!causal || kmax <= q.qmin);
   return q;
@@ -130,16 +137,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 
   const int item_idx = blockIdx.z;
   const Item& it = a.items[item_idx];
+  const ItemGeom gm = item_geom(it);
   const int64_t k0 = static_cast<int64_t>(blockIdx.x) * BN;   // early keys (most queries) first
-  if (k0 >= it.Skv) return;
+  if (k0 >= gm.Skv) return;
   const int b = blockIdx.y / a.H, h = blockIdx.y % a.H;
-  const int nk = static_cast<int>(min64(BN, it.Skv - k0));
+  const int nk = static_cast<int>(min64(BN, gm.Skv - k0));
   int64_t kmin, kmax;
-  tile_pos_range(it.ks, k0, nk, kmin, kmax);
+  tile_pos_range(gm.ks, k0, nk, kmin, kmax);
   const bool causal = a.causal != 0;
-  const int nqt = static_cast<int>((it.Sq + BM - 1) / BM);
+  const int nqt = static_cast<int>((gm.Sq + BM - 1) / BM);
   int n_vis = 0;
-  for (int t = 0; t < nqt; ++t) n_vis += q_tile(it, t, causal, nk, kmin, kmax).visible ? 1 : 0;
+  for (int t = 0; t < nqt; ++t) n_vis += q_tile(gm, t, causal, nk, kmin, kmax).visible ? 1 : 0;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* dk_base = it.dk + b * a.dkv.b + h * a.dkv.h;
@@ -167,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       mbar_init(&bars->dq_staged[i], 256);
     }
     mbar_init(&bars->ds_free, 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&bars->epi_staged[i], 128);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_ready, 256);
@@ -235,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     int n = 0;
     bool ok = true;
     for (int t = 0; t < nqt; ++t) {
-      const QTile qt = q_tile(it, t, causal, nk, kmin, kmax);
+      const QTile qt = q_tile(gm, t, causal, nk, kmin, kmax);
       if (!qt.visible) continue;
       const int st = n & 1;
       // lse/delta of this tile into registers while the stage drains
@@ -309,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       bool ok = mbar_wait(&bars->kv_full, 0, abort, status);
       int n = 0;
       for (int t = 0; ok && t < nqt; ++t) {
-        const QTile qt = q_tile(it, t, causal, nk, kmin, kmax);
+        const QTile qt = q_tile(gm, t, causal, nk, kmin, kmax);
         if (!qt.visible) continue;
         const int st = n & 1;
         if (!mbar_wait(&bars->q_full[st], (n >> 1) & 1, abort, status)) { ok = false; break; }
@@ -379,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const int row = qw * 32 + lane;           // key row (S^T) / query row (dQ)
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
     const bool krow_valid = row < nk;
-    const int64_t kpos = krow_valid ? seg_pos(it.ks, k0 + row) : INT64_MAX;
+    const int64_t kpos = krow_valid ? seg_pos(gm.ks, k0 + row) : INT64_MAX;
     const float sl2 = a.scale_log2;
     uint8_t* sds = smem + L::DS_OFF + wg * PANEL + (row >> 3) * 1024 + (row & 7) * 128;
     int n = 0;
@@ -401,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     };
     if (ok) ok = convert_q(0);
     for (int t = 0; ok && t < nqt; ++t) {
-      const QTile qt = q_tile(it, t, causal, nk, kmin, kmax);
+      const QTile qt = q_tile(gm, t, causal, nk, kmin, kmax);
       if (!qt.visible) continue;
       // -lse*log2e and delta of this warpgroup's 64 query columns (staged by warp 8)
       const float* nl2 = lse_sm + (n & 1) * 2 * BM + 64 * wg;
@@ -423,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll 1
         for (int j = 0; j < 64; ++j) {
           const int qc = 64 * wg + j;
-          const bool v = krow_valid && qc < qt.nq && (!causal || kpos <= seg_pos(it.qs, qt.q0 + qc));
+          const bool v = krow_valid && qc < qt.nq && (!causal || kpos <= seg_pos(gm.qs, qt.q0 + qc));
           vis |= static_cast<uint64_t>(v) << j;
         }
       }
@@ -537,30 +546,44 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       mbar_arrive(&bars->dq_staged[n & 1]);
       ++n;
     }
-    // dK (warpgroup 0) and dV (warpgroup 1): thread = key row
-    if (__all_sync(0xffffffffu, ok) && n > 0) {
+    // dK (warpgroup 0, times scale) and dV (warpgroup 1): thread = key row,
+    // staged fp32 in 32-column 128B-swizzled boxes over the K/V tiles (dK)
+    // and the Q stages (dV), free since the last MMA completed; one thread
+    // per warpgroup then has the TMA unit add them into (accumulate) or
+    // store them to global memory.  Key rows past the slab are skipped by
+    // the TMA bounds.
+    const bool epi = __all_sync(0xffffffffu, ok) && n > 0;
+    if (epi) {
       tc_fence_after();
       const uint32_t src = (wg == 0 ? tdK : tdV) + lane_off;
-      float* dst = (wg == 0 ? dk_base : dv_base) + (k0 + (krow_valid ? row : 0)) * a.dkv.s;
+      uint8_t* stg = smem + (wg == 0 ? L::K_OFF : L::Q_OFF) + (row >> 3) * 1024 + (row & 7) * 128;
       const float mul = wg == 0 ? a.scale : 1.f;
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < D; c += 32) {
         uint32_t r[32];
         tmem_ld32(src + c, r);
         tmem_wait_ld32(r);
-        if (krow_valid) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            float4 v = make_float4(mul * __uint_as_float(r[i]), mul * __uint_as_float(r[i + 1]),
-                                   mul * __uint_as_float(r[i + 2]), mul * __uint_as_float(r[i + 3]));
-            float4* p = reinterpret_cast<float4*>(dst + c + i);
-            if (a.accumulate) {
-              const float4 o = *p;
-              v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
-            }
-            *p = v;
-          }
+        for (int j = 0; j < 8; ++j) {
+          const float4 v = make_float4(mul * __uint_as_float(r[4 * j]), mul * __uint_as_float(r[4 * j + 1]),
+                                       mul * __uint_as_float(r[4 * j + 2]), mul * __uint_as_float(r[4 * j + 3]));
+          *reinterpret_cast<float4*>(stg + (c / 32) * PANEL + ((j ^ (row & 7)) << 4)) = v;
         }
+      }
+      fence_async_smem();
+      mbar_arrive(&bars->epi_staged[wg]);
+      if ((threadIdx.x & 127) == 0 && mbar_wait(&bars->epi_staged[wg], 0, abort, status)) {
+        const CUtensorMap* m = &ta.maps[item_idx][wg == 0 ? 5 : 6];
+        const uint8_t* base = smem + (wg == 0 ? L::K_OFF : L::Q_OFF);
+#pragma unroll
+        for (int bx = 0; bx < D / 32; ++bx) {
+          if (a.accumulate)
+            tma_reduce_add_4d(m, base + bx * PANEL, 32 * bx, static_cast<int>(k0), h, b);
+          else
+            tma_store_4d(m, base + bx * PANEL, 32 * bx, static_cast<int>(k0), h, b);
+        }
+        bulk_commit();
+        bulk_wait_all();
       }
     }
   }
@@ -596,20 +619,8 @@ cudaError_t tc_backward(AttnArgs& a, cudaStream_t st) {
   static TcArgs ta;
   static std::mutex mu;
   std::lock_guard<std::mutex> g(mu);
-  int64_t mt = 0;
-  for (int i = 0; i < a.n_items; ++i) {
-    const Item& it = a.items[i];
-    const int64_t t = (it.Skv + BN - 1) / BN;
-    if (t > mt) mt = t;
-    cudaError_t e;
-    if ((e = make_tmap_bf16(&ta.maps[i][0], it.q, a.D, it.Sq, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
-    if ((e = make_tmap_bf16(&ta.maps[i][1], it.k, a.D, it.Skv, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
-    if ((e = make_tmap_bf16(&ta.maps[i][2], it.v, a.D, it.Skv, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
-    if ((e = make_tmap_bf16(&ta.maps[i][3], it.dout, a.D, it.Sq, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
-    if ((e = make_tmap_f32(&ta.maps[i][4], it.o, a.D, it.Sq, a.H, a.B, a.o, 32, BM)) != cudaSuccess) return e;
-  }
-  // dq gathers contributions from every key tile through atomics: in
-  // overwrite mode it starts from zero
+  // dq gathers contributions from every key tile through TMA reduce-adds:
+  // in overwrite mode it starts from zero
   if (!a.accumulate) {
     if (a.o.s != a.D) return cudaErrorNotSupported;
     for (int i = 0; i < a.n_items; ++i) {
@@ -624,9 +635,33 @@ cudaError_t tc_backward(AttnArgs& a, cudaStream_t st) {
       }
     }
   }
-  a.max_k_tiles = static_cast<int>(mt);
-  ta.a = a;
-  return a.D == 64 ? launch<64>(ta, st) : launch<128>(ta, st);
+  // items are independent: launch them in groups that fit the parameters
+  for (int first = 0; first < a.n_items; first += kItemsPerLaunch) {
+    const int cnt = a.n_items - first < kItemsPerLaunch ? a.n_items - first : kItemsPerLaunch;
+    ta.a = a;
+    ta.a.n_items = cnt;
+    int64_t mt = 0;
+    for (int i = 0; i < cnt; ++i) {
+      const Item& it = a.items[first + i];
+      ta.a.items[i] = it;
+      const int64_t t = (it.Skv + BN - 1) / BN;
+      if (t > mt) mt = t;
+      CUtensorMap* m = ta.maps[i];
+      cudaError_t e;
+      if ((e = make_tmap_bf16(&m[0], it.q, a.D, it.Sq, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
+      if ((e = make_tmap_bf16(&m[1], it.k, a.D, it.Skv, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
+      if ((e = make_tmap_bf16(&m[2], it.v, a.D, it.Skv, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
+      if ((e = make_tmap_bf16(&m[3], it.dout, a.D, it.Sq, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
+      if ((e = make_tmap_f32(&m[4], it.o, a.D, it.Sq, a.H, a.B, a.o, 32, BM)) != cudaSuccess) return e;
+      if ((e = make_tmap_f32(&m[5], it.dk, a.D, it.Skv, a.H, a.B, a.dkv, 32, BN)) != cudaSuccess) return e;
+      if ((e = make_tmap_f32(&m[6], it.dv, a.D, it.Skv, a.H, a.B, a.dkv, 32, BN)) != cudaSuccess) return e;
+    }
+    if (mt == 0) continue;
+    ta.a.max_k_tiles = static_cast<int>(mt);
+    const cudaError_t e = a.D == 64 ? launch<64>(ta, st) : launch<128>(ta, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace sca

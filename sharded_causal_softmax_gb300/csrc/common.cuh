@@ -73,6 +73,22 @@ struct View {
   int64_t b, h, s;
 };
 
+// The position geometry of one item, copied once per CTA out of the kernel
+// parameters into registers: read in place, behind the dynamic item index,
+// every use is a constant-cache load, and the tile loops make hundreds.
+struct ItemGeom {
+  Segs qs, ks;
+  int64_t Sq, Skv;
+};
+SCA_INLINE ItemGeom item_geom(const Item& it) {
+  ItemGeom g;
+  g.qs = it.qs;
+  g.ks = it.ks;
+  g.Sq = it.Sq;
+  g.Skv = it.Skv;
+  return g;
+}
+
 struct AttnArgs {
   Item items[SCA_MAX_ITEMS];
   View q, kv, o, dkv;

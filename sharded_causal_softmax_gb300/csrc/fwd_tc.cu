@@ -92,20 +92,20 @@ struct TileInfo {
   bool visible, full;
 };
 
-SCA_INLINE TileInfo tile_info(const Item& it, int kt, bool causal, int64_t qmin, int64_t qmax) {
+SCA_INLINE TileInfo tile_info(const ItemGeom& g, int kt, bool causal, int64_t qmin, int64_t qmax) {
   TileInfo t;
   t.k0 = static_cast<int64_t>(kt) * BN;
-  t.nk = static_cast<int>(min64(BN, it.Skv - t.k0));
+  t.nk = static_cast<int>(min64(BN, g.Skv - t.k0));
   int64_t kmin, kmax;
-  tile_pos_range(it.ks, t.k0, t.nk, kmin, kmax);
+  tile_pos_range(g.ks, t.k0, t.nk, kmin, kmax);
   t.visible = !causal || kmin <= qmax;
   t.full = t.nk == BN && (!causal || kmax <= qmin);
   return t;
 }
 
 // First visible key tile at or after kt (nkt if none).
-SCA_INLINE int next_visible(const Item& it, int kt, int nkt, bool causal, int64_t qmin, int64_t qmax) {
-  while (kt < nkt && !tile_info(it, kt, causal, qmin, qmax).visible) ++kt;
+SCA_INLINE int next_visible(const ItemGeom& g, int kt, int nkt, bool causal, int64_t qmin, int64_t qmax) {
+  while (kt < nkt && !tile_info(g, kt, causal, qmin, qmax).visible) ++kt;
   return kt;
 }
 
@@ -119,17 +119,18 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
   const int item_idx = blockIdx.z;
   const Item& it = a.items[item_idx];
+  const ItemGeom gm = item_geom(it);
   const int64_t q0 = static_cast<int64_t>(a.max_q_tiles - 1 - blockIdx.x) * BM;  // heavy tiles first
-  if (q0 >= it.Sq) return;
+  if (q0 >= gm.Sq) return;
   const int b = blockIdx.y / a.H, h = blockIdx.y % a.H;
-  const int nq = static_cast<int>(min64(BM, it.Sq - q0));
+  const int nq = static_cast<int>(min64(BM, gm.Sq - q0));
   int64_t qmin, qmax;
-  tile_pos_range(it.qs, q0, nq, qmin, qmax);
-  const int nkt = static_cast<int>((it.Skv + BN - 1) / BN);
+  tile_pos_range(gm.qs, q0, nq, qmin, qmax);
+  const int nkt = static_cast<int>((gm.Skv + BN - 1) / BN);
   const bool causal = a.causal != 0;
 
   int n_vis = 0;
-  for (int kt = 0; kt < nkt; ++kt) n_vis += tile_info(it, kt, causal, qmin, qmax).visible ? 1 : 0;
+  for (int kt = 0; kt < nkt; ++kt) n_vis += tile_info(gm, kt, causal, qmin, qmax).visible ? 1 : 0;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (n_vis == 0) {
@@ -196,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       for (int p = 0; p < D / 64; ++p)
         tma_load_4d(smem + L::Q_OFF + p * PANEL, mq, &bars->q_full, 64 * p, static_cast<int>(q0), h, b);
       int n = 0;
-      for (int kt = next_visible(it, 0, nkt, causal, qmin, qmax); kt < nkt;
-           kt = next_visible(it, kt + 1, nkt, causal, qmin, qmax)) {
+      for (int kt = next_visible(gm, 0, nkt, causal, qmin, qmax); kt < nkt;
+           kt = next_visible(gm, kt + 1, nkt, causal, qmin, qmax)) {
         const int st = n % KST;
         if (!mbar_wait(&bars->k_empty[st], ((n / KST) & 1) ^ 1, abort, status)) break;
         mbar_arrive_expect_tx(&bars->k_full[st], L::TILE);
@@ -216,8 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       const CUtensorMap* mv = &ta.maps[item_idx][2];
       tma_prefetch_map(mv);
       int n = 0;
-      for (int kt = next_visible(it, 0, nkt, causal, qmin, qmax); kt < nkt;
-           kt = next_visible(it, kt + 1, nkt, causal, qmin, qmax)) {
+      for (int kt = next_visible(gm, 0, nkt, causal, qmin, qmax); kt < nkt;
+           kt = next_visible(gm, kt + 1, nkt, causal, qmin, qmax)) {
         const int st = n % VST;
         if (!mbar_wait(&bars->v_empty[st], ((n / VST) & 1) ^ 1, abort, status)) break;
         mbar_arrive_expect_tx(&bars->v_full[st], L::TILE);
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     const int row = qw * 32 + lane;          // query row == tensor-memory lane
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
     const bool row_valid = row < nq;
-    const int64_t qpos = row_valid ? seg_pos(it.qs, q0 + row) : INT64_MIN;
+    const int64_t qpos = row_valid ? seg_pos(gm.qs, q0 + row) : INT64_MIN;
     const float sl2 = a.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     int n = 0;
@@ -305,9 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     }
     tc_fence_before();
     mbar_arrive(&bars->q_tmem);
-    for (int kt = next_visible(it, 0, nkt, causal, qmin, qmax); ok && kt < nkt;
-         kt = next_visible(it, kt + 1, nkt, causal, qmin, qmax)) {
-      const TileInfo ti = tile_info(it, kt, causal, qmin, qmax);
+    for (int kt = next_visible(gm, 0, nkt, causal, qmin, qmax); ok && kt < nkt;
+         kt = next_visible(gm, kt + 1, nkt, causal, qmin, qmax)) {
+      const TileInfo ti = tile_info(gm, kt, causal, qmin, qmax);
       const int sb = n % SBUF;
       // observe PV_{n-2}: each pv_done barrier is then at most one phase ahead
       // of the phase this thread waits for next (a parity wait needs that)
@@ -326,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           const int c = 64 * g + i;
-          const bool vis = c < ti.nk && (!causal || seg_pos(it.ks, ti.k0 + c) <= qpos);
+          const bool vis = c < ti.nk && (!causal || seg_pos(gm.ks, ti.k0 + c) <= qpos);
           if (!vis) s[i] = -INFINITY;
         }
       }
