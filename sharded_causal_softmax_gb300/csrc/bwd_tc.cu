@@ -146,10 +146,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   tile_pos_range(gm.ks, k0, nk, kmin, kmax);
   const bool causal = a.causal != 0;
   const int nqt = static_cast<int>((gm.Sq + BM - 1) / BM);
-  int n_vis = 0;
-  for (int t = 0; t < nqt; ++t) n_vis += q_tile(gm, t, causal, nk, kmin, kmax).visible ? 1 : 0;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto qvis = [&](int t) { return q_tile(gm, t, causal, nk, kmin, kmax).visible; };
+  const int n_vis = count_tiles(nqt, lane, qvis);
   float* dk_base = it.dk + b * a.dkv.b + h * a.dkv.h;
   float* dv_base = it.dv + b * a.dkv.b + h * a.dkv.h;
 
@@ -243,9 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     };
     int n = 0;
     bool ok = true;
-    for (int t = 0; t < nqt; ++t) {
+    TileCursor cur;
+    for (int t; (t = cur.next(nqt, lane, qvis)) >= 0;) {
       const QTile qt = q_tile(gm, t, causal, nk, kmin, kmax);
-      if (!qt.visible) continue;
       const int st = n & 1;
       // lse/delta of this tile into registers while the stage drains
       float lse_r[BM / 32], dl_r[BM / 32];
@@ -307,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     }
   } else if (warp == 9) {
     // ------------------------------------------------------ MMA issuer
+    // one thread; it needs only the count of visible tiles, not their rows
     if (lane == 0) {
       constexpr uint32_t idesc_dp = idesc_bf16_f32(BN, BM, false, false);    // dP^T: M=keys, N=queries
       constexpr uint32_t idesc_s = idesc_f16_f32(BN, BM, false, false);      // S^T (fp16 K, Q)
@@ -316,17 +316,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       const uint32_t sK = smem_u32(smem + L::K_OFF), sV = smem_u32(smem + L::V_OFF);
       const uint32_t sDS = smem_u32(smem + L::DS_OFF);
       bool ok = mbar_wait(&bars->kv_full, 0, abort, status);
-      int n = 0;
-      for (int t = 0; ok && t < nqt; ++t) {
-        const QTile qt = q_tile(gm, t, causal, nk, kmin, kmax);
-        if (!qt.visible) continue;
+      for (int n = 0; ok && n < n_vis; ++n) {
         const int st = n & 1;
-        if (!mbar_wait(&bars->q_full[st], (n >> 1) & 1, abort, status)) { ok = false; break; }
-        tc_fence_after();
         const uint32_t sQ = smem_u32(smem + L::Q_OFF + st * L::TILE);
         const uint32_t sO = smem_u32(smem + L::DO_OFF + st * L::TILE);
         // S^T = K Q^T over the S^T columns (the previous dV has read P^T);
         // K and Q must have been converted to fp16
+        if (!mbar_wait(&bars->q_full[st], (n >> 1) & 1, abort, status)) { ok = false; break; }
         if (n == 0 && !mbar_wait(&bars->k_conv, 0, abort, status)) { ok = false; break; }
         if (!mbar_wait(&bars->q_conv, n & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
@@ -369,12 +365,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         }
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          umma_ss(tdP, sdesc_sw128(sDS + kk * 2048, PANEL, 1024), sdesc_sw128(sK + kk * 2048, PANEL, 1024), idesc_dq,
-                  kk > 0 ? 1u : 0u);
+          umma_ss(tdP, sdesc_sw128(sDS + kk * 2048, PANEL, 1024), sdesc_sw128(sK + kk * 2048, PANEL, 1024),
+                  idesc_dq, kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars->q_empty[st]);
         umma_commit(&bars->dq_full);
-        ++n;
       }
       if (!ok) {
         umma_commit(&bars->drain);
@@ -409,9 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       return w;
     };
     if (ok) ok = convert_q(0);
-    for (int t = 0; ok && t < nqt; ++t) {
+    TileCursor cur;
+    for (int t; ok && (t = cur.next(nqt, lane, qvis)) >= 0;) {
       const QTile qt = q_tile(gm, t, causal, nk, kmin, kmax);
-      if (!qt.visible) continue;
       // -lse*log2e and delta of this warpgroup's 64 query columns (staged by warp 8)
       const float* nl2 = lse_sm + (n & 1) * 2 * BM + 64 * wg;
       const float* dls = nl2 + BM;

@@ -54,6 +54,34 @@ __host__ __device__ __forceinline__ void tile_pos_range(const Segs& s, int64_t r
   }
 }
 
+// Walks, in order, the tiles t in [0, n) for which vis(t) holds, testing 32
+// candidates per warp-wide ballot.  All 32 lanes of a warp call next()
+// together with the same arguments; it returns -1 after the last tile.
+struct TileCursor {
+  int base = -32;
+  uint32_t mask = 0;
+  template <typename Vis>
+  __device__ __forceinline__ int next(int n, int lane, const Vis& vis) {
+    while (mask == 0) {
+      base += 32;
+      if (base >= n) return -1;
+      mask = __ballot_sync(0xffffffffu, base + lane < n && vis(base + lane));
+    }
+    const int t = base + __ffs(mask) - 1;
+    mask &= mask - 1;
+    return t;
+  }
+};
+
+// Number of t in [0, n) with vis(t), by warp-wide ballots (all lanes call).
+template <typename Vis>
+__device__ __forceinline__ int count_tiles(int n, int lane, const Vis& vis) {
+  int c = 0;
+  for (int base = 0; base < n; base += 32)
+    c += __popc(__ballot_sync(0xffffffffu, base + lane < n && vis(base + lane)));
+  return c;
+}
+
 // Per-item data of an attention launch (forward and backward share it).
 struct Item {
   const void* q;

@@ -103,12 +103,6 @@ SCA_INLINE TileInfo tile_info(const ItemGeom& g, int kt, bool causal, int64_t qm
   return t;
 }
 
-// First visible key tile at or after kt (nkt if none).
-SCA_INLINE int next_visible(const ItemGeom& g, int kt, int nkt, bool causal, int64_t qmin, int64_t qmax) {
-  while (kt < nkt && !tile_info(g, kt, causal, qmin, qmax).visible) ++kt;
-  return kt;
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ TcArgs ta) {
   using L = Layout<D>;
@@ -129,10 +123,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   const int nkt = static_cast<int>((gm.Skv + BN - 1) / BN);
   const bool causal = a.causal != 0;
 
-  int n_vis = 0;
-  for (int kt = 0; kt < nkt; ++kt) n_vis += tile_info(gm, kt, causal, qmin, qmax).visible ? 1 : 0;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto kvis = [&](int kt) { return tile_info(gm, kt, causal, qmin, qmax).visible; };
+  const int n_vis = count_tiles(nkt, lane, kvis);
   if (n_vis == 0) {
     // no visible key: the empty partial
     if (warp < 8) {
@@ -188,47 +181,54 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
   if (warp == kProdK) {
     // ------------------------------------------------ Q + K producer
+    // lane 0 waits and issues; the warp walks the tile list together
+    const CUtensorMap* mq = &ta.maps[item_idx][0];
+    const CUtensorMap* mk = &ta.maps[item_idx][1];
     if (lane == 0) {
-      const CUtensorMap* mq = &ta.maps[item_idx][0];
-      const CUtensorMap* mk = &ta.maps[item_idx][1];
       tma_prefetch_map(mq);
       tma_prefetch_map(mk);
       mbar_arrive_expect_tx(&bars->q_full, L::TILE);
       for (int p = 0; p < D / 64; ++p)
         tma_load_4d(smem + L::Q_OFF + p * PANEL, mq, &bars->q_full, 64 * p, static_cast<int>(q0), h, b);
-      int n = 0;
-      for (int kt = next_visible(gm, 0, nkt, causal, qmin, qmax); kt < nkt;
-           kt = next_visible(gm, kt + 1, nkt, causal, qmin, qmax)) {
-        const int st = n % KST;
-        if (!mbar_wait(&bars->k_empty[st], ((n / KST) & 1) ^ 1, abort, status)) break;
+    }
+    int n = 0;
+    TileCursor cur;
+    for (int kt; (kt = cur.next(nkt, lane, kvis)) >= 0;) {
+      const int st = n % KST;
+      int w = 0;
+      if (lane == 0 && mbar_wait(&bars->k_empty[st], ((n / KST) & 1) ^ 1, abort, status)) {
+        w = 1;
         mbar_arrive_expect_tx(&bars->k_full[st], L::TILE);
         for (int p = 0; p < D / 64; ++p)
           tma_load_4d(smem + L::K_OFF + st * L::TILE + p * PANEL, mk, &bars->k_full[st], 64 * p, kt * BN, h, b);
-        ++n;
       }
-      if (*abort) {  // let issued copies land before the CTA goes away
-        mbar_wait_drain(&bars->q_full, 0);
-        for (int j = (n > KST ? n - KST : 0); j < n; ++j) mbar_wait_drain(&bars->k_full[j % KST], (j / KST) & 1);
-      }
+      if (!__shfl_sync(0xffffffffu, w, 0)) break;
+      ++n;
+    }
+    if (lane == 0 && *abort) {  // let issued copies land before the CTA goes away
+      mbar_wait_drain(&bars->q_full, 0);
+      for (int j = (n > KST ? n - KST : 0); j < n; ++j) mbar_wait_drain(&bars->k_full[j % KST], (j / KST) & 1);
     }
   } else if (warp == kProdV) {
     // ------------------------------------------------------ V producer
-    if (lane == 0) {
-      const CUtensorMap* mv = &ta.maps[item_idx][2];
-      tma_prefetch_map(mv);
-      int n = 0;
-      for (int kt = next_visible(gm, 0, nkt, causal, qmin, qmax); kt < nkt;
-           kt = next_visible(gm, kt + 1, nkt, causal, qmin, qmax)) {
-        const int st = n % VST;
-        if (!mbar_wait(&bars->v_empty[st], ((n / VST) & 1) ^ 1, abort, status)) break;
+    const CUtensorMap* mv = &ta.maps[item_idx][2];
+    if (lane == 0) tma_prefetch_map(mv);
+    int n = 0;
+    TileCursor cur;
+    for (int kt; (kt = cur.next(nkt, lane, kvis)) >= 0;) {
+      const int st = n % VST;
+      int w = 0;
+      if (lane == 0 && mbar_wait(&bars->v_empty[st], ((n / VST) & 1) ^ 1, abort, status)) {
+        w = 1;
         mbar_arrive_expect_tx(&bars->v_full[st], L::TILE);
         for (int p = 0; p < D / 64; ++p)
           tma_load_4d(smem + L::V_OFF + st * L::TILE + p * PANEL, mv, &bars->v_full[st], 64 * p, kt * BN, h, b);
-        ++n;
       }
-      if (*abort) {
-        for (int j = (n > VST ? n - VST : 0); j < n; ++j) mbar_wait_drain(&bars->v_full[j % VST], (j / VST) & 1);
-      }
+      if (!__shfl_sync(0xffffffffu, w, 0)) break;
+      ++n;
+    }
+    if (lane == 0 && *abort) {
+      for (int j = (n > VST ? n - VST : 0); j < n; ++j) mbar_wait_drain(&bars->v_full[j % VST], (j / VST) & 1);
     }
   } else if (warp == kMma) {
     // ------------------------------------------------------ MMA issuer
@@ -306,8 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     }
     tc_fence_before();
     mbar_arrive(&bars->q_tmem);
-    for (int kt = next_visible(gm, 0, nkt, causal, qmin, qmax); ok && kt < nkt;
-         kt = next_visible(gm, kt + 1, nkt, causal, qmin, qmax)) {
+    TileCursor cur;
+    for (int kt; ok && (kt = cur.next(nkt, lane, kvis)) >= 0;) {
       const TileInfo ti = tile_info(gm, kt, causal, qmin, qmax);
       const int sb = n % SBUF;
       // observe PV_{n-2}: each pv_done barrier is then at most one phase ahead
