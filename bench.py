@@ -20,6 +20,7 @@ plain implementation), on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import atexit
 import dataclasses
 import hashlib
 import json
@@ -76,44 +77,53 @@ def barrier(ws: int):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons, sampled every `period_ms` from
+    before the warm-up on; summary() keeps the samples taken inside a host
+    time window (the timed region)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 20):
         self.gpu = gpu_index
+        self.period_ms = period_ms
         self.proc = None
-        self.lines = []
+        self.lines = []   # (host monotonic time, csv line)
 
-    def __enter__(self):
+    def start(self, wait_s: float = 5.0):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.reader = threading.Thread(target=self._read, daemon=True)
-            self.reader.start()
         except OSError:
             self.proc = None
+            return self
+        atexit.register(self.stop)   # never leave the sampler running
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        t_end = time.monotonic() + wait_s   # let it start sampling before the region opens
+        while not self.lines and time.monotonic() < t_end:
+            time.sleep(0.01)
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
-    def __exit__(self, *exc):
-        if self.proc is not None:
+    def stop(self):
+        if self.proc is not None and self.proc.poll() is None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0: float, t1: float):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        window = [ln for t, ln in self.lines if t0 <= t <= t1]
+        for line in window:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -127,7 +137,8 @@ class ClockSampler:
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "period_ms": self.period_ms}
 
 
 def load_peaks():
@@ -214,6 +225,7 @@ def run_gpu(args):
             kern += plan.kernels
         return kern
 
+    clocks = ClockSampler(local).start()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -225,14 +237,16 @@ def run_gpu(args):
     torch.cuda.synchronize()
     timing_on[0] = True
     launches = 0
-    with ClockSampler(local) as clocks:
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(args.steps):
-            launches += step()
-        t1.record(stream)
-        torch.cuda.synchronize()
+    h0 = time.monotonic()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        launches += step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.monotonic()
+    clocks.stop()
     timing_on[0] = False
     barrier(ws)
     ms = t0.elapsed_time(t1)
@@ -326,7 +340,7 @@ def run_gpu(args):
                    "flops_per_step": step_flops, "l2": "inputs larger than L2 (no flush)"
                    if sum(x.numel() * x.element_size() for x in inputs) > L2_BYTES else "inputs fit in L2",
                    "parallelism": f"{ws} independent replica(s), one per GPU"},
-        "clocks": clocks.summary(),
+        "clocks": clocks.summary(h0, h1),
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": launches,

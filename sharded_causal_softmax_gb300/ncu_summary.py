@@ -17,7 +17,12 @@ from collections import defaultdict
 
 COUNTERS = ["gpu__time_duration.sum", "dram__bytes_read.sum", "dram__bytes_write.sum",
             "gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed",
-            "sm__pipe_tensor_cycles_active_realtime.avg.pct_of_peak_sustained_elapsed",
+            "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed",
+            "smsp__inst_executed.sum",
+            "l1tex__data_pipe_lsu_wavefronts_mem_shared.sum.pct_of_peak_sustained_elapsed",
+            "l1tex__data_pipe_tc_wavefronts_mem_shared.sum.pct_of_peak_sustained_elapsed",
+            "l1tex__data_bank_conflicts_pipe_lsu_mem_shared.sum",
+            "l1tex__m_l1tex2xbar_write_bytes_mem_global_op_tma_red.sum",
             "sm__mem_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed",
             "sm__inst_executed_pipe_xu.avg.pct_of_peak_sustained_active",
             "sm__pipe_fma_cycles_active.avg.pct_of_peak_sustained_active",
