@@ -194,8 +194,11 @@ typedef struct {
  * With bf16 inputs the tensor-core kernel computes S, dK and dQ as fp16
  * products (Q and K are converted to fp16 inside the kernel, dS is rounded
  * to fp16): |q| and |k| must stay below 65504.  dq is summed over key tiles
- * with fp32 atomics, so it is reproducible only up to rounding order.
- * Errors as attn_fwd_shard. */
+ * by fp32 reduce-adds in no fixed order, so it is reproducible only up to
+ * rounding order; dk and dv have one writer per row.  The tensor-core path
+ * needs dq, dk, dv rows 16-byte aligned with strides that are multiples of
+ * 16 bytes (SCA_ERR_ALIGN otherwise), and in overwrite mode dq rows
+ * contiguous (dims->o.s == D).  Errors as attn_fwd_shard. */
 int attn_bwd_shard(const sca_bwd_item* items, int n_items, const sca_attn_dims* dims,
                    int* dev_status, void* stream);
 
