@@ -13,7 +13,9 @@
 //   dq[rows of tile i] += scale * dQ_i             (TMA reduce-add, fp32)
 //
 // The MMAs run in that order, so phase 1 overlaps dP^T, phase 2 overlaps
-// dV, and the next tile's S^T overlaps the read-back of dQ_i.
+// dV, and the next tile's S^T overlaps the read-back of dQ_i.  Both phases
+// signal each 32-query chunk, and dV and dK each run as two halves, so an
+// MMA half starts as soon as its chunk is written.
 //
 // Roles: warps 0-7 elementwise (two warpgroups; warpgroup g owns query
 // columns [64g, 64g+64), thread = key row = tensor-memory lane), then read
@@ -83,7 +85,8 @@ struct Bars {
   uint64_t ds_free;          // the reduce has read the dQ half staged in the dS panels
   uint64_t epi_staged[2];    // warpgroup g staged dK (g=0) / dV (g=1) for the final TMA write
   uint64_t s_full, dp_full;   // S^T / dP^T of the current tile in tensor memory
-  uint64_t p_ready, ds_ready; // P^T / dS^T written by warps 0-7 (dS also to smem)
+  uint64_t p_half[2];        // P^T of query chunk c (32 per warpgroup) written by warps 0-7
+  uint64_t ds_half[2];       // dS^T of query chunk c written (after chunk 1: dS in smem too)
   uint64_t dq_full, tmem_free;
   uint64_t k_conv, q_conv;   // K / the current Q tile converted to fp16
   uint64_t drain;
@@ -177,8 +180,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     for (int i = 0; i < 2; ++i) mbar_init(&bars->epi_staged[i], 128);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_ready, 256);
-    mbar_init(&bars->ds_ready, 256);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->p_half[i], 256);
+      mbar_init(&bars->ds_half[i], 256);
+    }
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->tmem_free, 256);
     mbar_init(&bars->k_conv, 256);
@@ -345,24 +350,37 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                   kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars->dp_full);
-        // dV += P^T dO  (A from tensor memory; query K-step kk lives in
-        // warpgroup kk/4's packed columns)
-        if (!mbar_wait(&bars->p_ready, n & 1, abort, status)) { ok = false; break; }
-        tc_fence_after();
+        // dV += P^T dO, then dK += dS^T Q (A from tensor memory).  Query
+        // K-step kk = 4g + 2c + e lives in warpgroup g's packed columns
+        // 64g + 16c + 8e and is ready once chunk c of both warpgroups is:
+        // each product runs as two halves, chunk 0's K-steps first.
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk) {
-          const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
-          umma_ts(tdV, tS + acol, sdesc_sw128(sO + kk * 2048, PANEL, 1024), idesc_dv, (n > 0 || kk > 0) ? 1u : 0u);
-        }
-        // dK += dS^T Q, then dQ = dS K over the dP^T columns, N = D: B = K
-        // tile, MN-major, its 64-column panels LBO apart
-        if (!mbar_wait(&bars->ds_ready, n & 1, abort, status)) { ok = false; break; }
-        tc_fence_after();
+        for (int c = 0; c < 2; ++c) {
+          if (!mbar_wait(&bars->p_half[c], n & 1, abort, status)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk) {
-          const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
-          umma_ts(tdK, tdP + acol, sdesc_sw128(sQ + kk * 2048, PANEL, 1024), idesc_dk, (n > 0 || kk > 0) ? 1u : 0u);
+          for (int q = 0; q < 4; ++q) {
+            const int kk = 4 * (q >> 1) + 2 * c + (q & 1);
+            const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
+            umma_ts(tdV, tS + acol, sdesc_sw128(sO + kk * 2048, PANEL, 1024), idesc_dv, (n > 0 || kk > 0) ? 1u : 0u);
+          }
         }
+        if (!ok) break;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (!mbar_wait(&bars->ds_half[c], n & 1, abort, status)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int kk = 4 * (q >> 1) + 2 * c + (q & 1);
+            const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
+            umma_ts(tdK, tdP + acol, sdesc_sw128(sQ + kk * 2048, PANEL, 1024), idesc_dk, (n > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        if (!ok) break;
+        // dQ = dS K over the dP^T columns (dK has read dS^T), N = D: A = the
+        // dS panels (complete after chunk 1), B = K tile, MN-major, its
+        // 64-column panels LBO apart
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           umma_ss(tdP, sdesc_sw128(sDS + kk * 2048, PANEL, 1024), sdesc_sw128(sK + kk * 2048, PANEL, 1024),
@@ -458,15 +476,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           }
           // over S^T columns this thread has already read
           tmem_st16(tS + lane_off + 64 * wg + 16 * c, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bars->p_half[c]);
         }
       };
       if (qt.full)
         exps(std::false_type{});
       else
         exps(std::true_type{});
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->p_ready);
       // phase 2: dS^T = P^T (dP^T - delta), fp16, to tensor memory (A of the
       // dK MMAs) and to this warpgroup's dS panel (A of the dQ MMAs)
       // the dS panels hold half of the previous tile's dQ until its reduce
@@ -502,11 +520,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           uint4 v = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
           *reinterpret_cast<uint4*>(sds + ((j ^ (row & 7)) << 4)) = v;
         }
+        tmem_wait_st();
+        if (c == 1) fence_async_smem();   // the whole dS panel, for the dQ MMAs
+        tc_fence_before();
+        mbar_arrive(&bars->ds_half[c]);
       }
-      tmem_wait_st();
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars->ds_ready);
       // the next tile's Q conversion overlaps this tile's dK/dQ MMAs
       if (n + 1 < n_vis && !convert_q(n + 1)) { ok = false; break; }
       // dQ read-back from the dP^T columns: thread = query row, warpgroup wg
