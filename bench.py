@@ -193,8 +193,11 @@ def run_gpu(args):
     dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     inputs = seeded_inputs.workload_inputs(w)
     dev_in = [x.to(device) for x in inputs]
+    if args.schedule:
+        w = dataclasses.replace(w, schedule=args.schedule)
     plan = sca.ShardedCausalAttention(w.B, w.H, w.S, w.D, w.P, layout=w.layout, dtype=dtype,
-                                      head_groups=w.head_groups, schedule=w.schedule, backward=w.backward)
+                                      head_groups=w.head_groups, schedule=w.schedule, backward=w.backward,
+                                      addressing=args.addressing)
     stream = torch.cuda.current_stream(device)
 
     # per-launch timing of the attention kernels (same stream they run on)
@@ -216,6 +219,35 @@ def run_gpu(args):
     timing_on = [False]
     sca.sharded.capi.attn_fwd_shard = timed("fwd", orig_fwd)
     sca.sharded.capi.attn_bwd_shard = timed("bwd", orig_bwd)
+
+    # HBM-bound kernels: events around each call, algorithmic bytes from its
+    # arguments (read + written once)
+    hbm = {"zigzag_permute_kernel": [], "merge_lse_kernel": [], "delta_kernel": []}
+
+    def timed_hbm(name, fn, nbytes):
+        def wrapper(*a, **k):
+            if not timing_on[0]:
+                return fn(*a, **k)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            r = fn(*a, **k)
+            e1.record(stream)
+            hbm[name].append((e0, e1, nbytes(*a)))
+            return r
+        return wrapper
+
+    def permute_bytes(src, dst, outer, S, row_bytes, *rest):
+        return 2 * outer * S * row_bytes
+
+    def merge_bytes(o_parts, lse_parts, n, rows, D, o_stride, lse_stride, o_out, lse_out, o_bf16, *rest):
+        return (n + 1) * rows * (4 * D + 4) + (2 * rows * D if o_bf16 else 0)
+
+    def delta_bytes(o, dout, dout_dtype, delta, rows, D, *rest):
+        return rows * (4 * D + (2 if dout_dtype == 0 else 4) * D + 4)
+
+    sca.sharded.capi.zigzag_permute = timed_hbm("zigzag_permute_kernel", sca.capi.zigzag_permute, permute_bytes)
+    sca.sharded.capi.attn_merge_lse = timed_hbm("merge_lse_kernel", sca.capi.attn_merge_lse, merge_bytes)
+    sca.sharded.capi.attn_bwd_delta = timed_hbm("delta_kernel", sca.capi.attn_bwd_delta, delta_bytes)
 
     def step():
         plan.forward(*dev_in[:3])
@@ -298,7 +330,9 @@ def run_gpu(args):
     kind = max(per, key=lambda k: per[k][0])
     total_ms, n = per[kind]
     avg_s = total_ms / n * 1e-3
-    launch_flops = flops(w, fwd=(kind == "fwd"), bwd=(kind == "bwd")) / w.P
+    # the FLOPs of that direction over the timed steps, shared by its launches
+    # (P per direction on the ring, one when fused)
+    launch_flops = flops(w, fwd=(kind == "fwd"), bwd=(kind == "bwd")) * args.steps / n
     tc = plan.uses_tensor_cores(kind)
     if tc:
         peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
@@ -317,8 +351,34 @@ def run_gpu(args):
                 "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": peak_note, "launches_timed": n, "avg_launch_ms": round(avg_s * 1e3, 4),
                 "flops_per_launch": launch_flops}
+    permute_alone = not hbm["zigzag_permute_kernel"] and w.layout == "zigzag"
+    if permute_alone:
+        # the step addresses rows by position and runs no permute: time the
+        # permute kernel alone on one input (forward and inverse), untimed
+        # for the step
+        src = dev_in[0]
+        scratch = torch.empty_like(src)
+        timing_on[0] = True
+        for inv in (0, 1, 0, 1):
+            sca.sharded.capi.zigzag_permute(src.data_ptr() if inv == 0 else scratch.data_ptr(),
+                                            scratch.data_ptr() if inv == 0 else src.data_ptr(),
+                                            w.B * w.H, w.S, w.D * src.element_size(), w.P, inv, stream.cuda_stream)
+        timing_on[0] = False
+        torch.cuda.synchronize()
+        del scratch
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    hbm_stats = {}
+    for name, evs in hbm.items():
+        if evs:
+            t = sum(a.elapsed_time(b) for a, b, _ in evs) * 1e-3
+            nb = sum(x for _, _, x in evs)
+            hbm_stats[name] = {"launches": len(evs), "avg_launch_ms": round(t / len(evs) * 1e3, 4),
+                               "gbs": round(nb / t / 1e9, 1), "frac": round(nb / t / 1e9 / hbm_peak, 4),
+                               "bytes_per_launch": nb // len(evs)}
+    if permute_alone and "zigzag_permute_kernel" in hbm_stats:
+        hbm_stats["zigzag_permute_kernel"]["note"] = "timed alone: the step addresses rows by position"
     other = {k: {"avg_launch_ms": round(v[0] / v[1], 4), "launches": v[1],
-                 "tflops": round(flops(w, fwd=(k == "fwd"), bwd=(k == "bwd")) / w.P / (v[0] / v[1] * 1e-3) / 1e12, 2)}
+                 "tflops": round(flops(w, fwd=(k == "fwd"), bwd=(k == "bwd")) * args.steps / v[0] * 1e-9, 2)}
              for k, v in per.items()}
 
     line = {
@@ -335,7 +395,8 @@ def run_gpu(args):
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded N(0,1))",
         "config": {"workload": w.description, "name": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "P": w.P,
-                   "layout": w.layout, "schedule": w.schedule, "head_groups": w.head_groups,
+                   "layout": w.layout, "schedule": w.schedule, "addressing": plan.addressing,
+                   "head_groups": w.head_groups,
                    "step": "fwd+bwd" if w.backward else "fwd",
                    "flops_per_step": step_flops, "l2": "inputs larger than L2 (no flush)"
                    if sum(x.numel() * x.element_size() for x in inputs) > L2_BYTES else "inputs fit in L2",
@@ -346,6 +407,7 @@ def run_gpu(args):
         "gpu_launches": launches,
         "roofline": roofline,
         "kernels": other,
+        "hbm_kernels": {"peak_gbs": hbm_peak, "peak_source": f"{peak_src} copy bandwidth", **hbm_stats},
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
@@ -435,6 +497,9 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="train_s32k")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--schedule", choices=["ring", "direct", "fused"], default=None,
+                    help="override the workload's schedule")
+    ap.add_argument("--addressing", choices=["auto", "position", "permuted"], default="auto")
     ap.add_argument("--heads", type=int, default=0,
                     help="override the head count (profiler captures of a smaller case; not a bench line)")
     args = ap.parse_args()

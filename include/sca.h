@@ -90,6 +90,15 @@ typedef struct {
   sca_view o;          /* fp32 o (forward) / dq (backward) view              */
   sca_view dkv;        /* fp32 dk, dv view (backward only)                   */
   int64_t lse_b, lse_h;/* fp32 lse (and delta) strides; row stride is 1       */
+  /* Row addressing.  0: slab row i of an item is row i of the tensor
+   * (shard-major slabs).  1: it is row pos(i) of the tensor, its global
+   * position from the item's segment map (natural order: the zigzag map
+   * folded into the addressing, no permuted copy).  By-position segments
+   * must be multiples of 128 rows (SCA_ERR_UNSUPPORTED otherwise). */
+  int32_t q_by_pos;    /* q, o, lse (forward); q, dout, dq, lse, delta (bwd) */
+  int32_t kv_by_pos;   /* k, v                                               */
+  int32_t dkv_by_pos;  /* dk, dv (backward only)                             */
+  int32_t reserved;    /* 0                                                  */
 } sca_attn_dims;
 
 /* One (query shard, key/value block) work item of the forward. */
@@ -162,6 +171,19 @@ int zigzag_permute(const void* src, void* dst, int64_t outer, int64_t S, int64_t
  * Enfoques Existentes").  Errors: SCA_ERR_ARG for out-of-range rows. */
 int ring_stage_block(const void* src, void* dst, int64_t outer, int64_t S_src, int64_t row0,
                      int64_t rows, int64_t row_bytes, void* stream);
+
+/* ring_stage_segments - the same hand-off for a block kept in natural order:
+ * its rows are the `seg->n` segments of `seg->len` rows starting at rows
+ * seg->start[i] of every (b, h) of a [outer, S_src, row] tensor (a zigzag
+ * shard: chunks r and 2P-1-r), gathered in segment order into a contiguous
+ * [outer, seg->n * seg->len, row] staging slab, one strided 2-D copy-engine
+ * copy per segment (double buffering of the METP abstract; block passing of
+ * "Avances en la capacitacion de LLMs de secuencia larga", section
+ * "Limitaciones de los Enfoques Existentes").  The caller owns both buffers;
+ * they must not overlap.  Errors: SCA_ERR_ARG for NULL pointers, segment
+ * counts outside {1, 2}, rows outside [0, S_src). */
+int ring_stage_segments(const void* src, void* dst, int64_t outer, int64_t S_src, const sca_segs* seg,
+                        int64_t row_bytes, void* stream);
 
 /* One (query shard, key/value block) work item of the backward.  dq, dk, dv
  * are fp32: with dims->accumulate = 1 the item ADDS its contribution, with 0

@@ -30,8 +30,8 @@ SCA_ALGO_SIMT = 1
 SCA_ALGO_TC = 2
 SCA_MAX_ITEMS = 32
 
-EXPORTED = ("attn_fwd_shard", "attn_merge_lse", "zigzag_permute", "ring_stage_block", "attn_bwd_shard",
-            "attn_bwd_delta", "sca_last_error", "sca_read_status", "sca_version")
+EXPORTED = ("attn_fwd_shard", "attn_merge_lse", "zigzag_permute", "ring_stage_block", "ring_stage_segments",
+            "attn_bwd_shard", "attn_bwd_delta", "sca_last_error", "sca_read_status", "sca_version")
 
 
 class ScaError(RuntimeError):
@@ -51,7 +51,8 @@ class sca_view(ctypes.Structure):
 class sca_attn_dims(ctypes.Structure):
     _fields_ = [("B", c_int32), ("H", c_int32), ("D", c_int32), ("dtype", c_int32), ("causal", c_int32),
                 ("algo", c_int32), ("scale", c_float), ("accumulate", c_int32), ("q", sca_view), ("kv", sca_view),
-                ("o", sca_view), ("dkv", sca_view), ("lse_b", c_int64), ("lse_h", c_int64)]
+                ("o", sca_view), ("dkv", sca_view), ("lse_b", c_int64), ("lse_h", c_int64),
+                ("q_by_pos", c_int32), ("kv_by_pos", c_int32), ("dkv_by_pos", c_int32), ("reserved", c_int32)]
 
 
 class sca_fwd_item(ctypes.Structure):
@@ -77,6 +78,7 @@ def _load():
                                    c_void_p, c_void_p, c_int, c_int64, c_void_p]),
         "zigzag_permute": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int, c_int, c_void_p]),
         "ring_stage_block": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_int64, c_void_p]),
+        "ring_stage_segments": (c_int, [c_void_p, c_void_p, c_int64, c_int64, POINTER(sca_segs), c_int64, c_void_p]),
         "attn_bwd_shard": (c_int, [POINTER(sca_bwd_item), c_int, POINTER(sca_attn_dims), c_void_p, c_void_p]),
         "attn_bwd_delta": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int64, c_int, c_void_p]),
         "sca_last_error": (c_char_p, []),
@@ -142,6 +144,11 @@ def zigzag_permute(src: int, dst: int, outer: int, S: int, row_bytes: int, P: in
 def ring_stage_block(src: int, dst: int, outer: int, S_src: int, row0: int, rows: int, row_bytes: int,
                      stream: int) -> int:
     return check(lib().ring_stage_block(src, dst, outer, S_src, row0, rows, row_bytes, stream))
+
+
+def ring_stage_segments(src: int, dst: int, outer: int, S_src: int, seg: sca_segs, row_bytes: int,
+                        stream: int) -> int:
+    return check(lib().ring_stage_segments(src, dst, outer, S_src, ctypes.byref(seg), row_bytes, stream))
 
 
 def attn_bwd_delta(o: int, dout: int, dout_dtype: int, delta: int, rows: int, D: int, stream: int) -> int:

@@ -42,6 +42,21 @@ static int check_dims(const sca_attn_dims* d, bool bwd) {
   SCA_REQUIRE(d->q.s >= d->D && d->kv.s >= d->D && d->o.s >= d->D && (!bwd || d->dkv.s >= d->D), SCA_ERR_ARG,
               "row strides must be >= D");
   SCA_REQUIRE(d->lse_b >= 0 && d->lse_h >= 0, SCA_ERR_ARG, "negative lse stride");
+  SCA_REQUIRE((d->q_by_pos == 0 || d->q_by_pos == 1) && (d->kv_by_pos == 0 || d->kv_by_pos == 1) &&
+                  (d->dkv_by_pos == 0 || d->dkv_by_pos == 1),
+              SCA_ERR_ARG, "q_by_pos, kv_by_pos, dkv_by_pos must be 0 or 1");
+  SCA_REQUIRE(bwd || d->dkv_by_pos == 0, SCA_ERR_ARG, "dkv_by_pos applies to the backward only");
+  return SCA_OK;
+}
+
+// A by-position slab is read and written in 128-row tiles that must not
+// straddle two segments.
+static int check_by_pos(const sca_segs& s, bool by_pos, const char* what, int idx) {
+  SCA_REQUIRE(!by_pos || s.len % 128 == 0, SCA_ERR_UNSUPPORTED,
+              "item %d: %s addressed by position needs segments of a multiple of 128 rows (len=%lld)", idx, what,
+              static_cast<long long>(s.len));
+  for (int i = 0; by_pos && i < s.n; ++i)
+    SCA_REQUIRE(s.start[i] >= 0, SCA_ERR_ARG, "item %d: %s addressed by position has a negative start", idx, what);
   return SCA_OK;
 }
 
@@ -62,6 +77,9 @@ static void fill_common(AttnArgs& a, const sca_attn_dims* d, int n_items, int* d
   a.lse_h = d->lse_h;
   a.status = dev_status;
   a.max_q_tiles = a.max_k_tiles = 0;
+  a.q_by_pos = d->q_by_pos;
+  a.kv_by_pos = d->kv_by_pos;
+  a.dkv_by_pos = d->dkv_by_pos;
 }
 
 static bool use_tc(const sca_attn_dims* d) {
@@ -87,6 +105,8 @@ extern "C" int attn_fwd_shard(const sca_fwd_item* items, int n_items, const sca_
     const sca_fwd_item& x = items[i];
     if ((rc = check_segs(x.q_pos, "q_pos", i)) != SCA_OK) return rc;
     if ((rc = check_segs(x.kv_pos, "kv_pos", i)) != SCA_OK) return rc;
+    if ((rc = check_by_pos(x.q_pos, dims->q_by_pos, "q", i)) != SCA_OK) return rc;
+    if ((rc = check_by_pos(x.kv_pos, dims->kv_by_pos, "k/v", i)) != SCA_OK) return rc;
     SCA_REQUIRE(x.q && x.k && x.v && x.o && x.lse, SCA_ERR_ARG, "item %d: NULL pointer", i);
     SCA_REQUIRE(aligned(x.q, in_align) && aligned(x.k, in_align) && aligned(x.v, in_align) && aligned(x.o, 16) &&
                     aligned(x.lse, 4),
@@ -131,6 +151,9 @@ extern "C" int attn_bwd_shard(const sca_bwd_item* items, int n_items, const sca_
     const sca_bwd_item& x = items[i];
     if ((rc = check_segs(x.q_pos, "q_pos", i)) != SCA_OK) return rc;
     if ((rc = check_segs(x.kv_pos, "kv_pos", i)) != SCA_OK) return rc;
+    if ((rc = check_by_pos(x.q_pos, dims->q_by_pos, "q", i)) != SCA_OK) return rc;
+    if ((rc = check_by_pos(x.kv_pos, dims->kv_by_pos, "k/v", i)) != SCA_OK) return rc;
+    if ((rc = check_by_pos(x.kv_pos, dims->dkv_by_pos, "dk/dv", i)) != SCA_OK) return rc;
     SCA_REQUIRE(x.q && x.k && x.v && x.dout && x.lse && x.delta && x.dq && x.dk && x.dv, SCA_ERR_ARG,
                 "item %d: NULL pointer", i);
     SCA_REQUIRE(aligned(x.q, 16) && aligned(x.k, 16) && aligned(x.v, 16) && aligned(x.dout, 16) &&

@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(kSimtThreads) fwd_simt_kernel(const __grid_con
   tile_pos_range(it.qs, q0, nq, qmin, qmax);
 
   float4 qv[NF], acc[NF];
-  const T* qp = static_cast<const T*>(it.q) + b * a.q.b + h * a.q.h + (valid ? qrow : 0) * a.q.s;
+  const int64_t qr = slab_row(it.qs, a.q_by_pos, valid ? qrow : 0);   // tensor row
+  const T* qp = static_cast<const T*>(it.q) + b * a.q.b + h * a.q.h + qr * a.q.s;
 #pragma unroll
   for (int t = 0; t < NF; ++t) {
     qv[t] = load4<T>(qp + 4 * (ql + 4 * t));
@@ -94,8 +95,9 @@ __global__ void __launch_bounds__(kSimtThreads) fwd_simt_kernel(const __grid_con
     if (a.causal && kmin > qmax) continue;
     const bool full = nk == kSimtKeys && (!a.causal || kmax <= qmin);
     __syncthreads();
-    load_rows<D, T>(Ks, kb + k0 * a.kv.s, a.kv.s, nk);
-    load_rows<D, T>(Vs, vb + k0 * a.kv.s, a.kv.s, nk);
+    const int64_t kr0 = slab_row(it.ks, a.kv_by_pos, k0);   // a tile never straddles segments
+    load_rows<D, T>(Ks, kb + kr0 * a.kv.s, a.kv.s, nk);
+    load_rows<D, T>(Vs, vb + kr0 * a.kv.s, a.kv.s, nk);
     __syncthreads();
 #pragma unroll 1
     for (int j0 = 0; j0 < kSimtKeys; j0 += 8) {
@@ -135,13 +137,13 @@ __global__ void __launch_bounds__(kSimtThreads) fwd_simt_kernel(const __grid_con
   }
   if (!valid) return;
   const float inv = l > 0.f ? 1.f / l : 0.f;
-  float* op = it.o + b * a.o.b + h * a.o.h + qrow * a.o.s;
+  float* op = it.o + b * a.o.b + h * a.o.h + qr * a.o.s;
 #pragma unroll
   for (int t = 0; t < NF; ++t) {
     const float4 r = make_float4(acc[t].x * inv, acc[t].y * inv, acc[t].z * inv, acc[t].w * inv);
     *reinterpret_cast<float4*>(op + 4 * (ql + 4 * t)) = r;
   }
-  if (ql == 0) it.lse[b * a.lse_b + h * a.lse_h + qrow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+  if (ql == 0) it.lse[b * a.lse_b + h * a.lse_h + qr] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
 // ----------------------------------------------------------- backward: dq
@@ -158,7 +160,7 @@ __global__ void __launch_bounds__(kSimtThreads) dq_simt_kernel(const __grid_cons
   const int ql = threadIdx.x & 3, rr = threadIdx.x >> 2;
   const int64_t qrow = q0 + rr;
   const bool valid = qrow < it.Sq;
-  const int64_t qr = valid ? qrow : 0;
+  const int64_t qr = slab_row(it.qs, a.q_by_pos, valid ? qrow : 0);   // tensor row
   const int64_t qpos = valid ? seg_pos(it.qs, qrow) : INT64_MIN;
   const int nq = static_cast<int>(min64(kSimtRows, it.Sq - q0));
   int64_t qmin, qmax;
@@ -187,8 +189,9 @@ __global__ void __launch_bounds__(kSimtThreads) dq_simt_kernel(const __grid_cons
     tile_pos_range(it.ks, k0, nk, kmin, kmax);
     if (a.causal && kmin > qmax) continue;
     __syncthreads();
-    load_rows<D, T>(Ks, kb + k0 * a.kv.s, a.kv.s, nk);
-    load_rows<D, T>(Vs, vb + k0 * a.kv.s, a.kv.s, nk);
+    const int64_t kr0 = slab_row(it.ks, a.kv_by_pos, k0);   // a tile never straddles segments
+    load_rows<D, T>(Ks, kb + kr0 * a.kv.s, a.kv.s, nk);
+    load_rows<D, T>(Vs, vb + kr0 * a.kv.s, a.kv.s, nk);
     __syncthreads();
 #pragma unroll 2
     for (int j = 0; j < kSimtKeys; ++j) {
@@ -208,7 +211,7 @@ __global__ void __launch_bounds__(kSimtThreads) dq_simt_kernel(const __grid_cons
     }
   }
   if (!valid) return;
-  float* out = it.o + b * a.o.b + h * a.o.h + qrow * a.o.s;
+  float* out = it.o + b * a.o.b + h * a.o.h + qr * a.o.s;
 #pragma unroll
   for (int t = 0; t < NF; ++t) {
     float4* p4 = reinterpret_cast<float4*>(out + 4 * (ql + 4 * t));
@@ -234,7 +237,8 @@ __global__ void __launch_bounds__(kSimtThreads) dkv_simt_kernel(const __grid_con
   const int ql = threadIdx.x & 3, rr = threadIdx.x >> 2;
   const int64_t krow = k0 + rr;
   const bool valid = krow < it.Skv;
-  const int64_t kr = valid ? krow : 0;
+  const int64_t kr = slab_row(it.ks, a.kv_by_pos, valid ? krow : 0);   // tensor rows of k/v and dk/dv
+  const int64_t dkr = slab_row(it.ks, a.dkv_by_pos, valid ? krow : 0);
   const int64_t kpos = valid ? seg_pos(it.ks, krow) : INT64_MAX;
   const int nk = static_cast<int>(min64(kSimtRows, it.Skv - k0));
   int64_t kmin, kmax;
@@ -262,13 +266,14 @@ __global__ void __launch_bounds__(kSimtThreads) dkv_simt_kernel(const __grid_con
     tile_pos_range(it.qs, r0, nq, qmin, qmax);
     if (a.causal && kmin > qmax) continue;
     __syncthreads();
-    load_rows<D, T>(Qs, qb + r0 * a.q.s, a.q.s, nq);
-    load_rows<D, T>(Ds, db + r0 * a.q.s, a.q.s, nq);
+    const int64_t qr0 = slab_row(it.qs, a.q_by_pos, r0);   // a tile never straddles segments
+    load_rows<D, T>(Qs, qb + qr0 * a.q.s, a.q.s, nq);
+    load_rows<D, T>(Ds, db + qr0 * a.q.s, a.q.s, nq);
     if (threadIdx.x < kSimtKeys) {
       const int i = threadIdx.x;
       const bool ok = i < nq;
-      Ls[i] = ok ? lb[r0 + i] : -INFINITY;
-      Dl[i] = ok ? dlb[r0 + i] : 0.f;
+      Ls[i] = ok ? lb[qr0 + i] : -INFINITY;
+      Dl[i] = ok ? dlb[qr0 + i] : 0.f;
       Ps[i] = ok ? seg_pos(it.qs, r0 + i) : INT64_MIN;
     }
     __syncthreads();
@@ -294,8 +299,8 @@ __global__ void __launch_bounds__(kSimtThreads) dkv_simt_kernel(const __grid_con
     }
   }
   if (!valid) return;
-  float* dkp = it.dk + b * a.dkv.b + h * a.dkv.h + krow * a.dkv.s;
-  float* dvp = it.dv + b * a.dkv.b + h * a.dkv.h + krow * a.dkv.s;
+  float* dkp = it.dk + b * a.dkv.b + h * a.dkv.h + dkr * a.dkv.s;
+  float* dvp = it.dv + b * a.dkv.b + h * a.dkv.h + dkr * a.dkv.s;
 #pragma unroll
   for (int t = 0; t < NF; ++t) {
     float4* pk = reinterpret_cast<float4*>(dkp + 4 * (ql + 4 * t));

@@ -158,8 +158,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   if (n_vis == 0) {
     // no query sees these keys: overwrite mode still owes zeros
     if (!a.accumulate && threadIdx.x < nk) {
-      float* pk = dk_base + (k0 + threadIdx.x) * a.dkv.s;
-      float* pv = dv_base + (k0 + threadIdx.x) * a.dkv.s;
+      const int64_t r = slab_row(gm.ks, a.dkv_by_pos, k0 + threadIdx.x);
+      float* pk = dk_base + r * a.dkv.s;
+      float* pv = dv_base + r * a.dkv.s;
       for (int c = 0; c < D; c += 4) {
         *reinterpret_cast<float4*>(pk + c) = make_float4(0.f, 0.f, 0.f, 0.f);
         *reinterpret_cast<float4*>(pv + c) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -217,8 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       tma_prefetch_map(mdq);
       mbar_arrive_expect_tx(&bars->kv_full, 2 * L::TILE);
       for (int p = 0; p < D / 64; ++p) {
-        tma_load_4d(smem + L::K_OFF + p * PANEL, mk, &bars->kv_full, 64 * p, static_cast<int>(k0), h, b);
-        tma_load_4d(smem + L::V_OFF + p * PANEL, mv, &bars->kv_full, 64 * p, static_cast<int>(k0), h, b);
+        const int krow0 = static_cast<int>(slab_row(gm.ks, a.kv_by_pos, k0));
+        tma_load_4d(smem + L::K_OFF + p * PANEL, mk, &bars->kv_full, 64 * p, krow0, h, b);
+        tma_load_4d(smem + L::V_OFF + p * PANEL, mv, &bars->kv_full, 64 * p, krow0, h, b);
       }
     }
     const float* lse_base = it.lse + b * a.lse_b + h * a.lse_h;
@@ -251,13 +253,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     for (int t; (t = cur.next(nqt, lane, qvis)) >= 0;) {
       const QTile qt = q_tile(gm, t, causal, nk, kmin, kmax);
       const int st = n & 1;
+      // tensor row of the tile's first query (a tile never straddles two
+      // segments when rows are addressed by position)
+      const int qrow0 = static_cast<int>(slab_row(gm.qs, a.q_by_pos, qt.q0));
       // lse/delta of this tile into registers while the stage drains
       float lse_r[BM / 32], dl_r[BM / 32];
 #pragma unroll
       for (int k = 0; k < BM / 32; ++k) {
         const int i = lane + 32 * k;
-        lse_r[k] = i < qt.nq ? lse_base[qt.q0 + i] : -INFINITY;
-        dl_r[k] = i < qt.nq ? dl_base[qt.q0 + i] : 0.f;
+        lse_r[k] = i < qt.nq ? lse_base[qrow0 + i] : -INFINITY;
+        dl_r[k] = i < qt.nq ? dl_base[qrow0 + i] : 0.f;
       }
       // Q stage st (and its lse/delta slot) is free once the MMAs of tile
       // n-2 have completed
@@ -268,8 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars->q_full[st], L::TILE);
         for (int p = 0; p < D / 64; ++p)
-          tma_load_4d(smem + L::Q_OFF + st * L::TILE + p * PANEL, mq, &bars->q_full[st], 64 * p,
-                      static_cast<int>(qt.q0), h, b);
+          tma_load_4d(smem + L::Q_OFF + st * L::TILE + p * PANEL, mq, &bars->q_full[st], 64 * p, qrow0, h, b);
       }
       float* l2s = lse_sm + st * 2 * BM;
 #pragma unroll
@@ -288,12 +292,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
       }
-      if (st) q0_st1 = static_cast<int>(qt.q0); else q0_st0 = static_cast<int>(qt.q0);
+      if (st) q0_st1 = qrow0; else q0_st0 = qrow0;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars->do_full[st], L::TILE);
         for (int p = 0; p < D / 64; ++p)
-          tma_load_4d(smem + L::DO_OFF + st * L::TILE + p * PANEL, mo, &bars->do_full[st], 64 * p,
-                      static_cast<int>(qt.q0), h, b);
+          tma_load_4d(smem + L::DO_OFF + st * L::TILE + p * PANEL, mo, &bars->do_full[st], 64 * p, qrow0, h, b);
       }
       ++n;
     }
@@ -587,13 +590,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       mbar_arrive(&bars->epi_staged[wg]);
       if ((threadIdx.x & 127) == 0 && mbar_wait(&bars->epi_staged[wg], 0, abort, status)) {
         const CUtensorMap* m = &ta.maps[item_idx][wg == 0 ? 5 : 6];
+        const int dkrow0 = static_cast<int>(slab_row(gm.ks, a.dkv_by_pos, k0));
         const uint8_t* base = smem + (wg == 0 ? L::K_OFF : L::Q_OFF);
 #pragma unroll
         for (int bx = 0; bx < D / 32; ++bx) {
           if (a.accumulate)
-            tma_reduce_add_4d(m, base + bx * PANEL, 32 * bx, static_cast<int>(k0), h, b);
+            tma_reduce_add_4d(m, base + bx * PANEL, 32 * bx, dkrow0, h, b);
           else
-            tma_store_4d(m, base + bx * PANEL, 32 * bx, static_cast<int>(k0), h, b);
+            tma_store_4d(m, base + bx * PANEL, 32 * bx, dkrow0, h, b);
         }
         bulk_commit();
         bulk_wait_all();
@@ -639,12 +643,19 @@ cudaError_t tc_backward(AttnArgs& a, cudaStream_t st) {
     for (int i = 0; i < a.n_items; ++i) {
       const Item& it = a.items[i];
       if (it.Sq == 0) continue;
-      for (int bb = 0; bb < a.B; ++bb) {
-        const size_t width = static_cast<size_t>(it.Sq * a.D) * 4;
-        const size_t pitch = a.H > 1 ? static_cast<size_t>(a.o.h) * 4 : width;   // one head: pitch unused
-        if (pitch < width) return cudaErrorNotSupported;
-        cudaError_t e = cudaMemset2DAsync(it.o + bb * a.o.b, pitch, 0, width, static_cast<size_t>(a.H), st);
-        if (e != cudaSuccess) return e;
+      // the item's dq rows: its slab, or each segment at its positions
+      const int parts = a.q_by_pos ? it.qs.n : 1;
+      for (int sgm = 0; sgm < parts; ++sgm) {
+        const int64_t row0 = a.q_by_pos ? (sgm == 0 ? it.qs.start0 : it.qs.start1) : 0;
+        const int64_t nrows = a.q_by_pos ? it.qs.len : it.Sq;
+        for (int bb = 0; bb < a.B; ++bb) {
+          const size_t width = static_cast<size_t>(nrows * a.D) * 4;
+          const size_t pitch = a.H > 1 ? static_cast<size_t>(a.o.h) * 4 : width;   // one head: pitch unused
+          if (pitch < width) return cudaErrorNotSupported;
+          cudaError_t e = cudaMemset2DAsync(it.o + bb * a.o.b + row0 * a.D, pitch, 0, width,
+                                            static_cast<size_t>(a.H), st);
+          if (e != cudaSuccess) return e;
+        }
       }
     }
   }
@@ -661,13 +672,15 @@ cudaError_t tc_backward(AttnArgs& a, cudaStream_t st) {
       if (t > mt) mt = t;
       CUtensorMap* m = ta.maps[i];
       cudaError_t e;
-      if ((e = make_tmap_bf16(&m[0], it.q, a.D, it.Sq, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
-      if ((e = make_tmap_bf16(&m[1], it.k, a.D, it.Skv, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
-      if ((e = make_tmap_bf16(&m[2], it.v, a.D, it.Skv, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
-      if ((e = make_tmap_bf16(&m[3], it.dout, a.D, it.Sq, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
-      if ((e = make_tmap_f32(&m[4], it.o, a.D, it.Sq, a.H, a.B, a.o, 32, BM)) != cudaSuccess) return e;
-      if ((e = make_tmap_f32(&m[5], it.dk, a.D, it.Skv, a.H, a.B, a.dkv, 32, BN)) != cudaSuccess) return e;
-      if ((e = make_tmap_f32(&m[6], it.dv, a.D, it.Skv, a.H, a.B, a.dkv, 32, BN)) != cudaSuccess) return e;
+      const int64_t qr = slab_extent(it.qs, a.q_by_pos), kr = slab_extent(it.ks, a.kv_by_pos),
+                    dkr = slab_extent(it.ks, a.dkv_by_pos);
+      if ((e = make_tmap_bf16(&m[0], it.q, a.D, qr, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
+      if ((e = make_tmap_bf16(&m[1], it.k, a.D, kr, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
+      if ((e = make_tmap_bf16(&m[2], it.v, a.D, kr, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
+      if ((e = make_tmap_bf16(&m[3], it.dout, a.D, qr, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
+      if ((e = make_tmap_f32(&m[4], it.o, a.D, qr, a.H, a.B, a.o, 32, BM)) != cudaSuccess) return e;
+      if ((e = make_tmap_f32(&m[5], it.dk, a.D, dkr, a.H, a.B, a.dkv, 32, BN)) != cudaSuccess) return e;
+      if ((e = make_tmap_f32(&m[6], it.dv, a.D, dkr, a.H, a.B, a.dkv, 32, BN)) != cudaSuccess) return e;
     }
     if (mt == 0) continue;
     ta.a.max_k_tiles = static_cast<int>(mt);

@@ -38,6 +38,20 @@ __host__ __device__ __forceinline__ int64_t seg_pos(const Segs& s, int64_t i) {
   return i < s.len ? s.start0 + i : s.start1 + (i - s.len);
 }
 
+// Tensor row of slab row i: i itself, or its global position when the
+// tensor is addressed by position (natural order).
+__host__ __device__ __forceinline__ int64_t slab_row(const Segs& s, bool by_pos, int64_t i) {
+  return by_pos ? seg_pos(s, i) : i;
+}
+
+// Rows a tensor must span to hold a slab of n*len rows: n*len, or past the
+// last global position when addressed by position.
+__host__ __device__ __forceinline__ int64_t slab_extent(const Segs& s, bool by_pos) {
+  if (!by_pos) return static_cast<int64_t>(s.n) * s.len;
+  const int64_t e0 = s.start0 + s.len, e1 = s.n > 1 ? s.start1 + s.len : 0;
+  return e0 > e1 ? e0 : e1;
+}
+
 // Positions of a tile of slab rows [r0, r0 + cnt) (cnt >= 1, at most two
 // segment parts): min and max global position.
 __host__ __device__ __forceinline__ void tile_pos_range(const Segs& s, int64_t r0, int64_t cnt,
@@ -128,6 +142,7 @@ struct AttnArgs {
   float scale_log2;   // scale * log2(e)
   int32_t max_q_tiles;
   int32_t max_k_tiles;
+  int32_t q_by_pos, kv_by_pos, dkv_by_pos;   // row addressing (see sca_attn_dims)
   int* status;
 };
 

@@ -131,9 +131,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (warp < 8) {
       const int row = (warp & 3) * 32 + lane, g = warp >> 2;
       if (row < nq) {
-        float* op = it.o + b * a.o.b + h * a.o.h + (q0 + row) * a.o.s + g * (D / 2);
+        const int64_t orow = slab_row(gm.qs, a.q_by_pos, q0 + row);
+        float* op = it.o + b * a.o.b + h * a.o.h + orow * a.o.s + g * (D / 2);
         for (int c = 0; c < D / 2; c += 4) *reinterpret_cast<float4*>(op + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (g == 0) it.lse[b * a.lse_b + h * a.lse_h + q0 + row] = -INFINITY;
+        if (g == 0) it.lse[b * a.lse_b + h * a.lse_h + orow] = -INFINITY;
       }
     }
     return;
@@ -189,7 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       tma_prefetch_map(mk);
       mbar_arrive_expect_tx(&bars->q_full, L::TILE);
       for (int p = 0; p < D / 64; ++p)
-        tma_load_4d(smem + L::Q_OFF + p * PANEL, mq, &bars->q_full, 64 * p, static_cast<int>(q0), h, b);
+        tma_load_4d(smem + L::Q_OFF + p * PANEL, mq, &bars->q_full, 64 * p,
+                    static_cast<int>(slab_row(gm.qs, a.q_by_pos, q0)), h, b);
     }
     int n = 0;
     TileCursor cur;
@@ -200,7 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         w = 1;
         mbar_arrive_expect_tx(&bars->k_full[st], L::TILE);
         for (int p = 0; p < D / 64; ++p)
-          tma_load_4d(smem + L::K_OFF + st * L::TILE + p * PANEL, mk, &bars->k_full[st], 64 * p, kt * BN, h, b);
+          tma_load_4d(smem + L::K_OFF + st * L::TILE + p * PANEL, mk, &bars->k_full[st], 64 * p,
+                      static_cast<int>(slab_row(gm.ks, a.kv_by_pos, static_cast<int64_t>(kt) * BN)), h, b);
       }
       if (!__shfl_sync(0xffffffffu, w, 0)) break;
       ++n;
@@ -222,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         w = 1;
         mbar_arrive_expect_tx(&bars->v_full[st], L::TILE);
         for (int p = 0; p < D / 64; ++p)
-          tma_load_4d(smem + L::V_OFF + st * L::TILE + p * PANEL, mv, &bars->v_full[st], 64 * p, kt * BN, h, b);
+          tma_load_4d(smem + L::V_OFF + st * L::TILE + p * PANEL, mv, &bars->v_full[st], 64 * p,
+                      static_cast<int>(slab_row(gm.ks, a.kv_by_pos, static_cast<int64_t>(kt) * BN)), h, b);
       }
       if (!__shfl_sync(0xffffffffu, w, 0)) break;
       ++n;
@@ -405,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-      float* op = it.o + b * a.o.b + h * a.o.h + (q0 + (row_valid ? row : 0)) * a.o.s + g * (D / 2);
+      const int64_t orow = slab_row(gm.qs, a.q_by_pos, q0 + (row_valid ? row : 0));
+      float* op = it.o + b * a.o.b + h * a.o.h + orow * a.o.s + g * (D / 2);
 #pragma unroll 1
       for (int c = 0; c < D / 2; c += 32) {
         uint32_t r[32];
@@ -421,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         }
       }
       if (row_valid && g == 0)
-        it.lse[b * a.lse_b + h * a.lse_h + q0 + row] = l_tot > 0.f ? (m_used + log2f(l_tot)) * kLn2 : -INFINITY;
+        it.lse[b * a.lse_b + h * a.lse_h + orow] = l_tot > 0.f ? (m_used + log2f(l_tot)) * kLn2 : -INFINITY;
     }
   }
 
@@ -462,9 +467,10 @@ cudaError_t tc_forward(AttnArgs& a, cudaStream_t st) {
     const int64_t t = (it.Sq + BM - 1) / BM;
     if (t > mt) mt = t;
     cudaError_t e;
-    if ((e = make_tmap_bf16(&ta.maps[i][0], it.q, a.D, it.Sq, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
-    if ((e = make_tmap_bf16(&ta.maps[i][1], it.k, a.D, it.Skv, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
-    if ((e = make_tmap_bf16(&ta.maps[i][2], it.v, a.D, it.Skv, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
+    const int64_t q_rows = slab_extent(it.qs, a.q_by_pos), kv_rows = slab_extent(it.ks, a.kv_by_pos);
+    if ((e = make_tmap_bf16(&ta.maps[i][0], it.q, a.D, q_rows, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&ta.maps[i][1], it.k, a.D, kv_rows, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&ta.maps[i][2], it.v, a.D, kv_rows, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
   }
   a.max_q_tiles = static_cast<int>(mt);
   ta.a = a;

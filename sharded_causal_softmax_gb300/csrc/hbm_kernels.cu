@@ -237,6 +237,32 @@ extern "C" int ring_stage_block(const void* src, void* dst, int64_t outer, int64
   return cuda_status(e, "ring_stage_block copy");
 }
 
+extern "C" int ring_stage_segments(const void* src, void* dst, int64_t outer, int64_t S_src, const sca_segs* seg,
+                                   int64_t row_bytes, void* stream) {
+  SCA_REQUIRE(src && dst && seg, SCA_ERR_ARG, "ring_stage_segments: NULL pointer");
+  SCA_REQUIRE(seg->n == 1 || seg->n == 2, SCA_ERR_ARG, "ring_stage_segments: seg->n=%d must be 1 or 2", seg->n);
+  SCA_REQUIRE(outer >= 0 && seg->len >= 0 && row_bytes > 0, SCA_ERR_ARG, "ring_stage_segments: negative size");
+  for (int i = 0; i < seg->n; ++i)
+    SCA_REQUIRE(seg->start[i] >= 0 && seg->start[i] + seg->len <= S_src, SCA_ERR_ARG,
+                "ring_stage_segments: segment %d rows [%lld, %lld) outside [0, %lld)", i,
+                static_cast<long long>(seg->start[i]), static_cast<long long>(seg->start[i] + seg->len),
+                static_cast<long long>(S_src));
+  if (outer == 0 || seg->len == 0) return SCA_OK;
+  const size_t width = static_cast<size_t>(seg->len * row_bytes);
+  const size_t dpitch = static_cast<size_t>(seg->n) * width;
+  SCA_REQUIRE(!overlap(src, outer * S_src * row_bytes,
+                       dst, outer * static_cast<int64_t>(dpitch)),
+              SCA_ERR_ARG, "ring_stage_segments: src and dst overlap");
+  for (int i = 0; i < seg->n; ++i) {
+    const char* s = static_cast<const char*>(src) + seg->start[i] * row_bytes;
+    const cudaError_t e = cudaMemcpy2DAsync(static_cast<char*>(dst) + i * width, dpitch, s,
+                                            static_cast<size_t>(S_src * row_bytes), width,
+                                            static_cast<size_t>(outer), cudaMemcpyDeviceToDevice, as_stream(stream));
+    if (e != cudaSuccess) return cuda_status(e, "ring_stage_segments copy");
+  }
+  return SCA_OK;
+}
+
 extern "C" int attn_merge_lse(const float* o_parts, const float* lse_parts, int n, int64_t rows, int D,
                               int64_t o_part_stride, int64_t lse_part_stride, float* o_out, float* lse_out,
                               void* o_bf16_out, int unpermute_P, int64_t S, void* stream) {

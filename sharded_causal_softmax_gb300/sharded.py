@@ -5,9 +5,13 @@ The schedule (host logic only; every byte is moved or computed by libsca):
 * Partition.  Zigzag (TSP page, "Zyphra presenta el paralelismo de secuencia
   y tensor (TSP)", section "Lo que realmente significa plegar"): the sequence
   is cut into 2P chunks of c rows and shard r owns chunks r and 2P-1-r, which
-  balances causal work; ``zigzag_permute`` lays Q, K, V out shard-major so a
-  shard is one contiguous slab of 2c rows per (batch, head).  Contiguous:
-  shard r owns rows [r S/P, (r+1) S/P) and nothing is permuted.
+  balances causal work.  Contiguous: shard r owns rows [r S/P, (r+1) S/P).
+* Addressing.  "position" (the default when every chunk is a multiple of 128
+  rows): the kernels read and write a shard's rows at their global positions
+  in the natural-order tensors, so the zigzag map lives in the TMA
+  coordinates and no permuted copy is made.  "permuted": ``zigzag_permute``
+  lays Q, K, V (and dO, lse, delta) out shard-major so a shard is one
+  contiguous slab, and the merge and the gradients undo it.
 * 2D split ("Avances en la capacitacion de LLMs de secuencia larga", section
   "Introduciendo la Atencion 2D"): G head groups x P context shards give
   G*P virtual ranks; rank (g, r) holds heads [g H/G, (g+1) H/G) of shard r.
@@ -19,13 +23,18 @@ The schedule (host logic only; every byte is moved or computed by libsca):
   engine on a side stream into the spare one of two staging buffers while
   step t computes (the double buffer of the METP abstract, FITEE
   10.1631/FITEE.2400602).  The "direct" schedule reads every block from its
-  home slab (the K/V all-gather reading of the TSP page).
+  home rows (the K/V all-gather reading of the TSP page).
 * Merge: the P partials of every row are combined exactly by log-sum-exp
-  rescaling, fused with the inverse zigzag permute (``attn_merge_lse``).
+  rescaling (``attn_merge_lse``), fused with the inverse permute when the
+  partials are shard-major.
+* "fused" schedule: all shards in one launch per direction.  Each CTA keeps
+  its running (m, l, O) over every key/value block, so there are no partials
+  and no merge; the backward writes each dK/dV row once.  One GPU holds
+  every block, so nothing is staged.
 * Backward: delta = rowsum(dO * O), then the same ring of steps; each step
   recomputes P from the final lse and adds into dQ of the rank's rows and
-  into dK/dV of the block's home rows (step 0 overwrites, so no zeroing pass
-  is needed); finally the gradients are permuted back to natural order.
+  into dK/dV of the block's rows (step 0 overwrites, so no zeroing pass is
+  needed).
 
 PyTorch supplies device memory, streams and events only.
 """
@@ -65,15 +74,19 @@ class ShardedCausalAttention:
     allocated per call.  Inputs are [B, H, S, D] tensors in natural order, of
     ``dtype`` (bf16 or fp32), contiguous, on the current CUDA device.
     Outputs are fp32 [B, H, S, D] (and lse [B, H, S], natural log).
+    ``backward`` reads the q, k, v of the last ``forward`` (kept by
+    reference) unless they are passed again.
     """
 
     def __init__(self, B, H, S, D, P, layout="zigzag", dtype=torch.bfloat16, head_groups=1,
                  schedule="ring", scale=None, causal=True, algo=capi.SCA_ALGO_AUTO, backward=False,
-                 bf16_out=False, device=None):
+                 bf16_out=False, device=None, addressing="auto"):
         if layout not in ("zigzag", "contiguous"):
             raise ValueError(f"layout {layout!r}")
-        if schedule not in ("ring", "direct"):
+        if schedule not in ("ring", "direct", "fused"):
             raise ValueError(f"schedule {schedule!r}")
+        if addressing not in ("auto", "position", "permuted"):
+            raise ValueError(f"addressing {addressing!r}")
         if dtype not in _DT:
             raise ValueError(f"dtype {dtype}")
         if S % (2 * P if layout == "zigzag" else P):
@@ -82,9 +95,19 @@ class ShardedCausalAttention:
             raise ValueError("head_groups must divide H")
         if head_groups * P > capi.SCA_MAX_ITEMS:
             raise ValueError(f"{head_groups * P} virtual ranks > {capi.SCA_MAX_ITEMS}")
+        zig = layout == "zigzag"
+        seg_len = S // (2 * P) if zig else S // P
+        if addressing == "auto":
+            addressing = "position" if seg_len % 128 == 0 else "permuted"
+        if addressing == "position" and seg_len % 128:
+            raise ValueError(f"position addressing needs shard segments of a multiple of 128 rows ({seg_len})")
         self.B, self.H, self.S, self.D, self.P = B, H, S, D, P
         self.G, self.Hg = head_groups, H // head_groups
         self.layout, self.schedule, self.dtype = layout, schedule, dtype
+        self.addressing = addressing
+        self.pos = addressing == "position"
+        fused = schedule == "fused"
+        self.perm = zig and not self.pos and not fused   # shard-major permuted copies
         self.scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
         self.causal, self.algo, self.backward_enabled = causal, algo, backward
         self.n_r = S // P                       # rows per shard
@@ -92,12 +115,11 @@ class ShardedCausalAttention:
         dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
         self.device = dev
         z = lambda *shape, dt=torch.float32: torch.empty(shape, dtype=dt, device=dev)
-        zig = layout == "zigzag"
-        self.qp = z(B, H, S, D, dt=dtype) if zig else None
-        self.kp = z(B, H, S, D, dt=dtype) if zig else None
-        self.vp = z(B, H, S, D, dt=dtype) if zig else None
-        self.o_parts = z(P, B, H, S, D)
-        self.lse_parts = z(P, B, H, S)
+        self.qp = z(B, H, S, D, dt=dtype) if self.perm else None
+        self.kp = z(B, H, S, D, dt=dtype) if self.perm else None
+        self.vp = z(B, H, S, D, dt=dtype) if self.perm else None
+        self.o_parts = z(P, B, H, S, D) if not fused else None
+        self.lse_parts = z(P, B, H, S) if not fused else None
         self.o = z(B, H, S, D)
         self.lse = z(B, H, S)
         self.o_bf16 = z(B, H, S, D, dt=torch.bfloat16) if bf16_out else None
@@ -110,16 +132,17 @@ class ShardedCausalAttention:
             self.dq = z(B, H, S, D)
             self.dk = z(B, H, S, D)
             self.dv = z(B, H, S, D)
-            self.dop = z(B, H, S, D, dt=dtype) if zig else None
-            self.lse_p = z(B, H, S) if zig else None
-            self.delta_p = z(B, H, S) if zig else None
-            self.dq_p = z(B, H, S, D) if zig else None
-            self.dk_p = z(B, H, S, D) if zig else None
-            self.dv_p = z(B, H, S, D) if zig else None
+            self.dop = z(B, H, S, D, dt=dtype) if self.perm else None
+            self.lse_p = z(B, H, S) if self.perm else None
+            self.delta_p = z(B, H, S) if self.perm else None
+            self.dq_p = z(B, H, S, D) if self.perm else None
+            self.dk_p = z(B, H, S, D) if self.perm else None
+            self.dv_p = z(B, H, S, D) if self.perm else None
         self.copy_stream = torch.cuda.Stream(device=dev) if ring else None
         self.ev_ready = torch.cuda.Event()
         self.ev_staged = [torch.cuda.Event() for _ in range(P)]
         self.ev_done = [torch.cuda.Event() for _ in range(P)]
+        self._inputs = None
         self.launches = 0   # kernels + copies issued by the last forward/backward
         self.kernels = 0    # kernels alone
 
@@ -129,6 +152,14 @@ class ShardedCausalAttention:
         capi.zigzag_permute(_ptr(src), _ptr(dst), self.B * self.H, self.S, row_bytes, self.P, inverse, stream)
         self.launches += 1
         self.kernels += 1
+
+    def _rows(self, g, r):
+        """Element offset (in rows of one head's sequence) of rank (g, r)'s
+        slab: the head group's first row, plus the shard's slab offset when
+        the tensors are shard-major (position addressing finds the rows by
+        their positions instead)."""
+        off = g * self.Hg * self.S
+        return off if self.pos else off + r * self.n_r
 
     # ------------------------------------------------- kernel descriptions
 
@@ -150,7 +181,7 @@ class ShardedCausalAttention:
     def kernels_per_attn_call(self, kind: str) -> int:
         return 2 if (kind == "bwd" and not self.uses_tensor_cores("bwd")) else 1
 
-    def _dims(self, kv_view, backward=False, accumulate=0):
+    def _dims(self, kv_view, backward=False, accumulate=0, q_by_pos=0, kv_by_pos=0, dkv_by_pos=0):
         d = capi.sca_attn_dims()
         d.B, d.H, d.D = self.B, self.Hg, self.D
         d.dtype = _DT[self.dtype]
@@ -164,6 +195,7 @@ class ShardedCausalAttention:
         d.o = capi.view(H * S * D, S * D, D)
         d.dkv = capi.view(H * S * D, S * D, D)
         d.lse_b, d.lse_h = H * S, S
+        d.q_by_pos, d.kv_by_pos, d.dkv_by_pos = int(q_by_pos), int(kv_by_pos), int(dkv_by_pos)
         return d
 
     def _home_kv_view(self):
@@ -177,7 +209,7 @@ class ShardedCausalAttention:
         P = self.P
         if self.stage_k is None or t == 0:
             j = ring_block(r, t, P)
-            off = (g * self.Hg * self.S + j * self.n_r) * self.D * self.eb
+            off = (g * self.Hg * self.S + (0 if self.pos else j * self.n_r)) * self.D * self.eb
             return _ptr(k_home) + off, _ptr(v_home) + off
         buf = t % 2
         return _ptr(self.stage_k[buf][g, r]), _ptr(self.stage_v[buf][g, r])
@@ -196,8 +228,12 @@ class ShardedCausalAttention:
                     for b in range(B):
                         off = ((b * self.H + g * Hg) * self.S) * row
                         for home, dst in ((k_home, dst_k), (v_home, dst_v)):
-                            capi.ring_stage_block(_ptr(home) + off, _ptr(dst[g, r, b]), Hg, self.S,
-                                                  src_r * n_r, n_r, row, cs)
+                            if self.pos:   # gather the block's chunks from natural order
+                                capi.ring_stage_segments(_ptr(home) + off, _ptr(dst[g, r, b]), Hg, self.S,
+                                                         shard_segs(self.S, P, self.layout, src_r), row, cs)
+                            else:
+                                capi.ring_stage_block(_ptr(home) + off, _ptr(dst[g, r, b]), Hg, self.S,
+                                                      src_r * n_r, n_r, row, cs)
                             self.launches += 1
             else:             # neighbours' staged blocks: a rotation by one rank
                 src_k, src_v = self.stage_k[(t_next - 1) % 2], self.stage_v[(t_next - 1) % 2]
@@ -209,8 +245,9 @@ class ShardedCausalAttention:
                     self.launches += 2
 
     def _ring(self, k_home, v_home, launch_step):
-        """Run launch_step(t, kv_ptrs(g, r), kv_view) for t = 0..P-1 with the
-        staging copies of step t+1 overlapped on the copy stream."""
+        """Run launch_step(t, kv_ptrs(g, r), kv_view, home) for t = 0..P-1
+        with the staging copies of step t+1 overlapped on the copy stream;
+        `home` says whether the blocks are read from their home rows."""
         cur = torch.cuda.current_stream(self.device)
         ring = self.stage_k is not None
         if ring:
@@ -225,8 +262,9 @@ class ShardedCausalAttention:
                     self.ev_staged[t + 1].record(self.copy_stream)
             if ring and t >= 1:
                 cur.wait_event(self.ev_staged[t])
-            view = self._home_kv_view() if (not ring or t == 0) else self._stage_kv_view()
-            launch_step(t, lambda g, r: self._kv_ptrs(k_home, v_home, t, g, r), view)
+            home = not ring or t == 0
+            view = self._home_kv_view() if home else self._stage_kv_view()
+            launch_step(t, lambda g, r: self._kv_ptrs(k_home, v_home, t, g, r), view, home)
             self.ev_done[t].record(cur)
         if ring:  # the staging buffers are reused by the next call
             cur.wait_stream(self.copy_stream)
@@ -236,10 +274,12 @@ class ShardedCausalAttention:
     def forward(self, q, k, v):
         self._check_inputs(q, k, v)
         self.launches = self.kernels = 0
+        self._inputs = (q, k, v)
         stream = torch.cuda.current_stream(self.device).cuda_stream
-        zig = self.layout == "zigzag"
+        if self.schedule == "fused":
+            return self._forward_fused(q, k, v, stream)
         row = self.D * self.eb
-        if zig:
+        if self.perm:
             self._permute(q, self.qp, row, 0, stream)
             self._permute(k, self.kp, row, 0, stream)
             self._permute(v, self.vp, row, 0, stream)
@@ -250,20 +290,21 @@ class ShardedCausalAttention:
         eb = self.eb
         st_ptr = _ptr(self.status)
 
-        def step(t, kv_ptrs, kv_view):
+        def step(t, kv_ptrs, kv_view, home):
             items = []
             for g in range(self.G):
                 for r in range(P):
                     it = capi.sca_fwd_item()
-                    hoff = g * self.Hg * S
-                    it.q = _ptr(qh) + (hoff + r * self.n_r) * D * eb
+                    rows = self._rows(g, r)
+                    it.q = _ptr(qh) + rows * D * eb
                     it.k, it.v = kv_ptrs(g, r)
-                    it.o = _ptr(self.o_parts[t]) + (hoff + r * self.n_r) * D * 4
-                    it.lse = _ptr(self.lse_parts[t]) + (hoff + r * self.n_r) * 4
+                    it.o = _ptr(self.o_parts[t]) + rows * D * 4
+                    it.lse = _ptr(self.lse_parts[t]) + rows * 4
                     it.q_pos = shard_segs(S, P, self.layout, r)
                     it.kv_pos = shard_segs(S, P, self.layout, ring_block(r, t, P))
                     items.append(it)
-            capi.attn_fwd_shard(items, self._dims(kv_view), st_ptr, stream)
+            dims = self._dims(kv_view, q_by_pos=self.pos, kv_by_pos=self.pos and home)
+            capi.attn_fwd_shard(items, dims, st_ptr, stream)
             self.launches += 1
             self.kernels += 1
 
@@ -271,29 +312,60 @@ class ShardedCausalAttention:
         rows = self.B * H * S
         capi.attn_merge_lse(_ptr(self.o_parts), _ptr(self.lse_parts), P, rows, D, rows * D, rows,
                             _ptr(self.o), _ptr(self.lse), _ptr(self.o_bf16) if self.o_bf16 is not None else 0,
-                            P if zig else 0, S, stream)
+                            P if self.perm else 0, S, stream)
         self.launches += 1
         self.kernels += 1
+        return self.o, self.lse
+
+    def _forward_fused(self, q, k, v, stream):
+        """Every shard in one launch: each head group is one item over the
+        whole sequence, so every CTA's online softmax runs over all blocks
+        and writes the final O and lse."""
+        S, D, eb = self.S, self.D, self.eb
+        items = []
+        for g in range(self.G):
+            rows = g * self.Hg * S
+            it = capi.sca_fwd_item()
+            it.q, it.k, it.v = _ptr(q) + rows * D * eb, _ptr(k) + rows * D * eb, _ptr(v) + rows * D * eb
+            it.o = _ptr(self.o) + rows * D * 4
+            it.lse = _ptr(self.lse) + rows * 4
+            it.q_pos = capi.segs(1, S, (0, 0))
+            it.kv_pos = capi.segs(1, S, (0, 0))
+            items.append(it)
+        capi.attn_fwd_shard(items, self._dims(self._home_kv_view()), _ptr(self.status), stream)
+        self.launches += 1
+        self.kernels += 1
+        if self.o_bf16 is not None:   # a one-partial merge is the bf16 rounding pass
+            rows = self.B * self.H * S
+            capi.attn_merge_lse(_ptr(self.o), _ptr(self.lse), 1, rows, D, rows * D, rows, _ptr(self.o),
+                                _ptr(self.lse), _ptr(self.o_bf16), 0, S, stream)
+            self.launches += 1
+            self.kernels += 1
         return self.o, self.lse
 
     # ----------------------------------------------------------- backward
 
     def backward(self, do, q=None, k=None, v=None):
-        """Gradients (dq, dk, dv) fp32 natural order, for the inputs of the
-        last ``forward`` (whose permuted copies are reused); for the
-        contiguous layout q, k, v must be passed again."""
+        """Gradients (dq, dk, dv) fp32 natural order for the inputs of the
+        last ``forward``."""
         if not self.backward_enabled:
             raise RuntimeError("plan built without backward=True")
+        if q is None:
+            if self._inputs is None:
+                raise RuntimeError("backward before forward")
+            q, k, v = self._inputs
+        self._check_inputs(do, q, k, v)
         self.launches = self.kernels = 0
         stream = torch.cuda.current_stream(self.device).cuda_stream
-        zig = self.layout == "zigzag"
         S, D, H, P, B = self.S, self.D, self.H, self.P, self.B
         eb = self.eb
-        rows = B * H * S
-        capi.attn_bwd_delta(_ptr(self.o), _ptr(do), _DT[self.dtype], _ptr(self.delta), rows, D, stream)
+        rows_all = B * H * S
+        capi.attn_bwd_delta(_ptr(self.o), _ptr(do), _DT[self.dtype], _ptr(self.delta), rows_all, D, stream)
         self.launches += 1
         self.kernels += 1
-        if zig:
+        if self.schedule == "fused":
+            return self._backward_fused(do, q, k, v, stream)
+        if self.perm:
             self._permute(do, self.dop, D * eb, 0, stream)
             self._permute(self.lse, self.lse_p, 4, 0, stream)
             self._permute(self.delta, self.delta_p, 4, 0, stream)
@@ -301,20 +373,17 @@ class ShardedCausalAttention:
             lse_h, dl_h = self.lse_p, self.delta_p
             dq, dk, dv = self.dq_p, self.dk_p, self.dv_p
         else:
-            if q is None:
-                raise ValueError("contiguous layout: pass q, k, v to backward")
             qh, kh, vh, doh = q, k, v, do
             lse_h, dl_h = self.lse, self.delta
             dq, dk, dv = self.dq, self.dk, self.dv
         st_ptr = _ptr(self.status)
 
-        def step(t, kv_ptrs, kv_view):
+        def step(t, kv_ptrs, kv_view, home):
             items = []
             for g in range(self.G):
                 for r in range(P):
                     j = ring_block(r, t, P)
-                    hoff = g * self.Hg * S
-                    qo, ko = hoff + r * self.n_r, hoff + j * self.n_r
+                    qo, ko = self._rows(g, r), self._rows(g, j)
                     it = capi.sca_bwd_item()
                     it.q = _ptr(qh) + qo * D * eb
                     it.dout = _ptr(doh) + qo * D * eb
@@ -327,16 +396,38 @@ class ShardedCausalAttention:
                     it.q_pos = shard_segs(S, P, self.layout, r)
                     it.kv_pos = shard_segs(S, P, self.layout, j)
                     items.append(it)
-            capi.attn_bwd_shard(items, self._dims(kv_view, backward=True, accumulate=1 if t > 0 else 0),
-                                st_ptr, stream)
+            dims = self._dims(kv_view, backward=True, accumulate=1 if t > 0 else 0, q_by_pos=self.pos,
+                              kv_by_pos=self.pos and home, dkv_by_pos=self.pos)
+            capi.attn_bwd_shard(items, dims, st_ptr, stream)
             self.launches += 1
             self.kernels += self.kernels_per_attn_call("bwd")
 
         self._ring(kh, vh, step)
-        if zig:
+        if self.perm:
             self._permute(dq, self.dq, D * 4, 1, stream)
             self._permute(dk, self.dk, D * 4, 1, stream)
             self._permute(dv, self.dv, D * 4, 1, stream)
+        return self.dq, self.dk, self.dv
+
+    def _backward_fused(self, do, q, k, v, stream):
+        """Every shard in one launch: each head group is one item over the
+        whole sequence; every key tile's dK/dV is complete in its CTA and
+        written once, dQ is summed over key tiles."""
+        S, D, eb = self.S, self.D, self.eb
+        items = []
+        for g in range(self.G):
+            rows = g * self.Hg * S
+            it = capi.sca_bwd_item()
+            it.q, it.k, it.v = _ptr(q) + rows * D * eb, _ptr(k) + rows * D * eb, _ptr(v) + rows * D * eb
+            it.dout = _ptr(do) + rows * D * eb
+            it.lse, it.delta = _ptr(self.lse) + rows * 4, _ptr(self.delta) + rows * 4
+            it.dq, it.dk, it.dv = (_ptr(x) + rows * D * 4 for x in (self.dq, self.dk, self.dv))
+            it.q_pos = capi.segs(1, S, (0, 0))
+            it.kv_pos = capi.segs(1, S, (0, 0))
+            items.append(it)
+        capi.attn_bwd_shard(items, self._dims(self._home_kv_view(), backward=True), _ptr(self.status), stream)
+        self.launches += 1
+        self.kernels += self.kernels_per_attn_call("bwd")
         return self.dq, self.dk, self.dv
 
     def read_status(self) -> int:

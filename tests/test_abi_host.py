@@ -55,6 +55,7 @@ int main(void) {
   P(sca_view)
   P(sca_attn_dims) F(sca_attn_dims, scale) F(sca_attn_dims, accumulate) F(sca_attn_dims, q)
   F(sca_attn_dims, kv) F(sca_attn_dims, o) F(sca_attn_dims, dkv) F(sca_attn_dims, lse_b) F(sca_attn_dims, lse_h)
+  F(sca_attn_dims, q_by_pos) F(sca_attn_dims, kv_by_pos) F(sca_attn_dims, dkv_by_pos)
   P(sca_fwd_item) F(sca_fwd_item, o) F(sca_fwd_item, lse) F(sca_fwd_item, q_pos) F(sca_fwd_item, kv_pos)
   P(sca_bwd_item) F(sca_bwd_item, dout) F(sca_bwd_item, delta) F(sca_bwd_item, dv) F(sca_bwd_item, q_pos)
   F(sca_bwd_item, kv_pos)
@@ -139,6 +140,10 @@ def _fwd_rc(lib, items, dims, n=None):
     ("bad_algo", capi.SCA_ERR_ARG),
     ("nan_scale", capi.SCA_ERR_ARG),
     ("too_many_heads", capi.SCA_ERR_ARG),
+    ("by_pos_flag_not_boolean", capi.SCA_ERR_ARG),
+    ("by_pos_segment_not_x128", capi.SCA_ERR_UNSUPPORTED),
+    ("by_pos_kv_segment_not_x128", capi.SCA_ERR_UNSUPPORTED),
+    ("dkv_by_pos_in_forward", capi.SCA_ERR_ARG),
 ])
 def test_fwd_rejects_bad_arguments(lib, case, expect):
     items, dims, n = [_item()], _dims(), None
@@ -167,12 +172,24 @@ def test_fwd_rejects_bad_arguments(lib, case, expect):
         dims = _dims(scale=float("nan"))
     elif case == "too_many_heads":
         dims = _dims(B=300, H=300)
+    elif case == "by_pos_flag_not_boolean":
+        dims = _dims(q_by_pos=2)
+    elif case == "by_pos_segment_not_x128":   # zigzag chunks of 96 rows: a tile would straddle two
+        dims = _dims(q_by_pos=1)
+        items = [_item(q_pos=capi.segs(2, 96, (0, 672)))]
+    elif case == "by_pos_kv_segment_not_x128":
+        dims = _dims(kv_by_pos=1)
+        items = [_item(kv_pos=capi.segs(1, 200, (0, 0)))]
+    elif case == "dkv_by_pos_in_forward":
+        dims = _dims(dkv_by_pos=1)
     rc = _fwd_rc(lib, items, dims, n)
     assert rc == expect, (case, rc, capi.last_error())
     assert capi.last_error()
 
 
 def test_bwd_rejects_bad_arguments(lib):
+    arr = (capi.sca_bwd_item * 1)(_bwd_item(kv_pos=capi.segs(2, 64, (0, 192))))
+    assert lib.attn_bwd_shard(arr, 1, ctypes.byref(_dims(dkv_by_pos=1)), None, None) == capi.SCA_ERR_UNSUPPORTED
     arr = (capi.sca_bwd_item * 1)(_bwd_item(delta=None))
     assert lib.attn_bwd_shard(arr, 1, ctypes.byref(_dims()), None, None) == capi.SCA_ERR_ARG
     arr = (capi.sca_bwd_item * 1)(_bwd_item(dk=A + 4))

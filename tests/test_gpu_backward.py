@@ -1,7 +1,8 @@
 """GPU parity of the sharded backward (delta, ring of attn_bwd_shard steps
-recomputing P from the saved lse, dK/dV summed across shards, inverse
-permute) against the fp64 oracle: small cases in full, the 32K training
-workload at full size on sampled query and key rows."""
+recomputing P from the saved lse, dK/dV summed across shards; rows by
+position or through permuted copies; the fused one-launch schedule) against
+the fp64 oracle: small cases in full, the 32K training workload at full
+size on sampled query and key rows."""
 import numpy as np
 import pytest
 import torch
@@ -22,18 +23,21 @@ def sca():
     return m
 
 
-@pytest.mark.parametrize("dtype,layout,P,G,schedule,S", [
-    ("bf16", "zigzag", 2, 1, "ring", 1024), ("bf16", "zigzag", 4, 1, "ring", 1024),
-    ("bf16", "zigzag", 4, 2, "direct", 1024), ("bf16", "contiguous", 2, 1, "ring", 768),
-    ("f32", "contiguous", 2, 1, "ring", 256), ("f32", "zigzag", 4, 1, "ring", 200 * 8 // 8)])
-def test_backward_small_full_oracle(sca, dtype, layout, P, G, schedule, S):
+@pytest.mark.parametrize("dtype,layout,P,G,schedule,S,addressing", [
+    ("bf16", "zigzag", 2, 1, "ring", 1024, "auto"), ("bf16", "zigzag", 4, 1, "ring", 1024, "auto"),
+    ("bf16", "zigzag", 4, 2, "direct", 1024, "auto"), ("bf16", "contiguous", 2, 1, "ring", 768, "auto"),
+    ("f32", "contiguous", 2, 1, "ring", 256, "auto"), ("f32", "zigzag", 4, 1, "ring", 200 * 8 // 8, "auto"),
+    ("bf16", "zigzag", 4, 1, "ring", 1024, "permuted"), ("bf16", "zigzag", 2, 2, "direct", 1024, "permuted"),
+    ("bf16", "zigzag", 4, 1, "fused", 1024, "auto"), ("bf16", "zigzag", 2, 2, "fused", 896, "auto"),
+    ("f32", "contiguous", 2, 1, "fused", 256, "auto"), ("f32", "zigzag", 4, 1, "ring", 1024, "position")])
+def test_backward_small_full_oracle(sca, dtype, layout, P, G, schedule, S, addressing):
     B, H, D = 1, 2, 128 if dtype == "bf16" else 64
     if layout == "zigzag" and S % (2 * P):
         S = 2 * P * (S // (2 * P))
     q, k, v, do = seeded_inputs.make_inputs(B, H, S, D, dtype, seed=200 + P, with_do=True)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     plan = sca.ShardedCausalAttention(B, H, S, D, P, layout=layout, dtype=tdt, head_groups=G, schedule=schedule,
-                                      backward=True)
+                                      backward=True, addressing=addressing)
     qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
     o, lse = plan.forward(qd, kd, vd)
     dq, dk, dv = plan.backward(dod, qd, kd, vd)
@@ -46,11 +50,12 @@ def test_backward_small_full_oracle(sca, dtype, layout, P, G, schedule, S):
         assert_close(name, got, ref, tol)
 
 
-def test_backward_repeat_overwrites(sca):
+@pytest.mark.parametrize("schedule", ["ring", "fused"])
+def test_backward_repeat_overwrites(sca, schedule):
     # step 0 overwrites the gradient buffers: a second call gives the same result
     B, H, S, D, P = 1, 2, 512, 128, 2
     q, k, v, do = (x.cuda() for x in seeded_inputs.make_inputs(B, H, S, D, "bf16", seed=9, with_do=True))
-    plan = sca.ShardedCausalAttention(B, H, S, D, P, backward=True)
+    plan = sca.ShardedCausalAttention(B, H, S, D, P, backward=True, schedule=schedule)
     plan.forward(q, k, v)
     a = [t.clone() for t in plan.backward(do)]
     plan.forward(q, k, v)
@@ -62,10 +67,11 @@ def test_backward_repeat_overwrites(sca):
     assert torch.allclose(a[0], b[0], rtol=0, atol=1e-5)
 
 
-def test_training_step_full_size_sampled(sca):
+@pytest.mark.parametrize("schedule", ["ring", "fused"])
+def test_training_step_full_size_sampled(sca, schedule):
     w = WORKLOADS["train_s32k"]
     q, k, v, do = seeded_inputs.workload_inputs(w)
-    plan = sca.ShardedCausalAttention(w.B, w.H, w.S, w.D, w.P, layout=w.layout, schedule=w.schedule, backward=True)
+    plan = sca.ShardedCausalAttention(w.B, w.H, w.S, w.D, w.P, layout=w.layout, schedule=schedule, backward=True)
     o, lse = plan.forward(q.cuda(), k.cuda(), v.cuda())
     dq, dk, dv = plan.backward(do.cuda())
     torch.cuda.synchronize()

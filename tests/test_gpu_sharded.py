@@ -1,7 +1,8 @@
-"""End-to-end sharded forward on the GPU (permute, ring of per-block partials
-with double-buffered staging, lse merge with fused inverse permute) against
-the fp64 oracle, on every forward workload at full size (sampled rows where
-the oracle would take too long)."""
+"""End-to-end sharded forward on the GPU (ring of per-block partials with
+double-buffered staging and the lse merge, rows addressed by position or
+through permuted copies; the fused one-launch schedule) against the fp64
+oracle, on every forward workload at full size (sampled rows where the
+oracle would take too long)."""
 import numpy as np
 import pytest
 import torch
@@ -37,21 +38,22 @@ def _run(sca, w, q, k, v, **kw):
     return plan, o, lse
 
 
-@pytest.mark.parametrize("name", ["tiny_f32", "fwd_s8k"])
-def test_forward_full_oracle(sca, name):
+@pytest.mark.parametrize("name,kw", [("tiny_f32", {}), ("fwd_s8k", {}), ("fwd_s8k", {"addressing": "permuted"}),
+                                     ("fwd_s8k", {"schedule": "fused"}), ("tiny_f32", {"schedule": "fused"})])
+def test_forward_full_oracle(sca, name, kw):
     w = WORKLOADS[name]
     q, k, v = seeded_inputs.workload_inputs(w)[:3]
-    _, o, lse = _run(sca, w, q, k, v)
+    _, o, lse = _run(sca, w, q, k, v, **kw)
     ro, rl = oracle.attention(q, k, v, scale_for(w.D))
     assert_close("o", o, ro, tol_for(w.dtype))
     assert_close("lse", lse, rl, tol_for(w.dtype))
 
 
-@pytest.mark.parametrize("name", ["ring_s128k", "2d_s32k"])
-def test_forward_sampled_rows_full_size(sca, name):
+@pytest.mark.parametrize("name,kw", [("ring_s128k", {}), ("2d_s32k", {}), ("ring_s128k", {"schedule": "fused"})])
+def test_forward_sampled_rows_full_size(sca, name, kw):
     w = WORKLOADS[name]
     q, k, v = seeded_inputs.workload_inputs(w)[:3]
-    _, o, lse = _run(sca, w, q, k, v)
+    _, o, lse = _run(sca, w, q, k, v, **kw)
     rows = seeded_inputs.sample_rows(w.B, w.H, w.S, w.sample_rows, w.seed).numpy()
     ro, rl = oracle.attention_rows(q, k, v, scale_for(w.D), rows)
     idx = torch.as_tensor(rows, device=o.device)
@@ -62,12 +64,15 @@ def test_forward_sampled_rows_full_size(sca, name):
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
 
 
-@pytest.mark.parametrize("layout,P,G", [("zigzag", 4, 1), ("zigzag", 8, 1), ("contiguous", 4, 1),
-                                        ("zigzag", 2, 4), ("contiguous", 1, 1), ("zigzag", 1, 2)])
-def test_forward_small_full_oracle(sca, layout, P, G):
+@pytest.mark.parametrize("layout,P,G,kw", [
+    ("zigzag", 4, 1, {}), ("zigzag", 8, 1, {}), ("contiguous", 4, 1, {}), ("zigzag", 2, 4, {}),
+    ("contiguous", 1, 1, {}), ("zigzag", 1, 2, {}), ("zigzag", 4, 1, {"addressing": "permuted"}),
+    ("zigzag", 2, 4, {"addressing": "permuted", "schedule": "direct"}), ("zigzag", 4, 1, {"schedule": "fused"}),
+    ("zigzag", 2, 4, {"schedule": "fused"})])
+def test_forward_small_full_oracle(sca, layout, P, G, kw):
     B, H, S, D = 2, 4, 1024, 128
     q, k, v = seeded_inputs.make_inputs(B, H, S, D, "bf16", seed=100 + P + G)
-    plan = sca.ShardedCausalAttention(B, H, S, D, P, layout=layout, head_groups=G)
+    plan = sca.ShardedCausalAttention(B, H, S, D, P, layout=layout, head_groups=G, **kw)
     o, lse = plan.forward(q.cuda(), k.cuda(), v.cuda())
     ro, rl = oracle.attention(q, k, v, scale_for(D))
     assert_close("o", o, ro, tol_for("bf16"))
@@ -78,15 +83,22 @@ def test_forward_small_full_oracle(sca, layout, P, G):
 
 
 def test_ring_staging_equals_direct_reads(sca):
+    # staged or home blocks, positions or permuted copies: the same partials
+    # and the same merge, so bit-identical results; the fused schedule sums
+    # in another order, so equal up to rounding
     w = WORKLOADS["ring_s128k"]
     S, H = 16384, 4
     q, k, v = seeded_inputs.make_inputs(w.B, H, S, w.D, "bf16", seed=w.seed)
     outs = []
-    for schedule in ("ring", "direct"):
-        plan = sca.ShardedCausalAttention(w.B, H, S, w.D, w.P, schedule=schedule)
+    for kw in ({"schedule": "ring"}, {"schedule": "direct"}, {"schedule": "ring", "addressing": "permuted"},
+               {"schedule": "direct", "addressing": "permuted"}, {"schedule": "fused"}):
+        plan = sca.ShardedCausalAttention(w.B, H, S, w.D, w.P, **kw)
         o, lse = plan.forward(q.cuda(), k.cuda(), v.cuda())
         outs.append((o.clone(), lse.clone()))
-    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    for o, lse in outs[1:4]:
+        assert torch.equal(outs[0][0], o) and torch.equal(outs[0][1], lse)
+    assert torch.allclose(outs[0][0], outs[4][0], rtol=0, atol=2e-3)
+    assert torch.allclose(outs[0][1], outs[4][1], rtol=0, atol=1e-4)
 
 
 def test_repeated_calls_are_deterministic(sca):
@@ -98,9 +110,10 @@ def test_repeated_calls_are_deterministic(sca):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_bf16_output_copy(sca):
+@pytest.mark.parametrize("schedule", ["ring", "fused"])
+def test_bf16_output_copy(sca, schedule):
     B, H, S, D, P = 1, 2, 512, 128, 2
     q, k, v = seeded_inputs.make_inputs(B, H, S, D, "bf16", seed=4)
-    plan = sca.ShardedCausalAttention(B, H, S, D, P, bf16_out=True)
+    plan = sca.ShardedCausalAttention(B, H, S, D, P, bf16_out=True, schedule=schedule)
     o, _ = plan.forward(q.cuda(), k.cuda(), v.cuda())
     assert torch.equal(plan.o_bf16, o.to(torch.bfloat16))
