@@ -28,12 +28,16 @@ What it computes, and where that comes from:
   merges per-block partials.
 * ``attention_backward`` - gradients of the same unit, with P recomputed from
   the saved lse (textbook softmax-attention backward).
+* ``attention_gqa`` / ``attention_backward_gqa`` - grouped-query attention:
+  query heads in consecutive groups share one key/value head ("Avances en la
+  capacitacion de LLMs de secuencia larga", section "Comprendiendo la
+  Arquitectura de los LLMs"); the key/value gradients sum over the group.
 
 Everything is float64 numpy; matmul is the only library primitive used.
 """
 from .attention import (attention, attention_rows, attention_backward, attention_backward_block,
-                        backward_query_rows, backward_key_columns, merge_lse,
-                        softmax_matrix)
+                        attention_backward_gqa, attention_gqa, backward_query_rows, backward_key_columns,
+                        kv_head_of, merge_lse, softmax_matrix)
 from .shards import (chunk_len, zigzag_order, contiguous_order, shard_order,
                      shard_positions, permute_rows, ring_visit_order,
                      double_ring_visit_order, sharded_attention,
@@ -41,6 +45,7 @@ from .shards import (chunk_len, zigzag_order, contiguous_order, shard_order,
 
 __all__ = [
     "attention", "attention_rows", "attention_backward", "attention_backward_block",
+    "attention_gqa", "attention_backward_gqa", "kv_head_of",
     "backward_query_rows",
     "backward_key_columns", "merge_lse", "softmax_matrix", "chunk_len",
     "zigzag_order", "contiguous_order", "shard_order", "shard_positions",

@@ -261,3 +261,66 @@ def attention_backward_block(q, k, v, do, lse, delta, scale, causal=True, q_pos=
     p = _probs(s, lse)
     ds = p * (do @ v.T - delta[:, None])
     return scale * (ds @ k), scale * (ds.T @ q), p.T @ do
+
+
+# -------------------------------------------- grouped-query attention ----
+#
+# "Avances en la capacitacion de LLMs de secuencia larga", section
+# "Comprendiendo la Arquitectura de los LLMs": grouped-query attention groups
+# the query heads so that each group shares one key/value head (the 7B-GQA
+# model of section "Evaluacion y Comparacion con Sistemas Existentes").  The
+# page does not say which query heads form a group; the reading here is
+# consecutive groups: with H query heads and Hkv key/value heads, query head
+# h reads key/value head h // (H / Hkv).
+
+def kv_head_of(h: int, n_heads: int, n_kv_heads: int) -> int:
+    """Key/value head that query head h reads."""
+    if n_heads % n_kv_heads:
+        raise ValueError(f"{n_heads} query heads are not a multiple of {n_kv_heads} key/value heads")
+    return h // (n_heads // n_kv_heads)
+
+
+def attention_gqa(q, k, v, scale, causal=True):
+    """(o, lse) of grouped-query causal attention, float64.
+
+    q: [B, H, S, D]; k, v: [B, Hkv, S, D] with H a multiple of Hkv.  Each
+    query head is the single-head attention of its rows against the
+    key/value head of its group.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, S, _ = q.shape
+    Hkv = k.shape[1]
+    o = np.zeros(q.shape[:3] + (v.shape[-1],))
+    lse = np.zeros(q.shape[:3])
+    for b in range(B):
+        for h in range(H):
+            hk = kv_head_of(h, H, Hkv)
+            o[b, h], lse[b, h] = attention(q[b, h], k[b, hk], v[b, hk], scale, causal=causal)
+    return o, lse
+
+
+def attention_backward_gqa(q, k, v, do, scale, causal=True, o=None, lse=None):
+    """(dq, dk, dv) of grouped-query causal attention, float64.
+
+    dq per query head; the dk, dv of a key/value head are the sums of the
+    single-head gradients of every query head that reads it (the head is
+    one input of all of them).
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    if o is None or lse is None:
+        o, lse = attention_gqa(q, k, v, scale, causal=causal)
+    o, lse = _f64(o), _f64(lse)
+    B, H = q.shape[:2]
+    Hkv = k.shape[1]
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            hk = kv_head_of(h, H, Hkv)
+            gq, gk, gv = attention_backward(q[b, h], k[b, hk], v[b, hk], do[b, h], scale, causal=causal,
+                                            o=o[b, h], lse=lse[b, h])
+            dq[b, h] = gq
+            dk[b, hk] += gk
+            dv[b, hk] += gv
+    return dq, dk, dv

@@ -74,6 +74,24 @@ def _backward_no_delta(q, k, v, do, scale, causal=True, o=None, lse=None):
 
 _orig_backward = oatt.attention_backward
 
+
+def _kv_head_interleaved(h, n_heads, n_kv_heads):
+    # wrong grouping: query heads dealt round-robin over the key/value heads
+    return h % n_kv_heads
+
+
+def _backward_gqa_last_head_wins(q, k, v, do, scale, causal=True, o=None, lse=None):
+    # slip: the key/value gradient of a group is overwritten, not summed
+    q, k, v, do = map(oatt._f64, (q, k, v, do))
+    B, H = q.shape[:2]
+    Hkv = k.shape[1]
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            hk = h // (H // Hkv)
+            dq[b, h], dk[b, hk], dv[b, hk] = oatt.attention_backward(q[b, h], k[b, hk], v[b, hk], do[b, h], scale)
+    return dq, dk, dv
+
 FORWARD_PINS = [pins.test_first_row_sees_only_itself, pins.test_closed_form_q_zero_causal,
                 pins.test_softmax_rows_sum_to_one, pins.test_lse_matches_torch_logsumexp,
                 lambda: pins.test_forward_matches_torch_sdpa_fp64(True),
@@ -83,6 +101,8 @@ MERGE_PINS = [pins.test_merge_two_halves_closed_form,
 ZIGZAG_PINS = [pins.test_zigzag_matches_golden_chunk_map,
                lambda: pins.test_zigzag_balances_causal_work(4, 5)]
 BACKWARD_PINS = [pins.test_backward_finite_differences, pins.test_backward_invariants]
+GQA_PINS = [lambda: pins.test_gqa_forward_matches_torch_sdpa_on_repeated_kv(4, 2),
+            lambda: pins.test_gqa_backward_matches_torch_autograd(4, 2), pins.test_gqa_backward_finite_differences]
 
 
 def _some_pin_fails(pin_list):
@@ -116,6 +136,17 @@ def test_planted_backward_mistake_is_caught(monkeypatch, bad):
     assert _some_pin_fails(BACKWARD_PINS), f"no pin caught mutation {bad.__name__}"
 
 
+def test_planted_gqa_grouping_mistake_is_caught(monkeypatch):
+    monkeypatch.setattr(oatt, "kv_head_of", _kv_head_interleaved)
+    assert _some_pin_fails(GQA_PINS[:1]), "no pin caught the interleaved grouping"
+
+
+def test_planted_gqa_backward_mistake_is_caught(monkeypatch):
+    monkeypatch.setattr(oatt, "attention_backward_gqa", _backward_gqa_last_head_wins)
+    monkeypatch.setattr(oracle, "attention_backward_gqa", _backward_gqa_last_head_wins)
+    assert _some_pin_fails(GQA_PINS[1:]), "no pin caught the unsummed key/value gradient"
+
+
 def test_unmutated_oracle_passes_every_listed_pin():
-    for lst in (FORWARD_PINS, MERGE_PINS, ZIGZAG_PINS, BACKWARD_PINS):
+    for lst in (FORWARD_PINS, MERGE_PINS, ZIGZAG_PINS, BACKWARD_PINS, GQA_PINS):
         assert not _some_pin_fails(lst)

@@ -338,3 +338,70 @@ def test_block_backward_contributions_sum_to_full(layout, P):
     np.testing.assert_allclose(dq, fq, atol=1e-12)
     np.testing.assert_allclose(dk, fk, atol=1e-12)
     np.testing.assert_allclose(dv, fv, atol=1e-12)
+
+
+# ---------------------------------------------- grouped-query attention ----
+
+def _rep(x, group):
+    """Key/value heads expanded to one per query head (torch's repeat_interleave)."""
+    return torch.repeat_interleave(x, group, dim=1)
+
+
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (4, 2), (6, 1), (8, 2)])
+def test_gqa_forward_matches_torch_sdpa_on_repeated_kv(H, Hkv):
+    B, S, D = 2, 40, 8
+    g = torch.Generator().manual_seed(H * 10 + Hkv)
+    q = torch.randn(B, H, S, D, dtype=torch.float64, generator=g)
+    k, v = (torch.randn(B, Hkv, S, D, dtype=torch.float64, generator=g) for _ in range(2))
+    o, lse = oracle.attention_gqa(q, k, v, 1 / math.sqrt(D))
+    kr, vr = _rep(k, H // Hkv), _rep(v, H // Hkv)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, kr, vr, is_causal=True)
+    np.testing.assert_allclose(o, ref.numpy(), atol=1e-12)
+    s = (q @ kr.transpose(-1, -2)) / math.sqrt(D)
+    s = s.masked_fill(torch.ones(S, S, dtype=torch.bool).triu(1), float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), atol=1e-12)
+
+
+def test_gqa_with_one_query_head_per_group_is_mha():
+    B, H, S, D = 1, 3, 30, 4
+    q, k, v = (RNG.standard_normal((B, H, S, D)) for _ in range(3))
+    o, lse = oracle.attention_gqa(q, k, v, 0.5)
+    ro, rl = oracle.attention(q, k, v, 0.5)
+    np.testing.assert_array_equal(o, ro)
+    np.testing.assert_array_equal(lse, rl)
+
+
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (6, 3), (4, 1)])
+def test_gqa_backward_matches_torch_autograd(H, Hkv):
+    # autograd through repeat_interleave sums each key/value head's gradient
+    # over the query heads that read it
+    B, S, D = 1, 50, 8
+    g = torch.Generator().manual_seed(H + Hkv)
+    q, do = (torch.randn(B, H, S, D, dtype=torch.float64, generator=g) for _ in range(2))
+    k, v = (torch.randn(B, Hkv, S, D, dtype=torch.float64, generator=g) for _ in range(2))
+    qq, kk, vv = (x.clone().requires_grad_() for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(qq, _rep(kk, H // Hkv), _rep(vv, H // Hkv), is_causal=True)
+    o.backward(do)
+    dq, dk, dv = oracle.attention_backward_gqa(q, k, v, do, 1 / math.sqrt(D))
+    np.testing.assert_allclose(dq, qq.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dk, kk.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dv, vv.grad.numpy(), atol=1e-11)
+
+
+def test_gqa_backward_finite_differences():
+    B, H, Hkv, S, D, h = 1, 4, 2, 5, 2, 1e-6
+    q, do = (RNG.standard_normal((B, H, S, D)) for _ in range(2))
+    k, v = (RNG.standard_normal((B, Hkv, S, D)) for _ in range(2))
+    dq, dk, dv = oracle.attention_backward_gqa(q, k, v, do, 0.7)
+
+    def loss(k_, v_):
+        return float((oracle.attention_gqa(q, k_, v_, 0.7)[0] * do).sum())
+
+    for which, ref in ((0, dk), (1, dv)):
+        fd = np.zeros_like(k)
+        for idx in np.ndindex(fd.shape):
+            plus, minus = [k.copy(), v.copy()], [k.copy(), v.copy()]
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            fd[idx] = (loss(*plus) - loss(*minus)) / (2 * h)
+        np.testing.assert_allclose(ref, fd, rtol=1e-6, atol=1e-8)
