@@ -188,7 +188,9 @@ def run_gpu(args):
     barrier(ws)
     w = WORKLOADS[args.workload]
     if args.heads:   # a smaller case of the same kernels, for profiler captures
-        w = dataclasses.replace(w, H=args.heads, head_groups=1 if args.heads % w.head_groups else w.head_groups,
+        kvh = None if w.kv_heads is None else max(1, args.heads * w.kv_heads // w.H)
+        w = dataclasses.replace(w, H=args.heads, kv_heads=kvh,
+                                head_groups=1 if args.heads % w.head_groups else w.head_groups,
                                 description=w.description + f" (profiling case: H={args.heads})")
     dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     inputs = seeded_inputs.workload_inputs(w)
@@ -197,7 +199,7 @@ def run_gpu(args):
         w = dataclasses.replace(w, schedule=args.schedule)
     plan = sca.ShardedCausalAttention(w.B, w.H, w.S, w.D, w.P, layout=w.layout, dtype=dtype,
                                       head_groups=w.head_groups, schedule=w.schedule, backward=w.backward,
-                                      addressing=args.addressing)
+                                      addressing=args.addressing, kv_heads=w.kv_heads)
     stream = torch.cuda.current_stream(device)
 
     # per-launch timing of the attention kernels (same stream they run on)
@@ -396,6 +398,7 @@ def run_gpu(args):
         "data": "synthetic (seeded N(0,1))",
         "config": {"workload": w.description, "name": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "P": w.P,
                    "layout": w.layout, "schedule": w.schedule, "addressing": plan.addressing,
+                   "kv_heads": w.kv_heads or w.H,
                    "head_groups": w.head_groups,
                    "step": "fwd+bwd" if w.backward else "fwd",
                    "flops_per_step": step_flops, "l2": "inputs larger than L2 (no flush)"

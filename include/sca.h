@@ -98,7 +98,13 @@ typedef struct {
   int32_t q_by_pos;    /* q, o, lse (forward); q, dout, dq, lse, delta (bwd) */
   int32_t kv_by_pos;   /* k, v                                               */
   int32_t dkv_by_pos;  /* dk, dv (backward only)                             */
-  int32_t reserved;    /* 0                                                  */
+  /* Key/value heads (grouped-query attention, "Avances en la capacitacion
+   * de LLMs de secuencia larga", section "Comprendiendo la Arquitectura de
+   * los LLMs": query heads in groups share one key/value head).  0 or H:
+   * one per query head.  Otherwise H must be a multiple of it and query
+   * head h reads key/value head h / (H / kv_heads); k, v (and dk, dv, which
+   * then sum over the group) have kv_heads heads in the kv / dkv views. */
+  int32_t kv_heads;
 } sca_attn_dims;
 
 /* One (query shard, key/value block) work item of the forward. */
@@ -214,8 +220,10 @@ typedef struct {
  * larga", section "Escalabilidad y Gestion de Memoria".)
  * Items in one call must not share dq rows nor dk/dv rows.
  * With bf16 inputs the tensor-core kernel computes S, dK and dQ as fp16
- * products (Q and K are converted to fp16 inside the kernel, dS is rounded
- * to fp16): |q| and |k| must stay below 65504.  dq is summed over key tiles
+ * products (q and k are converted to fp16 inside the kernel, dS is rounded
+ * to fp16), and with grouped-query heads dP and dV too (v and dout
+ * converted, P rounded to fp16): |q|, |k| (and |v|, |dout|) must stay below
+ * 65504.  dq is summed over key tiles
  * by fp32 reduce-adds in no fixed order, so it is reproducible only up to
  * rounding order; dk and dv have one writer per row.  The tensor-core path
  * needs dq, dk, dv rows 16-byte aligned with strides that are multiples of

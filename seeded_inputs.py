@@ -5,15 +5,19 @@ normally distributed tensors from a seeded CPU generator, rounds them to the
 storage dtype, and picks seeded row samples.  Both the fp64 oracle and the
 GPU path read their inputs from here, so the two compute on identical values.
 
-Workloads (shapes, dtypes, seeds, shard counts) are the five synthetic cases
-this library is checked and measured on; head dim 128 matches the 7B decoder
+Workloads (shapes, dtypes, seeds, shard counts) are the synthetic cases this
+library is checked and measured on; head dim 128 matches the 7B decoder
 (h=4096, 32 heads) that the TSP news page ("Zyphra presenta el paralelismo de
 secuencia y tensor (TSP)", section "Resultados de memoria y rendimiento")
-uses as its reference model.
+uses as its reference model.  The grouped-query case stands for the 7B-GQA
+model of "Avances en la capacitacion de LLMs de secuencia larga" (section
+"Evaluacion y Comparacion con Sistemas Existentes"): 32 query heads; the page
+gives no key/value head count, 8 is the reading taken.
 
 Recipe (fixed, so a reader can regenerate any case):
   g = torch.Generator('cpu').manual_seed(seed)
-  draw torch.randn([B,H,S,D], float32) in the order Q, K, V[, dO]
+  draw torch.randn in the order Q [B,H,S,D], K, V [B,Hkv,S,D] (Hkv = H
+  unless grouped-query), dO [B,H,S,D], all float32
   round to the storage dtype (bf16 round-to-nearest-even) when it is bf16
   Q *= q_mult (exact in bf16 for q_mult = 2)
 Sampled rows: torch.Generator('cpu').manual_seed(10_000 + seed), per (b, h)
@@ -43,6 +47,7 @@ class Workload:
     schedule: str = "ring"      # "ring" (staged KV blocks) or "direct"
     sample_rows: int = 0        # 0: oracle checks every row
     description: str = ""
+    kv_heads: int | None = None  # grouped-query attention: key/value heads
 
 
 WORKLOADS = {
@@ -68,6 +73,11 @@ WORKLOADS = {
         "train_s32k", B=1, H=16, S=32768, D=128, dtype="bf16", seed=4, P=4,
         layout="zigzag", backward=True, sample_rows=256,
         description="training step fwd+bwd B1 H16 S32768 D128 bf16, P=4 zigzag"),
+    "gqa_s32k": Workload(
+        "gqa_s32k", B=1, H=32, S=32768, D=128, dtype="bf16", seed=5, P=4,
+        layout="zigzag", backward=True, sample_rows=256, kv_heads=8,
+        description="grouped-query training step fwd+bwd B1 H32 (8 key/value heads) S32768 D128 bf16, "
+                    "P=4 zigzag"),
 }
 
 
@@ -80,13 +90,15 @@ def _round(x: torch.Tensor, dtype: str) -> torch.Tensor:
 
 
 def make_inputs(B: int, H: int, S: int, D: int, dtype: str, seed: int,
-                q_mult: float = 1.0, with_do: bool = False):
-    """Return (q, k, v[, do]) CPU tensors in the storage dtype, [B,H,S,D]."""
+                q_mult: float = 1.0, with_do: bool = False, kv_heads: int | None = None):
+    """Return (q, k, v[, do]) CPU tensors in the storage dtype: q, do
+    [B,H,S,D]; k, v [B,kv_heads,S,D] (kv_heads = H by default)."""
     g = torch.Generator(device="cpu").manual_seed(seed)
     names = ["q", "k", "v"] + (["do"] if with_do else [])
     out = []
     for name in names:
-        x = torch.randn([B, H, S, D], generator=g, dtype=torch.float32)
+        heads = H if (kv_heads is None or name in ("q", "do")) else kv_heads
+        x = torch.randn([B, heads, S, D], generator=g, dtype=torch.float32)
         x = _round(x, dtype)
         if name == "q" and q_mult != 1.0:
             x = x * q_mult
@@ -95,9 +107,12 @@ def make_inputs(B: int, H: int, S: int, D: int, dtype: str, seed: int,
 
 
 def workload_inputs(w: Workload, S: int | None = None, H: int | None = None):
-    """Inputs of a named workload (optionally with fewer rows/heads for quick runs)."""
-    return make_inputs(w.B, H or w.H, S or w.S, w.D, w.dtype, w.seed,
-                       q_mult=w.q_mult, with_do=w.backward)
+    """Inputs of a named workload (optionally with fewer rows/heads for quick
+    runs; a grouped-query workload keeps its query heads per key/value head)."""
+    Hq = H or w.H
+    kv = None if w.kv_heads is None else max(1, Hq * w.kv_heads // w.H)
+    return make_inputs(w.B, Hq, S or w.S, w.D, w.dtype, w.seed,
+                       q_mult=w.q_mult, with_do=w.backward, kv_heads=kv)
 
 
 def sample_rows(B: int, H: int, S: int, n: int, seed: int) -> torch.Tensor:

@@ -52,7 +52,7 @@ class sca_attn_dims(ctypes.Structure):
     _fields_ = [("B", c_int32), ("H", c_int32), ("D", c_int32), ("dtype", c_int32), ("causal", c_int32),
                 ("algo", c_int32), ("scale", c_float), ("accumulate", c_int32), ("q", sca_view), ("kv", sca_view),
                 ("o", sca_view), ("dkv", sca_view), ("lse_b", c_int64), ("lse_h", c_int64),
-                ("q_by_pos", c_int32), ("kv_by_pos", c_int32), ("dkv_by_pos", c_int32), ("reserved", c_int32)]
+                ("q_by_pos", c_int32), ("kv_by_pos", c_int32), ("dkv_by_pos", c_int32), ("kv_heads", c_int32)]
 
 
 class sca_fwd_item(ctypes.Structure):

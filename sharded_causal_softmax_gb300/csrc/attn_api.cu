@@ -46,6 +46,8 @@ static int check_dims(const sca_attn_dims* d, bool bwd) {
                   (d->dkv_by_pos == 0 || d->dkv_by_pos == 1),
               SCA_ERR_ARG, "q_by_pos, kv_by_pos, dkv_by_pos must be 0 or 1");
   SCA_REQUIRE(bwd || d->dkv_by_pos == 0, SCA_ERR_ARG, "dkv_by_pos applies to the backward only");
+  SCA_REQUIRE(d->kv_heads >= 0 && (d->kv_heads == 0 || d->H % d->kv_heads == 0), SCA_ERR_ARG,
+              "kv_heads=%d must be 0 or divide H=%d", d->kv_heads, d->H);
   return SCA_OK;
 }
 
@@ -80,6 +82,8 @@ static void fill_common(AttnArgs& a, const sca_attn_dims* d, int n_items, int* d
   a.q_by_pos = d->q_by_pos;
   a.kv_by_pos = d->kv_by_pos;
   a.dkv_by_pos = d->dkv_by_pos;
+  a.Hkv = d->kv_heads > 0 ? d->kv_heads : d->H;
+  a.group = d->H / a.Hkv;
 }
 
 static bool use_tc(const sca_attn_dims* d) {

@@ -84,8 +84,9 @@ __global__ void __launch_bounds__(kSimtThreads) fwd_simt_kernel(const __grid_con
     acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   float m = -INFINITY, l = 0.f;
-  const T* kb = static_cast<const T*>(it.k) + b * a.kv.b + h * a.kv.h;
-  const T* vb = static_cast<const T*>(it.v) + b * a.kv.b + h * a.kv.h;
+  const int hk = h / a.group;   // key/value head of this query head
+  const T* kb = static_cast<const T*>(it.k) + b * a.kv.b + hk * a.kv.h;
+  const T* vb = static_cast<const T*>(it.v) + b * a.kv.b + hk * a.kv.h;
   const int nkt = static_cast<int>((it.Skv + kSimtKeys - 1) / kSimtKeys);
   for (int kt = 0; kt < nkt; ++kt) {
     const int64_t k0 = static_cast<int64_t>(kt) * kSimtKeys;
@@ -179,8 +180,9 @@ __global__ void __launch_bounds__(kSimtThreads) dq_simt_kernel(const __grid_cons
   const float lse2 = lse * kLog2e;
   const float dlt = it.delta[b * a.lse_b + h * a.lse_h + qr];
   const bool row_live = valid && lse != -INFINITY;
-  const T* kb = static_cast<const T*>(it.k) + b * a.kv.b + h * a.kv.h;
-  const T* vb = static_cast<const T*>(it.v) + b * a.kv.b + h * a.kv.h;
+  const int hk = h / a.group;   // key/value head of this query head
+  const T* kb = static_cast<const T*>(it.k) + b * a.kv.b + hk * a.kv.h;
+  const T* vb = static_cast<const T*>(it.v) + b * a.kv.b + hk * a.kv.h;
   const int nkt = static_cast<int>((it.Skv + kSimtKeys - 1) / kSimtKeys);
   for (int kt = 0; kt < nkt; ++kt) {
     const int64_t k0 = static_cast<int64_t>(kt) * kSimtKeys;
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(kSimtThreads) dkv_simt_kernel(const __grid_con
   const Item& it = a.items[blockIdx.z];
   const int64_t k0 = static_cast<int64_t>(blockIdx.x) * kSimtRows;
   if (k0 >= it.Skv) return;
-  const int b = blockIdx.y / a.H, h = blockIdx.y % a.H;
+  const int b = blockIdx.y / a.Hkv, hk = blockIdx.y % a.Hkv;   // a key/value head
   const int ql = threadIdx.x & 3, rr = threadIdx.x >> 2;
   const int64_t krow = k0 + rr;
   const bool valid = krow < it.Skv;
@@ -245,8 +247,8 @@ __global__ void __launch_bounds__(kSimtThreads) dkv_simt_kernel(const __grid_con
   tile_pos_range(it.ks, k0, nk, kmin, kmax);
 
   float4 kv4[NF], vv4[NF], dk[NF], dv[NF];
-  const T* kp = static_cast<const T*>(it.k) + b * a.kv.b + h * a.kv.h + kr * a.kv.s;
-  const T* vp = static_cast<const T*>(it.v) + b * a.kv.b + h * a.kv.h + kr * a.kv.s;
+  const T* kp = static_cast<const T*>(it.k) + b * a.kv.b + hk * a.kv.h + kr * a.kv.s;
+  const T* vp = static_cast<const T*>(it.v) + b * a.kv.b + hk * a.kv.h + kr * a.kv.s;
 #pragma unroll
   for (int t = 0; t < NF; ++t) {
     kv4[t] = load4<T>(kp + 4 * (ql + 4 * t));
@@ -254,53 +256,56 @@ __global__ void __launch_bounds__(kSimtThreads) dkv_simt_kernel(const __grid_con
     dk[t] = make_float4(0.f, 0.f, 0.f, 0.f);
     dv[t] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  const T* qb = static_cast<const T*>(it.q) + b * a.q.b + h * a.q.h;
-  const T* db = static_cast<const T*>(it.dout) + b * a.q.b + h * a.q.h;
-  const float* lb = it.lse + b * a.lse_b + h * a.lse_h;
-  const float* dlb = it.delta + b * a.lse_b + h * a.lse_h;
   const int nqt = static_cast<int>((it.Sq + kSimtKeys - 1) / kSimtKeys);
-  for (int qt = 0; qt < nqt; ++qt) {
-    const int64_t r0 = static_cast<int64_t>(qt) * kSimtKeys;
-    const int nq = static_cast<int>(min64(kSimtKeys, it.Sq - r0));
-    int64_t qmin, qmax;
-    tile_pos_range(it.qs, r0, nq, qmin, qmax);
-    if (a.causal && kmin > qmax) continue;
-    __syncthreads();
-    const int64_t qr0 = slab_row(it.qs, a.q_by_pos, r0);   // a tile never straddles segments
-    load_rows<D, T>(Qs, qb + qr0 * a.q.s, a.q.s, nq);
-    load_rows<D, T>(Ds, db + qr0 * a.q.s, a.q.s, nq);
-    if (threadIdx.x < kSimtKeys) {
-      const int i = threadIdx.x;
-      const bool ok = i < nq;
-      Ls[i] = ok ? lb[qr0 + i] : -INFINITY;
-      Dl[i] = ok ? dlb[qr0 + i] : 0.f;
-      Ps[i] = ok ? seg_pos(it.qs, r0 + i) : INT64_MIN;
-    }
-    __syncthreads();
-#pragma unroll 2
-    for (int i = 0; i < kSimtKeys; ++i) {
-      float s = 0.f, dpv = 0.f;
-#pragma unroll
-      for (int t = 0; t < NF; ++t) {
-        s += dot4(Qs[i][ql + 4 * t], kv4[t]);
-        dpv += dot4(Ds[i][ql + 4 * t], vv4[t]);
+  // every query head that reads this key/value head contributes
+  for (int h = hk * a.group; h < (hk + 1) * a.group; ++h) {
+    const T* qb = static_cast<const T*>(it.q) + b * a.q.b + h * a.q.h;
+    const T* db = static_cast<const T*>(it.dout) + b * a.q.b + h * a.q.h;
+    const float* lb = it.lse + b * a.lse_b + h * a.lse_h;
+    const float* dlb = it.delta + b * a.lse_b + h * a.lse_h;
+    for (int qt = 0; qt < nqt; ++qt) {
+      const int64_t r0 = static_cast<int64_t>(qt) * kSimtKeys;
+      const int nq = static_cast<int>(min64(kSimtKeys, it.Sq - r0));
+      int64_t qmin, qmax;
+      tile_pos_range(it.qs, r0, nq, qmin, qmax);
+      if (a.causal && kmin > qmax) continue;
+      __syncthreads();
+      const int64_t qr0 = slab_row(it.qs, a.q_by_pos, r0);   // a tile never straddles segments
+      load_rows<D, T>(Qs, qb + qr0 * a.q.s, a.q.s, nq);
+      load_rows<D, T>(Ds, db + qr0 * a.q.s, a.q.s, nq);
+      if (threadIdx.x < kSimtKeys) {
+        const int i = threadIdx.x;
+        const bool ok = i < nq;
+        Ls[i] = ok ? lb[qr0 + i] : -INFINITY;
+        Dl[i] = ok ? dlb[qr0 + i] : 0.f;
+        Ps[i] = ok ? seg_pos(it.qs, r0 + i) : INT64_MIN;
       }
-      s = quad_sum(s);
-      dpv = quad_sum(dpv);
-      const float lse = Ls[i];
-      const bool vis = valid && lse != -INFINITY && (!a.causal || kpos <= Ps[i]);
-      const float p = vis ? exp2f(s * a.scale_log2 - lse * kLog2e) : 0.f;
-      const float ds = p * (dpv - Dl[i]);
+      __syncthreads();
+#pragma unroll 2
+      for (int i = 0; i < kSimtKeys; ++i) {
+        float s = 0.f, dpv = 0.f;
 #pragma unroll
-      for (int t = 0; t < NF; ++t) {
-        axpy4(dv[t], p, Ds[i][ql + 4 * t]);
-        axpy4(dk[t], ds, Qs[i][ql + 4 * t]);
+        for (int t = 0; t < NF; ++t) {
+          s += dot4(Qs[i][ql + 4 * t], kv4[t]);
+          dpv += dot4(Ds[i][ql + 4 * t], vv4[t]);
+        }
+        s = quad_sum(s);
+        dpv = quad_sum(dpv);
+        const float lse = Ls[i];
+        const bool vis = valid && lse != -INFINITY && (!a.causal || kpos <= Ps[i]);
+        const float p = vis ? exp2f(s * a.scale_log2 - lse * kLog2e) : 0.f;
+        const float ds = p * (dpv - Dl[i]);
+#pragma unroll
+        for (int t = 0; t < NF; ++t) {
+          axpy4(dv[t], p, Ds[i][ql + 4 * t]);
+          axpy4(dk[t], ds, Qs[i][ql + 4 * t]);
+        }
       }
     }
   }
   if (!valid) return;
-  float* dkp = it.dk + b * a.dkv.b + h * a.dkv.h + dkr * a.dkv.s;
-  float* dvp = it.dv + b * a.dkv.b + h * a.dkv.h + dkr * a.dkv.s;
+  float* dkp = it.dk + b * a.dkv.b + hk * a.dkv.h + dkr * a.dkv.s;
+  float* dvp = it.dv + b * a.dkv.b + hk * a.dkv.h + dkr * a.dkv.s;
 #pragma unroll
   for (int t = 0; t < NF; ++t) {
     float4* pk = reinterpret_cast<float4*>(dkp + 4 * (ql + 4 * t));
@@ -342,7 +347,7 @@ static cudaError_t launch_bwd(AttnArgs& a, cudaStream_t st) {
   dq_simt_kernel<D, T><<<gq, kSimtThreads, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 gk(a.max_k_tiles, a.B * a.H, a.n_items);
+  dim3 gk(a.max_k_tiles, a.B * a.Hkv, a.n_items);
   dkv_simt_kernel<D, T><<<gk, kSimtThreads, 0, st>>>(a);
   return cudaGetLastError();
 }

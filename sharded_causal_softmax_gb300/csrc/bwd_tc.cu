@@ -1,9 +1,11 @@
 // Backward of one (query shard, key block) item on the 5th-generation
 // tensor cores (sm_103a), recomputing P from the saved lse.
 //
-// One CTA owns a tile of 128 keys of one (item, batch, head), keeps dK and
-// dV for it in tensor memory, and walks the query tiles (128 rows) that can
-// see it.  Per query tile i:
+// One CTA owns a tile of 128 keys of one (item, batch, key/value head),
+// keeps dK and dV for it in tensor memory, and walks the query tiles (128
+// rows) that can see it, of every query head that reads this key/value head
+// (one head, or a group under grouped-query attention), so dK and dV sum
+// over the group in tensor memory.  Per query tile i:
 //
 //   S^T = K Q_i^T          dP^T = V dO_i^T        (A = K/V, B = Q/dO; smem)
 //   P^T = exp(scale S^T - lse_i)                   (warps 0-7, phase 1)
@@ -31,11 +33,14 @@
 // until dQ_i has been read back, its S^T only for dV to have read P^T.
 //
 // Precision: S^T, dK and dQ run as fp16 MMAs.  The elementwise warps convert
-// the K tile (once) and each Q tile in shared memory from bf16 to fp16 (exact
-// for |x| in [2^-14, 65504], so inputs must stay inside the fp16 range), and
-// dS is rounded to fp16 (2^-11 relative) instead of bf16 (2^-8): with few
-// visible keys a query's dQ is a short sum of large dS terms and bf16 dS
-// alone would cost more than 1e-2.  dP^T and dV stay bf16 (V, dO, P^T).
+// the K tile (once) and each Q tile in shared memory from bf16 to fp16
+// (exact for |x| in [2^-14, 65504], so inputs must stay inside the fp16
+// range), and round dS to fp16 (2^-11 relative) instead of bf16 (2^-8):
+// with few visible keys a query's dQ is a short sum of large dS terms and
+// bf16 dS alone would cost more than 1e-2.  dP^T and dV take bf16 V, dO, P^T,
+// except under grouped-query attention (F16PV), where dV sums P^T dO over
+// every query head of the group and bf16 P missed 1e-2: there V (once) and
+// each dO tile are converted too and P^T is rounded to fp16.
 //
 // Every wait is bounded (ptx.cuh); on expiry the CTA records
 // SCA_ERR_TIMEOUT, drains in-flight copies/MMAs (bounded), frees tensor
@@ -88,7 +93,8 @@ struct Bars {
   uint64_t p_half[2];        // P^T of query chunk c (32 per warpgroup) written by warps 0-7
   uint64_t ds_half[2];       // dS^T of query chunk c written (after chunk 1: dS in smem too)
   uint64_t dq_full, tmem_free;
-  uint64_t k_conv, q_conv;   // K / the current Q tile converted to fp16
+  uint64_t k_conv, q_conv;   // K and V / the current Q tile converted to fp16
+  uint64_t do_conv;          // the current dO tile converted to fp16
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -124,7 +130,10 @@ SCA_INLINE QTile q_tile(const ItemGeom& g, int t, bool causal, int nk, int64_t k
 
 SCA_INLINE void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-template <int D>
+// F16PV: P^T, V and dO in fp16 too, so dP^T and dV are fp16 MMAs (chosen for
+// grouped-query attention, where dV sums over the group); otherwise those
+// two products take the bf16 inputs as they are.
+template <int D, bool F16PV>
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ TcArgs ta) {
   using L = Layout<D>;
   const AttnArgs& a = ta.a;
@@ -143,7 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   const ItemGeom gm = item_geom(it);
   const int64_t k0 = static_cast<int64_t>(blockIdx.x) * BN;   // early keys (most queries) first
   if (k0 >= gm.Skv) return;
-  const int b = blockIdx.y / a.H, h = blockIdx.y % a.H;
+  // one key/value head; its query heads [h0, h0 + group) all read it
+  const int b = blockIdx.y / a.Hkv, hk = blockIdx.y % a.Hkv;
+  const int h0 = hk * a.group;
   const int nk = static_cast<int>(min64(BN, gm.Skv - k0));
   int64_t kmin, kmax;
   tile_pos_range(gm.ks, k0, nk, kmin, kmax);
@@ -151,9 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   const int nqt = static_cast<int>((gm.Sq + BM - 1) / BM);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto qvis = [&](int t) { return q_tile(gm, t, causal, nk, kmin, kmax).visible; };
-  const int n_vis = count_tiles(nqt, lane, qvis);
-  float* dk_base = it.dk + b * a.dkv.b + h * a.dkv.h;
-  float* dv_base = it.dv + b * a.dkv.b + h * a.dkv.h;
+  // the same query tiles are visible for every query head of the group
+  const int n_vis = count_tiles(nqt, lane, qvis) * a.group;
+  float* dk_base = it.dk + b * a.dkv.b + hk * a.dkv.h;
+  float* dv_base = it.dv + b * a.dkv.b + hk * a.dkv.h;
 
   if (n_vis == 0) {
     // no query sees these keys: overwrite mode still owes zeros
@@ -189,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     mbar_init(&bars->tmem_free, 256);
     mbar_init(&bars->k_conv, 256);
     mbar_init(&bars->q_conv, 256);
+    mbar_init(&bars->do_conv, 256);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -219,13 +232,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       mbar_arrive_expect_tx(&bars->kv_full, 2 * L::TILE);
       for (int p = 0; p < D / 64; ++p) {
         const int krow0 = static_cast<int>(slab_row(gm.ks, a.kv_by_pos, k0));
-        tma_load_4d(smem + L::K_OFF + p * PANEL, mk, &bars->kv_full, 64 * p, krow0, h, b);
-        tma_load_4d(smem + L::V_OFF + p * PANEL, mv, &bars->kv_full, 64 * p, krow0, h, b);
+        tma_load_4d(smem + L::K_OFF + p * PANEL, mk, &bars->kv_full, 64 * p, krow0, hk, b);
+        tma_load_4d(smem + L::V_OFF + p * PANEL, mv, &bars->kv_full, 64 * p, krow0, hk, b);
       }
     }
-    const float* lse_base = it.lse + b * a.lse_b + h * a.lse_h;
-    const float* dl_base = it.delta + b * a.lse_b + h * a.lse_h;
     int q0_st0 = 0, q0_st1 = 0;   // first query row of the tile each stage holds
+    int h_st0 = 0, h_st1 = 0;     // and its query head
     // dq[rows of the j-th visible tile] += its staged dQ, D/32 boxes of 32
     // fp32 columns: the first D/64 (warpgroup 0's half) from the dS panels,
     // the rest from the tile's dO stage.  Two bulk groups; once the first is
@@ -234,13 +246,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       const int sj = j & 1;
       const bool w = __all_sync(0xffffffffu, mbar_wait(&bars->dq_staged[sj], (j >> 1) & 1, abort, status));
       if (w && lane == 0) {
-        const int row0 = sj ? q0_st1 : q0_st0;
+        const int row0 = sj ? q0_st1 : q0_st0, hq = sj ? h_st1 : h_st0;
 #pragma unroll
-        for (int bx = 0; bx < D / 64; ++bx) tma_reduce_add_4d(mdq, smem + L::DS_OFF + bx * PANEL, 32 * bx, row0, h, b);
+        for (int bx = 0; bx < D / 64; ++bx)
+          tma_reduce_add_4d(mdq, smem + L::DS_OFF + bx * PANEL, 32 * bx, row0, hq, b);
         bulk_commit();
 #pragma unroll
         for (int bx = 0; bx < D / 64; ++bx)
-          tma_reduce_add_4d(mdq, smem + L::DO_OFF + sj * L::TILE + bx * PANEL, D / 2 + 32 * bx, row0, h, b);
+          tma_reduce_add_4d(mdq, smem + L::DO_OFF + sj * L::TILE + bx * PANEL, D / 2 + 32 * bx, row0, hq, b);
         bulk_commit();
         bulk_wait_read<1>();
         mbar_arrive(&bars->ds_free);
@@ -249,56 +262,66 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     };
     int n = 0;
     bool ok = true;
-    TileCursor cur;
-    for (int t; (t = cur.next(nqt, lane, qvis)) >= 0;) {
-      const QTile qt = q_tile(gm, t, causal, nk, kmin, kmax);
-      const int st = n & 1;
-      // tensor row of the tile's first query (a tile never straddles two
-      // segments when rows are addressed by position)
-      const int qrow0 = static_cast<int>(slab_row(gm.qs, a.q_by_pos, qt.q0));
-      // lse/delta of this tile into registers while the stage drains
-      float lse_r[BM / 32], dl_r[BM / 32];
+    for (int h = h0; ok && h < h0 + a.group; ++h) {
+      const float* lse_base = it.lse + b * a.lse_b + h * a.lse_h;
+      const float* dl_base = it.delta + b * a.lse_b + h * a.lse_h;
+      TileCursor cur;
+      for (int t; (t = cur.next(nqt, lane, qvis)) >= 0;) {
+        const QTile qt = q_tile(gm, t, causal, nk, kmin, kmax);
+        const int st = n & 1;
+        // tensor row of the tile's first query (a tile never straddles two
+        // segments when rows are addressed by position)
+        const int qrow0 = static_cast<int>(slab_row(gm.qs, a.q_by_pos, qt.q0));
+        // lse/delta of this tile into registers while the stage drains
+        float lse_r[BM / 32], dl_r[BM / 32];
 #pragma unroll
-      for (int k = 0; k < BM / 32; ++k) {
-        const int i = lane + 32 * k;
-        lse_r[k] = i < qt.nq ? lse_base[qrow0 + i] : -INFINITY;
-        dl_r[k] = i < qt.nq ? dl_base[qrow0 + i] : 0.f;
-      }
-      // Q stage st (and its lse/delta slot) is free once the MMAs of tile
-      // n-2 have completed
-      if (n >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bars->q_empty[st], ((n - 2) >> 1) & 1, abort, status))) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->q_full[st], L::TILE);
-        for (int p = 0; p < D / 64; ++p)
-          tma_load_4d(smem + L::Q_OFF + st * L::TILE + p * PANEL, mq, &bars->q_full[st], 64 * p, qrow0, h, b);
-      }
-      float* l2s = lse_sm + st * 2 * BM;
+        for (int k = 0; k < BM / 32; ++k) {
+          const int i = lane + 32 * k;
+          lse_r[k] = i < qt.nq ? lse_base[qrow0 + i] : -INFINITY;
+          dl_r[k] = i < qt.nq ? dl_base[qrow0 + i] : 0.f;
+        }
+        // Q stage st (and its lse/delta slot) is free once the MMAs of tile
+        // n-2 have completed
+        if (n >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bars->q_empty[st], ((n - 2) >> 1) & 1, abort, status))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->q_full[st], L::TILE);
+          for (int p = 0; p < D / 64; ++p)
+            tma_load_4d(smem + L::Q_OFF + st * L::TILE + p * PANEL, mq, &bars->q_full[st], 64 * p, qrow0, h, b);
+        }
+        float* l2s = lse_sm + st * 2 * BM;
 #pragma unroll
-      for (int k = 0; k < BM / 32; ++k) {
-        // -lse*log2(e), or -inf where P must be 0 (row past the slab, or a
-        // row that sees no key at all), so exp2(s*scale*log2e + it) is P
-        const int i = lane + 32 * k;
-        l2s[i] = lse_r[k] == -INFINITY ? -INFINITY : -lse_r[k] * kLog2e;
-        l2s[BM + i] = dl_r[k];
+        for (int k = 0; k < BM / 32; ++k) {
+          // -lse*log2(e), or -inf where P must be 0 (row past the slab, or a
+          // row that sees no key at all), so exp2(s*scale*log2e + it) is P
+          const int i = lane + 32 * k;
+          l2s[i] = lse_r[k] == -INFINITY ? -INFINITY : -lse_r[k] * kLog2e;
+          l2s[BM + i] = dl_r[k];
+        }
+        mbar_arrive(&bars->q_full[st]);
+        // dO stage st still holds half of tile n-2's dQ until its reduce has
+        // read it
+        if (n >= 2) {
+          if (!reduce_tile(n - 2)) { ok = false; break; }
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+        }
+        if (st) {
+          q0_st1 = qrow0;
+          h_st1 = h;
+        } else {
+          q0_st0 = qrow0;
+          h_st0 = h;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->do_full[st], L::TILE);
+          for (int p = 0; p < D / 64; ++p)
+            tma_load_4d(smem + L::DO_OFF + st * L::TILE + p * PANEL, mo, &bars->do_full[st], 64 * p, qrow0, h, b);
+        }
+        ++n;
       }
-      mbar_arrive(&bars->q_full[st]);
-      // dO stage st still holds half of tile n-2's dQ until its reduce has
-      // read it
-      if (n >= 2) {
-        if (!reduce_tile(n - 2)) { ok = false; break; }
-        if (lane == 0) bulk_wait_read<0>();
-        __syncwarp();
-      }
-      if (st) q0_st1 = qrow0; else q0_st0 = qrow0;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->do_full[st], L::TILE);
-        for (int p = 0; p < D / 64; ++p)
-          tma_load_4d(smem + L::DO_OFF + st * L::TILE + p * PANEL, mo, &bars->do_full[st], 64 * p, qrow0, h, b);
-      }
-      ++n;
     }
     // the last two tiles' reduces
     for (int j = (n > 2 ? n - 2 : 0); ok && j < n; ++j) ok = reduce_tile(j);
@@ -316,9 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     // ------------------------------------------------------ MMA issuer
     // one thread; it needs only the count of visible tiles, not their rows
     if (lane == 0) {
-      constexpr uint32_t idesc_dp = idesc_bf16_f32(BN, BM, false, false);    // dP^T: M=keys, N=queries
+      constexpr uint32_t idesc_dp = F16PV ? idesc_f16_f32(BN, BM, false, false)    // dP^T: M=keys, N=queries
+                                          : idesc_bf16_f32(BN, BM, false, false);
       constexpr uint32_t idesc_s = idesc_f16_f32(BN, BM, false, false);      // S^T (fp16 K, Q)
-      constexpr uint32_t idesc_dv = idesc_bf16_f32(BN, D, false, true);      // dV: M=keys, N=D
+      constexpr uint32_t idesc_dv = F16PV ? idesc_f16_f32(BN, D, false, true)      // dV: M=keys, N=D
+                                          : idesc_bf16_f32(BN, D, false, true);
       constexpr uint32_t idesc_dk = idesc_f16_f32(BN, D, false, true);       // dK (fp16 dS^T, Q)
       constexpr uint32_t idesc_dq = idesc_f16_f32(BM, D, true, true);        // dQ: M=queries, N=D
       const uint32_t sK = smem_u32(smem + L::K_OFF), sV = smem_u32(smem + L::V_OFF);
@@ -344,7 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         // dP^T = V dO^T over the dP^T columns, which hold the previous dQ
         // until it is read back
         if (n > 0 && !mbar_wait(&bars->tmem_free, (n - 1) & 1, abort, status)) { ok = false; break; }
-        if (!mbar_wait(&bars->do_full[st], (n >> 1) & 1, abort, status)) { ok = false; break; }
+        if (F16PV ? !mbar_wait(&bars->do_conv, n & 1, abort, status)      // V, dO converted to fp16
+                  : !mbar_wait(&bars->do_full[st], (n >> 1) & 1, abort, status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -409,8 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     uint8_t* sds = smem + L::DS_OFF + wg * PANEL + (row >> 3) * 1024 + (row & 7) * 128;
     int n = 0;
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_full, 0, abort, status));
-    if (ok) {
-      smem_bf16_to_f16<L::TILE, 256>(smem + L::K_OFF, threadIdx.x);
+    if (ok) {   // K (and V) to fp16; the two tiles are contiguous
+      smem_bf16_to_f16<(F16PV ? 2 : 1) * L::TILE, 256>(smem + L::K_OFF, threadIdx.x);
       fence_async_smem();
     }
     mbar_arrive(&bars->k_conv);
@@ -424,143 +453,161 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       mbar_arrive(&bars->q_conv);
       return w;
     };
-    if (ok) ok = convert_q(0);
-    TileCursor cur;
-    for (int t; ok && (t = cur.next(nqt, lane, qvis)) >= 0;) {
-      const QTile qt = q_tile(gm, t, causal, nk, kmin, kmax);
-      // -lse*log2e and delta of this warpgroup's 64 query columns (staged by warp 8)
-      const float* nl2 = lse_sm + (n & 1) * 2 * BM + 64 * wg;
-      const float* dls = nl2 + BM;
-      // phase 1: P^T = exp2(s * scale * log2(e) - lse * log2(e)), kept in fp32
-      // for phase 2 and written to tensor memory as bf16 for the dV MMAs
-      bool w = mbar_wait(&bars->s_full, n & 1, abort, status);
-      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t pr[64];   // S^T, then P^T (fp32 bits)
-      tmem_ld32(tS + lane_off + 64 * wg, pr);
-      tmem_ld32(tS + lane_off + 64 * wg + 32, pr + 32);
-      // tiles that may hold masked pairs or ragged rows: bit j set when query
-      // column 64*wg + j is visible to this thread's key (rows past the slab
-      // already have lse = -inf, so P = 0 there)
-      uint64_t vis = ~0ull;
-      if (!qt.full) {
-        vis = 0;
-#pragma unroll 1
-        for (int j = 0; j < 64; ++j) {
-          const int qc = 64 * wg + j;
-          const bool v = krow_valid && qc < qt.nq && (!causal || kpos <= seg_pos(gm.qs, qt.q0 + qc));
-          vis |= static_cast<uint64_t>(v) << j;
-        }
+    // dO of the j-th visible tile to fp16 (F16PV only)
+    auto convert_do = [&](int j) -> bool {
+      const bool w = __all_sync(0xffffffffu, mbar_wait(&bars->do_full[j & 1], (j >> 1) & 1, abort, status));
+      if (w) {
+        smem_bf16_to_f16<L::TILE, 256>(smem + L::DO_OFF + (j & 1) * L::TILE, threadIdx.x);
+        fence_async_smem();
       }
-      tmem_wait_ld32(pr);
-      tmem_wait_ld32(pr + 32);
-      auto exps = [&](auto masked) {
+      mbar_arrive(&bars->do_conv);
+      return w;
+    };
+    if (ok) ok = convert_q(0);
+    if constexpr (F16PV) {
+      if (ok) ok = convert_do(0);
+    }
+    for (int hq = 0; ok && hq < a.group; ++hq) {   // each query head of the group in turn
+      TileCursor cur;
+      for (int t; ok && (t = cur.next(nqt, lane, qvis)) >= 0;) {
+        const QTile qt = q_tile(gm, t, causal, nk, kmin, kmax);
+        // -lse*log2e and delta of this warpgroup's 64 query columns (staged by warp 8)
+        const float* nl2 = lse_sm + (n & 1) * 2 * BM + 64 * wg;
+        const float* dls = nl2 + BM;
+        // phase 1: P^T = exp2(s * scale * log2(e) - lse * log2(e)), kept in fp32
+        // for phase 2 and written to tensor memory as bf16 for the dV MMAs
+        bool w = mbar_wait(&bars->s_full, n & 1, abort, status);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t pr[64];   // S^T, then P^T (fp32 bits)
+        tmem_ld32(tS + lane_off + 64 * wg, pr);
+        tmem_ld32(tS + lane_off + 64 * wg + 32, pr + 32);
+        // tiles that may hold masked pairs or ragged rows: bit j set when query
+        // column 64*wg + j is visible to this thread's key (rows past the slab
+        // already have lse = -inf, so P = 0 there)
+        uint64_t vis = ~0ull;
+        if (!qt.full) {
+          vis = 0;
+#pragma unroll 1
+          for (int j = 0; j < 64; ++j) {
+            const int qc = 64 * wg + j;
+            const bool v = krow_valid && qc < qt.nq && (!causal || kpos <= seg_pos(gm.qs, qt.q0 + qc));
+            vis |= static_cast<uint64_t>(v) << j;
+          }
+        }
+        tmem_wait_ld32(pr);
+        tmem_wait_ld32(pr + 32);
+        auto exps = [&](auto masked) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(nl2 + 32 * c + i);   // broadcast reads
+              const float2 lp[2] = {make_float2(l4.x, l4.y), make_float2(l4.z, l4.w)};
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const int j = 32 * c + i + 2 * u;
+                const float2 x = ffma2(make_float2(__uint_as_float(pr[j]), __uint_as_float(pr[j + 1])),
+                                       make_float2(sl2, sl2), lp[u]);
+                float p0 = ex2(x.x), p1 = ex2(x.y);
+                if (decltype(masked)::value) {
+                  p0 = (vis >> j) & 1 ? p0 : 0.f;
+                  p1 = (vis >> (j + 1)) & 1 ? p1 : 0.f;
+                }
+                pr[j] = __float_as_uint(p0);
+                pr[j + 1] = __float_as_uint(p1);
+                pk[(i + 2 * u) >> 1] = F16PV ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+              }
+            }
+            // over S^T columns this thread has already read
+            tmem_st16(tS + lane_off + 64 * wg + 16 * c, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bars->p_half[c]);
+          }
+        };
+        if (qt.full)
+          exps(std::false_type{});
+        else
+          exps(std::true_type{});
+        // phase 2: dS^T = P^T (dP^T - delta), fp16, to tensor memory (A of the
+        // dK MMAs) and to this warpgroup's dS panel (A of the dQ MMAs)
+        // the dS panels hold half of the previous tile's dQ until its reduce
+        // has read them
+        w = mbar_wait(&bars->dp_full, n & 1, abort, status);
+        if (w && n > 0) w = mbar_wait(&bars->ds_free, (n - 1) & 1, abort, status);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t pk[16];
+          uint32_t dr[32];
+          tmem_ld32(tdP + lane_off + 64 * wg + 32 * c, dr);
+          tmem_wait_ld32(dr);
+          uint32_t dk[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(nl2 + 32 * c + i);   // broadcast reads
-            const float2 lp[2] = {make_float2(l4.x, l4.y), make_float2(l4.z, l4.w)};
+            const float4 d4 = *reinterpret_cast<const float4*>(dls + 32 * c + i);
+            const float2 dp[2] = {make_float2(d4.x, d4.y), make_float2(d4.z, d4.w)};
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const int j = 32 * c + i + 2 * u;
-              const float2 x = ffma2(make_float2(__uint_as_float(pr[j]), __uint_as_float(pr[j + 1])),
-                                     make_float2(sl2, sl2), lp[u]);
-              float p0 = ex2(x.x), p1 = ex2(x.y);
-              if (decltype(masked)::value) {
-                p0 = (vis >> j) & 1 ? p0 : 0.f;
-                p1 = (vis >> (j + 1)) & 1 ? p1 : 0.f;
-              }
-              pr[j] = __float_as_uint(p0);
-              pr[j + 1] = __float_as_uint(p1);
-              pk[(i + 2 * u) >> 1] = pack_bf16x2(p0, p1);
+              const int j = i + 2 * u;
+              const float2 pp = make_float2(__uint_as_float(pr[32 * c + j]), __uint_as_float(pr[32 * c + j + 1]));
+              const float2 d = fmul2(pp, fsub2(make_float2(__uint_as_float(dr[j]), __uint_as_float(dr[j + 1])), dp[u]));
+              dk[j >> 1] = pack_f16x2(d.x, d.y);
             }
           }
-          // over S^T columns this thread has already read
-          tmem_st16(tS + lane_off + 64 * wg + 16 * c, pk);
+          tmem_st16(tdP + lane_off + 64 * wg + 16 * c, dk);
+          // dS^T row into shared memory (MN-major, 128B swizzle): chunk j of
+          // 16 bytes holds queries 8j..8j+7 of this warpgroup's panel
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = 4 * c + u;
+            uint4 v = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+            *reinterpret_cast<uint4*>(sds + ((j ^ (row & 7)) << 4)) = v;
+          }
           tmem_wait_st();
+          if (c == 1) fence_async_smem();   // the whole dS panel, for the dQ MMAs
           tc_fence_before();
-          mbar_arrive(&bars->p_half[c]);
+          mbar_arrive(&bars->ds_half[c]);
         }
-      };
-      if (qt.full)
-        exps(std::false_type{});
-      else
-        exps(std::true_type{});
-      // phase 2: dS^T = P^T (dP^T - delta), fp16, to tensor memory (A of the
-      // dK MMAs) and to this warpgroup's dS panel (A of the dQ MMAs)
-      // the dS panels hold half of the previous tile's dQ until its reduce
-      // has read them
-      w = mbar_wait(&bars->dp_full, n & 1, abort, status);
-      if (w && n > 0) w = mbar_wait(&bars->ds_free, (n - 1) & 1, abort, status);
-      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-      tc_fence_after();
+        // the next tile's Q conversion overlaps this tile's dK/dQ MMAs
+        if (n + 1 < n_vis && !convert_q(n + 1)) { ok = false; break; }
+        // dQ read-back from the dP^T columns: thread = query row, warpgroup wg
+        // takes columns [wg*D/2, (wg+1)*D/2).  Tensor memory is released before
+        // the reduces are issued, so the next tile's dP^T never waits on them.
+        w = mbar_wait(&bars->dq_full, n & 1, abort, status);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t r[D / 2];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t dr[32];
-        tmem_ld32(tdP + lane_off + 64 * wg + 32 * c, dr);
-        tmem_wait_ld32(dr);
-        uint32_t dk[16];
+        for (int c = 0; c < D / 2; c += 32) tmem_ld32(tdP + lane_off + wg * (D / 2) + c, r + c);
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(dls + 32 * c + i);
-          const float2 dp[2] = {make_float2(d4.x, d4.y), make_float2(d4.z, d4.w)};
+        for (int c = 0; c < D / 2; c += 32) tmem_wait_ld32(r + c);
+        tc_fence_before();
+        mbar_arrive(&bars->tmem_free);
+        // scale * dQ staged for the producer's TMA reduce-add over the dS panels
+        // (warpgroup 0) or this tile's dO (warpgroup 1), both free since the
+        // dQ MMA ran: 32-column boxes of 128 rows, 128B-swizzled like the
+        // reduce's map
+        uint8_t* stg = smem + (wg == 0 ? L::DS_OFF : L::DO_OFF + (n & 1) * L::TILE) + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int j = i + 2 * u;
-            const float2 pp = make_float2(__uint_as_float(pr[32 * c + j]), __uint_as_float(pr[32 * c + j + 1]));
-            const float2 d = fmul2(pp, fsub2(make_float2(__uint_as_float(dr[j]), __uint_as_float(dr[j + 1])), dp[u]));
-            dk[j >> 1] = pack_f16x2(d.x, d.y);
+        for (int sub = 0; sub < D / 64; ++sub) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t* x = r + 32 * sub + 4 * j;
+            const float4 v = make_float4(a.scale * __uint_as_float(x[0]), a.scale * __uint_as_float(x[1]),
+                                         a.scale * __uint_as_float(x[2]), a.scale * __uint_as_float(x[3]));
+            *reinterpret_cast<float4*>(stg + sub * PANEL + ((j ^ (row & 7)) << 4)) = v;
           }
         }
-        tmem_st16(tdP + lane_off + 64 * wg + 16 * c, dk);
-        // dS^T row into shared memory (MN-major, 128B swizzle): chunk j of
-        // 16 bytes holds queries 8j..8j+7 of this warpgroup's panel
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int j = 4 * c + u;
-          uint4 v = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
-          *reinterpret_cast<uint4*>(sds + ((j ^ (row & 7)) << 4)) = v;
+        fence_async_smem();
+        mbar_arrive(&bars->dq_staged[n & 1]);
+        if constexpr (F16PV) {   // after the dQ read-back, which the next dP^T waits for anyway
+          if (n + 1 < n_vis && !convert_do(n + 1)) { ok = false; break; }
         }
-        tmem_wait_st();
-        if (c == 1) fence_async_smem();   // the whole dS panel, for the dQ MMAs
-        tc_fence_before();
-        mbar_arrive(&bars->ds_half[c]);
+        ++n;
       }
-      // the next tile's Q conversion overlaps this tile's dK/dQ MMAs
-      if (n + 1 < n_vis && !convert_q(n + 1)) { ok = false; break; }
-      // dQ read-back from the dP^T columns: thread = query row, warpgroup wg
-      // takes columns [wg*D/2, (wg+1)*D/2).  Tensor memory is released before
-      // the reduces are issued, so the next tile's dP^T never waits on them.
-      w = mbar_wait(&bars->dq_full, n & 1, abort, status);
-      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t r[D / 2];
-#pragma unroll
-      for (int c = 0; c < D / 2; c += 32) tmem_ld32(tdP + lane_off + wg * (D / 2) + c, r + c);
-#pragma unroll
-      for (int c = 0; c < D / 2; c += 32) tmem_wait_ld32(r + c);
-      tc_fence_before();
-      mbar_arrive(&bars->tmem_free);
-      // scale * dQ staged for the producer's TMA reduce-add over the dS panels
-      // (warpgroup 0) or this tile's dO (warpgroup 1), both free since the
-      // dQ MMA ran: 32-column boxes of 128 rows, 128B-swizzled like the
-      // reduce's map
-      uint8_t* stg = smem + (wg == 0 ? L::DS_OFF : L::DO_OFF + (n & 1) * L::TILE) + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-      for (int sub = 0; sub < D / 64; ++sub) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t* x = r + 32 * sub + 4 * j;
-          const float4 v = make_float4(a.scale * __uint_as_float(x[0]), a.scale * __uint_as_float(x[1]),
-                                       a.scale * __uint_as_float(x[2]), a.scale * __uint_as_float(x[3]));
-          *reinterpret_cast<float4*>(stg + sub * PANEL + ((j ^ (row & 7)) << 4)) = v;
-        }
-      }
-      fence_async_smem();
-      mbar_arrive(&bars->dq_staged[n & 1]);
-      ++n;
     }
     // dK (warpgroup 0, times scale) and dV (warpgroup 1): thread = key row,
     // staged fp32 in 32-column 128B-swizzled boxes over the K/V tiles (dK)
@@ -595,9 +642,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
         for (int bx = 0; bx < D / 32; ++bx) {
           if (a.accumulate)
-            tma_reduce_add_4d(m, base + bx * PANEL, 32 * bx, dkrow0, h, b);
+            tma_reduce_add_4d(m, base + bx * PANEL, 32 * bx, dkrow0, hk, b);
           else
-            tma_store_4d(m, base + bx * PANEL, 32 * bx, dkrow0, h, b);
+            tma_store_4d(m, base + bx * PANEL, 32 * bx, dkrow0, hk, b);
         }
         bulk_commit();
         bulk_wait_all();
@@ -613,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   }
 }
 
-template <int D>
+template <int D, bool F16PV>
 static cudaError_t launch(TcArgs& ta, cudaStream_t st) {
   using L = Layout<D>;
   static std::once_flag once[64];
@@ -621,11 +668,12 @@ static cudaError_t launch(TcArgs& ta, cudaStream_t st) {
   int dev = 0;
   cudaGetDevice(&dev);
   std::call_once(once[dev & 63], [&] {
-    attr_err[dev & 63] = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    attr_err[dev & 63] =
+        cudaFuncSetAttribute(bwd_tc_kernel<D, F16PV>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   });
   if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
-  dim3 grid(ta.a.max_k_tiles, ta.a.B * ta.a.H, ta.a.n_items);
-  bwd_tc_kernel<D><<<grid, kThreads, L::SMEM, st>>>(ta);
+  dim3 grid(ta.a.max_k_tiles, ta.a.B * ta.a.Hkv, ta.a.n_items);   // one CTA per key tile of a key/value head
+  bwd_tc_kernel<D, F16PV><<<grid, kThreads, L::SMEM, st>>>(ta);
   return cudaGetLastError();
 }
 
@@ -675,16 +723,18 @@ cudaError_t tc_backward(AttnArgs& a, cudaStream_t st) {
       const int64_t qr = slab_extent(it.qs, a.q_by_pos), kr = slab_extent(it.ks, a.kv_by_pos),
                     dkr = slab_extent(it.ks, a.dkv_by_pos);
       if ((e = make_tmap_bf16(&m[0], it.q, a.D, qr, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
-      if ((e = make_tmap_bf16(&m[1], it.k, a.D, kr, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
-      if ((e = make_tmap_bf16(&m[2], it.v, a.D, kr, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
+      if ((e = make_tmap_bf16(&m[1], it.k, a.D, kr, a.Hkv, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
+      if ((e = make_tmap_bf16(&m[2], it.v, a.D, kr, a.Hkv, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
       if ((e = make_tmap_bf16(&m[3], it.dout, a.D, qr, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
       if ((e = make_tmap_f32(&m[4], it.o, a.D, qr, a.H, a.B, a.o, 32, BM)) != cudaSuccess) return e;
-      if ((e = make_tmap_f32(&m[5], it.dk, a.D, dkr, a.H, a.B, a.dkv, 32, BN)) != cudaSuccess) return e;
-      if ((e = make_tmap_f32(&m[6], it.dv, a.D, dkr, a.H, a.B, a.dkv, 32, BN)) != cudaSuccess) return e;
+      if ((e = make_tmap_f32(&m[5], it.dk, a.D, dkr, a.Hkv, a.B, a.dkv, 32, BN)) != cudaSuccess) return e;
+      if ((e = make_tmap_f32(&m[6], it.dv, a.D, dkr, a.Hkv, a.B, a.dkv, 32, BN)) != cudaSuccess) return e;
     }
     if (mt == 0) continue;
     ta.a.max_k_tiles = static_cast<int>(mt);
-    const cudaError_t e = a.D == 64 ? launch<64>(ta, st) : launch<128>(ta, st);
+    const bool f16pv = a.group > 1;
+    const cudaError_t e = a.D == 64 ? (f16pv ? launch<64, true>(ta, st) : launch<64, false>(ta, st))
+                                    : (f16pv ? launch<128, true>(ta, st) : launch<128, false>(ta, st));
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   const int64_t q0 = static_cast<int64_t>(a.max_q_tiles - 1 - blockIdx.x) * BM;  // heavy tiles first
   if (q0 >= gm.Sq) return;
   const int b = blockIdx.y / a.H, h = blockIdx.y % a.H;
+  const int hk = h / a.group;   // key/value head of this query head
   const int nq = static_cast<int>(min64(BM, gm.Sq - q0));
   int64_t qmin, qmax;
   tile_pos_range(gm.qs, q0, nq, qmin, qmax);
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         mbar_arrive_expect_tx(&bars->k_full[st], L::TILE);
         for (int p = 0; p < D / 64; ++p)
           tma_load_4d(smem + L::K_OFF + st * L::TILE + p * PANEL, mk, &bars->k_full[st], 64 * p,
-                      static_cast<int>(slab_row(gm.ks, a.kv_by_pos, static_cast<int64_t>(kt) * BN)), h, b);
+                      static_cast<int>(slab_row(gm.ks, a.kv_by_pos, static_cast<int64_t>(kt) * BN)), hk, b);
       }
       if (!__shfl_sync(0xffffffffu, w, 0)) break;
       ++n;
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         mbar_arrive_expect_tx(&bars->v_full[st], L::TILE);
         for (int p = 0; p < D / 64; ++p)
           tma_load_4d(smem + L::V_OFF + st * L::TILE + p * PANEL, mv, &bars->v_full[st], 64 * p,
-                      static_cast<int>(slab_row(gm.ks, a.kv_by_pos, static_cast<int64_t>(kt) * BN)), h, b);
+                      static_cast<int>(slab_row(gm.ks, a.kv_by_pos, static_cast<int64_t>(kt) * BN)), hk, b);
       }
       if (!__shfl_sync(0xffffffffu, w, 0)) break;
       ++n;
@@ -469,8 +470,8 @@ cudaError_t tc_forward(AttnArgs& a, cudaStream_t st) {
     cudaError_t e;
     const int64_t q_rows = slab_extent(it.qs, a.q_by_pos), kv_rows = slab_extent(it.ks, a.kv_by_pos);
     if ((e = make_tmap_bf16(&ta.maps[i][0], it.q, a.D, q_rows, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
-    if ((e = make_tmap_bf16(&ta.maps[i][1], it.k, a.D, kv_rows, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
-    if ((e = make_tmap_bf16(&ta.maps[i][2], it.v, a.D, kv_rows, a.H, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&ta.maps[i][1], it.k, a.D, kv_rows, a.Hkv, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&ta.maps[i][2], it.v, a.D, kv_rows, a.Hkv, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
   }
   a.max_q_tiles = static_cast<int>(mt);
   ta.a = a;

@@ -75,12 +75,14 @@ class ShardedCausalAttention:
     ``dtype`` (bf16 or fp32), contiguous, on the current CUDA device.
     Outputs are fp32 [B, H, S, D] (and lse [B, H, S], natural log).
     ``backward`` reads the q, k, v of the last ``forward`` (kept by
-    reference) unless they are passed again.
+    reference) unless they are passed again.  With ``kv_heads`` < H
+    (grouped-query attention) k and v, and dk and dv, have kv_heads heads;
+    query head h reads key/value head h // (H // kv_heads).
     """
 
     def __init__(self, B, H, S, D, P, layout="zigzag", dtype=torch.bfloat16, head_groups=1,
                  schedule="ring", scale=None, causal=True, algo=capi.SCA_ALGO_AUTO, backward=False,
-                 bf16_out=False, device=None, addressing="auto"):
+                 bf16_out=False, device=None, addressing="auto", kv_heads=None):
         if layout not in ("zigzag", "contiguous"):
             raise ValueError(f"layout {layout!r}")
         if schedule not in ("ring", "direct", "fused"):
@@ -91,8 +93,11 @@ class ShardedCausalAttention:
             raise ValueError(f"dtype {dtype}")
         if S % (2 * P if layout == "zigzag" else P):
             raise ValueError(f"S={S} not divisible into {P} {layout} shards")
-        if H % head_groups:
-            raise ValueError("head_groups must divide H")
+        Hkv = H if kv_heads is None else int(kv_heads)
+        if Hkv < 1 or H % Hkv:
+            raise ValueError(f"kv_heads={kv_heads} must divide H={H}")
+        if H % head_groups or Hkv % head_groups:
+            raise ValueError("head_groups must divide H and kv_heads")
         if head_groups * P > capi.SCA_MAX_ITEMS:
             raise ValueError(f"{head_groups * P} virtual ranks > {capi.SCA_MAX_ITEMS}")
         zig = layout == "zigzag"
@@ -103,6 +108,7 @@ class ShardedCausalAttention:
             raise ValueError(f"position addressing needs shard segments of a multiple of 128 rows ({seg_len})")
         self.B, self.H, self.S, self.D, self.P = B, H, S, D, P
         self.G, self.Hg = head_groups, H // head_groups
+        self.Hkv, self.Hkvg = Hkv, Hkv // head_groups   # key/value heads: all, per head group
         self.layout, self.schedule, self.dtype = layout, schedule, dtype
         self.addressing = addressing
         self.pos = addressing == "position"
@@ -116,28 +122,28 @@ class ShardedCausalAttention:
         self.device = dev
         z = lambda *shape, dt=torch.float32: torch.empty(shape, dtype=dt, device=dev)
         self.qp = z(B, H, S, D, dt=dtype) if self.perm else None
-        self.kp = z(B, H, S, D, dt=dtype) if self.perm else None
-        self.vp = z(B, H, S, D, dt=dtype) if self.perm else None
+        self.kp = z(B, Hkv, S, D, dt=dtype) if self.perm else None
+        self.vp = z(B, Hkv, S, D, dt=dtype) if self.perm else None
         self.o_parts = z(P, B, H, S, D) if not fused else None
         self.lse_parts = z(P, B, H, S) if not fused else None
         self.o = z(B, H, S, D)
         self.lse = z(B, H, S)
         self.o_bf16 = z(B, H, S, D, dt=torch.bfloat16) if bf16_out else None
         ring = schedule == "ring" and P > 1
-        self.stage_k = [z(self.G, P, B, self.Hg, self.n_r, D, dt=dtype) for _ in range(2)] if ring else None
-        self.stage_v = [z(self.G, P, B, self.Hg, self.n_r, D, dt=dtype) for _ in range(2)] if ring else None
+        self.stage_k = [z(self.G, P, B, self.Hkvg, self.n_r, D, dt=dtype) for _ in range(2)] if ring else None
+        self.stage_v = [z(self.G, P, B, self.Hkvg, self.n_r, D, dt=dtype) for _ in range(2)] if ring else None
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         if backward:
             self.delta = z(B, H, S)
             self.dq = z(B, H, S, D)
-            self.dk = z(B, H, S, D)
-            self.dv = z(B, H, S, D)
+            self.dk = z(B, Hkv, S, D)
+            self.dv = z(B, Hkv, S, D)
             self.dop = z(B, H, S, D, dt=dtype) if self.perm else None
             self.lse_p = z(B, H, S) if self.perm else None
             self.delta_p = z(B, H, S) if self.perm else None
             self.dq_p = z(B, H, S, D) if self.perm else None
-            self.dk_p = z(B, H, S, D) if self.perm else None
-            self.dv_p = z(B, H, S, D) if self.perm else None
+            self.dk_p = z(B, Hkv, S, D) if self.perm else None
+            self.dv_p = z(B, Hkv, S, D) if self.perm else None
         self.copy_stream = torch.cuda.Stream(device=dev) if ring else None
         self.ev_ready = torch.cuda.Event()
         self.ev_staged = [torch.cuda.Event() for _ in range(P)]
@@ -149,7 +155,8 @@ class ShardedCausalAttention:
     # ------------------------------------------------------------ helpers
 
     def _permute(self, src, dst, row_bytes, inverse, stream):
-        capi.zigzag_permute(_ptr(src), _ptr(dst), self.B * self.H, self.S, row_bytes, self.P, inverse, stream)
+        capi.zigzag_permute(_ptr(src), _ptr(dst), src.numel() // (self.S * (row_bytes // src.element_size())),
+                            self.S, row_bytes, self.P, inverse, stream)
         self.launches += 1
         self.kernels += 1
 
@@ -160,6 +167,11 @@ class ShardedCausalAttention:
         their positions instead)."""
         off = g * self.Hg * self.S
         return off if self.pos else off + r * self.n_r
+
+    def _kv_rows(self, g, j):
+        """The same for key/value-side tensors (kv_heads heads)."""
+        off = g * self.Hkvg * self.S
+        return off if self.pos else off + j * self.n_r
 
     # ------------------------------------------------- kernel descriptions
 
@@ -184,6 +196,7 @@ class ShardedCausalAttention:
     def _dims(self, kv_view, backward=False, accumulate=0, q_by_pos=0, kv_by_pos=0, dkv_by_pos=0):
         d = capi.sca_attn_dims()
         d.B, d.H, d.D = self.B, self.Hg, self.D
+        d.kv_heads = self.Hkvg
         d.dtype = _DT[self.dtype]
         d.causal = 1 if self.causal else 0
         d.algo = self.algo
@@ -193,23 +206,22 @@ class ShardedCausalAttention:
         d.q = capi.view(H * S * D, S * D, D)
         d.kv = kv_view
         d.o = capi.view(H * S * D, S * D, D)
-        d.dkv = capi.view(H * S * D, S * D, D)
+        d.dkv = capi.view(self.Hkv * S * D, S * D, D)
         d.lse_b, d.lse_h = H * S, S
         d.q_by_pos, d.kv_by_pos, d.dkv_by_pos = int(q_by_pos), int(kv_by_pos), int(dkv_by_pos)
         return d
 
     def _home_kv_view(self):
-        return capi.view(self.H * self.S * self.D, self.S * self.D, self.D)
+        return capi.view(self.Hkv * self.S * self.D, self.S * self.D, self.D)
 
     def _stage_kv_view(self):
-        return capi.view(self.Hg * self.n_r * self.D, self.n_r * self.D, self.D)
+        return capi.view(self.Hkvg * self.n_r * self.D, self.n_r * self.D, self.D)
 
     def _kv_ptrs(self, k_home, v_home, t, g, r):
         """(k, v) base pointers of the block rank (g, r) holds at step t."""
         P = self.P
         if self.stage_k is None or t == 0:
-            j = ring_block(r, t, P)
-            off = (g * self.Hg * self.S + (0 if self.pos else j * self.n_r)) * self.D * self.eb
+            off = self._kv_rows(g, ring_block(r, t, P)) * self.D * self.eb
             return _ptr(k_home) + off, _ptr(v_home) + off
         buf = t % 2
         return _ptr(self.stage_k[buf][g, r]), _ptr(self.stage_v[buf][g, r])
@@ -217,7 +229,7 @@ class ShardedCausalAttention:
     def _stage(self, k_home, v_home, t_next):
         """Ring pass into the spare buffer: rank (g, r) receives what rank
         (g, r-1) holds at step t_next - 1."""
-        P, B, Hg, n_r, D, eb = self.P, self.B, self.Hg, self.n_r, self.D, self.eb
+        P, B, Hg, n_r, D, eb = self.P, self.B, self.Hkvg, self.n_r, self.D, self.eb
         cs = self.copy_stream.cuda_stream
         dst_k, dst_v = self.stage_k[t_next % 2], self.stage_v[t_next % 2]
         row = D * eb
@@ -226,7 +238,7 @@ class ShardedCausalAttention:
                 for r in range(P):
                     src_r = (r - 1) % P
                     for b in range(B):
-                        off = ((b * self.H + g * Hg) * self.S) * row
+                        off = ((b * self.Hkv + g * Hg) * self.S) * row
                         for home, dst in ((k_home, dst_k), (v_home, dst_v)):
                             if self.pos:   # gather the block's chunks from natural order
                                 capi.ring_stage_segments(_ptr(home) + off, _ptr(dst[g, r, b]), Hg, self.S,
@@ -272,7 +284,8 @@ class ShardedCausalAttention:
     # ------------------------------------------------------------ forward
 
     def forward(self, q, k, v):
-        self._check_inputs(q, k, v)
+        self._check_inputs(q)
+        self._check_inputs(k, v, heads=self.Hkv)
         self.launches = self.kernels = 0
         self._inputs = (q, k, v)
         stream = torch.cuda.current_stream(self.device).cuda_stream
@@ -324,9 +337,9 @@ class ShardedCausalAttention:
         S, D, eb = self.S, self.D, self.eb
         items = []
         for g in range(self.G):
-            rows = g * self.Hg * S
+            rows, kv_rows = g * self.Hg * S, g * self.Hkvg * S
             it = capi.sca_fwd_item()
-            it.q, it.k, it.v = _ptr(q) + rows * D * eb, _ptr(k) + rows * D * eb, _ptr(v) + rows * D * eb
+            it.q, it.k, it.v = _ptr(q) + rows * D * eb, _ptr(k) + kv_rows * D * eb, _ptr(v) + kv_rows * D * eb
             it.o = _ptr(self.o) + rows * D * 4
             it.lse = _ptr(self.lse) + rows * 4
             it.q_pos = capi.segs(1, S, (0, 0))
@@ -354,7 +367,8 @@ class ShardedCausalAttention:
             if self._inputs is None:
                 raise RuntimeError("backward before forward")
             q, k, v = self._inputs
-        self._check_inputs(do, q, k, v)
+        self._check_inputs(do, q)
+        self._check_inputs(k, v, heads=self.Hkv)
         self.launches = self.kernels = 0
         stream = torch.cuda.current_stream(self.device).cuda_stream
         S, D, H, P, B = self.S, self.D, self.H, self.P, self.B
@@ -383,7 +397,7 @@ class ShardedCausalAttention:
             for g in range(self.G):
                 for r in range(P):
                     j = ring_block(r, t, P)
-                    qo, ko = self._rows(g, r), self._rows(g, j)
+                    qo, ko = self._rows(g, r), self._kv_rows(g, j)
                     it = capi.sca_bwd_item()
                     it.q = _ptr(qh) + qo * D * eb
                     it.dout = _ptr(doh) + qo * D * eb
@@ -416,12 +430,13 @@ class ShardedCausalAttention:
         S, D, eb = self.S, self.D, self.eb
         items = []
         for g in range(self.G):
-            rows = g * self.Hg * S
+            rows, kv_rows = g * self.Hg * S, g * self.Hkvg * S
             it = capi.sca_bwd_item()
-            it.q, it.k, it.v = _ptr(q) + rows * D * eb, _ptr(k) + rows * D * eb, _ptr(v) + rows * D * eb
+            it.q, it.k, it.v = _ptr(q) + rows * D * eb, _ptr(k) + kv_rows * D * eb, _ptr(v) + kv_rows * D * eb
             it.dout = _ptr(do) + rows * D * eb
             it.lse, it.delta = _ptr(self.lse) + rows * 4, _ptr(self.delta) + rows * 4
-            it.dq, it.dk, it.dv = (_ptr(x) + rows * D * 4 for x in (self.dq, self.dk, self.dv))
+            it.dq = _ptr(self.dq) + rows * D * 4
+            it.dk, it.dv = _ptr(self.dk) + kv_rows * D * 4, _ptr(self.dv) + kv_rows * D * 4
             it.q_pos = capi.segs(1, S, (0, 0))
             it.kv_pos = capi.segs(1, S, (0, 0))
             items.append(it)
@@ -434,9 +449,10 @@ class ShardedCausalAttention:
         """Synchronise and return the device status word (0 = OK)."""
         return capi.sca_read_status(_ptr(self.status), torch.cuda.current_stream(self.device).cuda_stream)
 
-    def _check_inputs(self, *ts):
+    def _check_inputs(self, *ts, heads=None):
+        H = self.H if heads is None else heads
         for t in ts:
             if t.dtype != self.dtype or t.device != self.device or not t.is_contiguous() or \
-                    tuple(t.shape) != (self.B, self.H, self.S, self.D):
-                raise ValueError(f"expected contiguous {self.dtype} [{self.B},{self.H},{self.S},{self.D}] "
+                    tuple(t.shape) != (self.B, H, self.S, self.D):
+                raise ValueError(f"expected contiguous {self.dtype} [{self.B},{H},{self.S},{self.D}] "
                                  f"on {self.device}, got {t.dtype} {tuple(t.shape)} on {t.device}")

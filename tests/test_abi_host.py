@@ -55,7 +55,7 @@ int main(void) {
   P(sca_view)
   P(sca_attn_dims) F(sca_attn_dims, scale) F(sca_attn_dims, accumulate) F(sca_attn_dims, q)
   F(sca_attn_dims, kv) F(sca_attn_dims, o) F(sca_attn_dims, dkv) F(sca_attn_dims, lse_b) F(sca_attn_dims, lse_h)
-  F(sca_attn_dims, q_by_pos) F(sca_attn_dims, kv_by_pos) F(sca_attn_dims, dkv_by_pos)
+  F(sca_attn_dims, q_by_pos) F(sca_attn_dims, kv_by_pos) F(sca_attn_dims, dkv_by_pos) F(sca_attn_dims, kv_heads)
   P(sca_fwd_item) F(sca_fwd_item, o) F(sca_fwd_item, lse) F(sca_fwd_item, q_pos) F(sca_fwd_item, kv_pos)
   P(sca_bwd_item) F(sca_bwd_item, dout) F(sca_bwd_item, delta) F(sca_bwd_item, dv) F(sca_bwd_item, q_pos)
   F(sca_bwd_item, kv_pos)
@@ -144,6 +144,8 @@ def _fwd_rc(lib, items, dims, n=None):
     ("by_pos_segment_not_x128", capi.SCA_ERR_UNSUPPORTED),
     ("by_pos_kv_segment_not_x128", capi.SCA_ERR_UNSUPPORTED),
     ("dkv_by_pos_in_forward", capi.SCA_ERR_ARG),
+    ("kv_heads_not_dividing", capi.SCA_ERR_ARG),
+    ("kv_heads_negative", capi.SCA_ERR_ARG),
 ])
 def test_fwd_rejects_bad_arguments(lib, case, expect):
     items, dims, n = [_item()], _dims(), None
@@ -182,6 +184,10 @@ def test_fwd_rejects_bad_arguments(lib, case, expect):
         items = [_item(kv_pos=capi.segs(1, 200, (0, 0)))]
     elif case == "dkv_by_pos_in_forward":
         dims = _dims(dkv_by_pos=1)
+    elif case == "kv_heads_not_dividing":   # H = 2
+        dims = _dims(kv_heads=3)
+    elif case == "kv_heads_negative":
+        dims = _dims(kv_heads=-1)
     rc = _fwd_rc(lib, items, dims, n)
     assert rc == expect, (case, rc, capi.last_error())
     assert capi.last_error()

@@ -1,0 +1,33 @@
+"""Host-side argument checks of the sharded schedule (they run before any
+device memory is touched, so no GPU is needed)."""
+import pytest
+
+from sharded_causal_softmax_gb300.sharded import ShardedCausalAttention, ring_block, shard_segs
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(kv_heads=3), "kv_heads"),                          # 3 does not divide 8
+    (dict(kv_heads=2, head_groups=4), "head_groups"),        # 4 groups cannot split 2 key/value heads
+    (dict(schedule="spiral"), "schedule"),
+    (dict(addressing="sideways"), "addressing"),
+    (dict(addressing="position", S=768), "128"),             # zigzag chunks of 96 rows
+    (dict(layout="diagonal"), "layout"),
+])
+def test_schedule_rejects_bad_arguments(kw, msg):
+    args = dict(B=1, H=8, S=1024, D=128, P=4)
+    args.update({k: v for k, v in kw.items() if k in args})
+    extra = {k: v for k, v in kw.items() if k not in args}
+    with pytest.raises(ValueError, match=msg):
+        ShardedCausalAttention(args["B"], args["H"], args["S"], args["D"], args["P"], **extra)
+
+
+def test_ring_order_and_zigzag_segments():
+    P = 4
+    # every shard visits every block exactly once, starting with its own
+    for r in range(P):
+        assert sorted(ring_block(r, t, P) for t in range(P)) == list(range(P))
+        assert ring_block(r, 0, P) == r
+    s = shard_segs(1024, P, "zigzag", 1)
+    assert (s.n, s.len, s.start[0], s.start[1]) == (2, 128, 128, 768)
+    s = shard_segs(1024, P, "contiguous", 3)
+    assert (s.n, s.len, s.start[0]) == (1, 256, 768)
