@@ -32,12 +32,18 @@ What it computes, and where that comes from:
   query heads in consecutive groups share one key/value head ("Avances en la
   capacitacion de LLMs de secuencia larga", section "Comprendiendo la
   Arquitectura de los LLMs"); the key/value gradients sum over the group.
+* ``linear`` - causal linear attention and its sequence-parallel form
+  (LASP: states passed point to point between contiguous shards; "Effiziente
+  Parallelisierung linearer Aufmerksamkeitssequenzen fuer skalierbare
+  Sprachmodelle").
 
 Everything is float64 numpy; matmul is the only library primitive used.
 """
 from .attention import (attention, attention_rows, attention_backward, attention_backward_block,
                         attention_backward_gqa, attention_gqa, backward_query_rows, backward_key_columns,
                         kv_head_of, merge_lse, softmax_matrix)
+from .linear import (lasp_backward, lasp_forward, linear_attention, linear_attention_backward,
+                     shard_bounds)
 from .shards import (chunk_len, zigzag_order, contiguous_order, shard_order,
                      shard_positions, permute_rows, ring_visit_order,
                      double_ring_visit_order, sharded_attention,
@@ -50,5 +56,6 @@ __all__ = [
     "backward_key_columns", "merge_lse", "softmax_matrix", "chunk_len",
     "zigzag_order", "contiguous_order", "shard_order", "shard_positions",
     "permute_rows", "ring_visit_order", "double_ring_visit_order",
-    "sharded_attention", "visible_pairs",
+    "sharded_attention", "visible_pairs", "linear_attention", "linear_attention_backward",
+    "lasp_forward", "lasp_backward", "shard_bounds",
 ]
