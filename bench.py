@@ -47,6 +47,15 @@ L2_BYTES = 129 * 2 ** 20
 
 
 def flops(w, fwd=True, bwd=True):
+    if w.method == "lasp":
+        # the chunked linear-attention algorithm with blocks of C rows, per row:
+        # forward K^T V and Q.state (2 D^2 each) and the block's left product
+        # (2 C D twice); backward two state products more and six block ones
+        C, rows = 64.0, w.B * w.H * w.S
+        f = rows * (4.0 * w.D * w.D + 4.0 * C * w.D) if fwd else 0.0
+        if bwd and w.backward:
+            f += rows * (8.0 * w.D * w.D + 12.0 * C * w.D)
+        return f
     f = 2.0 * w.B * w.H * w.S * w.S * w.D if fwd else 0.0
     if bwd and w.backward:
         f += 5.0 * w.B * w.H * w.S * w.S * w.D
@@ -198,6 +207,8 @@ def run_gpu(args):
     if args.schedule:
         w = dataclasses.replace(w, schedule=args.schedule)
     def make_plan():
+        if w.method == "lasp":
+            return sca.ShardedLinearAttention(w.B, w.H, w.S, w.D, w.P, dtype=dtype, backward=w.backward)
         return sca.ShardedCausalAttention(w.B, w.H, w.S, w.D, w.P, layout=w.layout, dtype=dtype,
                                           head_groups=w.head_groups, schedule=w.schedule, backward=w.backward,
                                           addressing=args.addressing, kv_heads=w.kv_heads)
@@ -224,6 +235,8 @@ def run_gpu(args):
     timing_on = [False]
     sca.sharded.capi.attn_fwd_shard = timed("fwd", orig_fwd)
     sca.sharded.capi.attn_bwd_shard = timed("bwd", orig_bwd)
+    sca.capi.lasp_fwd = timed("fwd", sca.capi.lasp_fwd)
+    sca.capi.lasp_bwd = timed("bwd", sca.capi.lasp_bwd)
 
     # HBM-bound kernels: events around each call, algorithmic bytes from its
     # arguments (read + written once)
@@ -304,7 +317,8 @@ def run_gpu(args):
     dins = [dev_in, [torch.empty_like(x) for x in dev_in]]
 
     def results(p):
-        return [p.o, p.lse] + ([p.dq, p.dk, p.dv] if w.backward else [])
+        out = [p.o] + ([p.lse] if hasattr(p, "lse") else [])
+        return out + ([p.dq, p.dk, p.dv] if w.backward else [])
 
     outs_host = [[torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in results(p)] for p in plans]
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
@@ -428,7 +442,7 @@ def run_gpu(args):
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded N(0,1))",
         "config": {"workload": w.description, "name": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "P": w.P,
-                   "layout": w.layout, "schedule": w.schedule, "addressing": plan.addressing,
+                   "method": w.method, "layout": w.layout, "schedule": w.schedule, "addressing": plan.addressing,
                    "kv_heads": w.kv_heads or w.H,
                    "head_groups": w.head_groups,
                    "step": "fwd+bwd" if w.backward else "fwd",
@@ -460,13 +474,18 @@ def oracle_sample(w, S_sample):
     prefix is itself a causal attention problem): inputs and FLOPs."""
     ins = seeded_inputs.workload_inputs(w)
     head = [x[:1, :1, :S_sample] for x in ins]
-    f = 2.0 * S_sample * S_sample * w.D + (5.0 * S_sample * S_sample * w.D if w.backward else 0.0)
+    f = flops(dataclasses.replace(w, B=1, H=1, S=S_sample))
     return head, f
 
 
 def run_oracle_once(w, head):
     import oracle
     scale = 1.0 / math.sqrt(w.D)
+    if w.method == "lasp":
+        oracle.linear_attention(head[0], head[1], head[2], scale)
+        if w.backward:
+            oracle.linear_attention_backward(head[0], head[1], head[2], head[3], scale)
+        return
     o, lse = oracle.attention(head[0], head[1], head[2], scale)
     if w.backward:
         oracle.attention_backward(head[0], head[1], head[2], head[3], scale, o=o, lse=lse)

@@ -238,6 +238,59 @@ int attn_bwd_shard(const sca_bwd_item* items, int n_items, const sca_attn_dims* 
 int attn_bwd_delta(const float* o, const void* dout, int dout_dtype, float* delta,
                    int64_t rows, int D, void* stream);
 
+/* ---- Linear attention sequence parallelism (LASP) --------------------
+ * Causal linear attention (identity feature map, no normalisation):
+ *   o_t = scale * sum_{s <= t} (q_t . k_s) v_s
+ * over P contiguous shards of the sequence, which exchange D x D states
+ * point to point: the k^T v of earlier shards in the forward, the q^T dO of
+ * later shards in the backward, and use the right product q . state
+ * ("Effiziente Parallelisierung linearer Aufmerksamkeitssequenzen fuer
+ * skalierbare Sprachmodelle", the LASP summary; it prints no formula, this
+ * is the plain reading).  Tensors q, k, v, dout are row-contiguous
+ * [BH, S, D] (BH = batch x heads) of dtype bf16 or fp32; o, dq, dk, dv are
+ * fp32 [BH, S, D], overwritten.  Rows go in blocks of SCA_LASP_BLOCK; S must
+ * be a multiple of SCA_LASP_BLOCK * P.  States are fp32 D x D, row index the
+ * first factor's column: per block st [BH, S/SCA_LASP_BLOCK, D, D], per
+ * shard [BH, P, D, D]; the caller owns every buffer (no allocation).  All
+ * arithmetic is fp32 on the CUDA cores.  Errors: SCA_ERR_ARG (NULL
+ * pointers, sizes), SCA_ERR_UNSUPPORTED (D not 64 or 128), SCA_ERR_CUDA. */
+#define SCA_LASP_BLOCK 64
+
+/* lasp_block_states - st[bh][j] = A_j^T B_j over the rows of block j:
+ * (A, B) = (k, v) for the forward, (q, dout) for the backward. */
+int lasp_block_states(const void* a, const void* b, int dtype, float* st, int64_t BH, int64_t S, int D,
+                      void* stream);
+
+/* lasp_scan - within each of the P shards (contiguous runs of blocks),
+ * replaces st[bh][j] by the sum over the shard's blocks before j
+ * (reverse = 0) or after j (reverse = 1), in place, and writes the sum over
+ * all the shard's blocks to shard_total[bh][r]. */
+int lasp_scan(float* st, float* shard_total, int64_t BH, int64_t S, int D, int P, int reverse, void* stream);
+
+/* lasp_exchange - the point-to-point pass of shard states, one hop at a
+ * time along the ring: shard_in[bh][r] = sum of shard_total[bh][s] over
+ * s < r (reverse = 0: shard r-1 sends to r) or s > r (reverse = 1: shard r+1
+ * sends to r). */
+int lasp_exchange(const float* shard_total, float* shard_in, int64_t BH, int D, int P, int reverse,
+                  void* stream);
+
+/* lasp_fwd - for every block j of shard r:
+ *   o_j = scale * (q_j (st[j] + shard_in[r]) + tril(q_j k_j^T) v_j)
+ * with st, shard_in from lasp_block_states(k, v) / lasp_scan(reverse = 0) /
+ * lasp_exchange(reverse = 0). */
+int lasp_fwd(const void* q, const void* k, const void* v, int dtype, const float* st, const float* shard_in,
+             float* o, int64_t BH, int64_t S, int D, int P, float scale, void* stream);
+
+/* lasp_bwd - for every block j of shard r, with F = st_fwd[j] + in_fwd[r]
+ * (the forward states) and G = st_bwd[j] + in_bwd[r] (from
+ * lasp_block_states(q, dout), lasp_scan and lasp_exchange with reverse = 1):
+ *   dq_j = scale * (dout_j F^T + tril(dout_j v_j^T) k_j)
+ *   dk_j = scale * (v_j G^T + tril(dout_j v_j^T)^T q_j)
+ *   dv_j = scale * (k_j G + tril(q_j k_j^T)^T dout_j) */
+int lasp_bwd(const void* q, const void* k, const void* v, const void* dout, int dtype, const float* st_fwd,
+             const float* in_fwd, const float* st_bwd, const float* in_bwd, float* dq, float* dk, float* dv,
+             int64_t BH, int64_t S, int D, int P, float scale, void* stream);
+
 /* Message of the last non-OK return on the calling thread ("" if none). */
 const char* sca_last_error(void);
 

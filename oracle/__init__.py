@@ -43,7 +43,7 @@ from .attention import (attention, attention_rows, attention_backward, attention
                         attention_backward_gqa, attention_gqa, backward_query_rows, backward_key_columns,
                         kv_head_of, merge_lse, softmax_matrix)
 from .linear import (lasp_backward, lasp_forward, linear_attention, linear_attention_backward,
-                     shard_bounds)
+                     linear_attention_rows, linear_dkv_rows, linear_dq_rows, shard_bounds)
 from .shards import (chunk_len, zigzag_order, contiguous_order, shard_order,
                      shard_positions, permute_rows, ring_visit_order,
                      double_ring_visit_order, sharded_attention,
@@ -57,5 +57,6 @@ __all__ = [
     "zigzag_order", "contiguous_order", "shard_order", "shard_positions",
     "permute_rows", "ring_visit_order", "double_ring_visit_order",
     "sharded_attention", "visible_pairs", "linear_attention", "linear_attention_backward",
-    "lasp_forward", "lasp_backward", "shard_bounds",
+    "lasp_forward", "lasp_backward", "shard_bounds", "linear_attention_rows", "linear_dq_rows",
+    "linear_dkv_rows",
 ]

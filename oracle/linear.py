@@ -137,3 +137,23 @@ def lasp_backward(q, k, v, do, scale, P, block):
             dv[r0:r1] = scale * (kb @ state_b + pm.T @ dob)
             state_b = state_b + qb.T @ dob
     return (dq, dk, dv), received
+
+
+def linear_attention_rows(q, k, v, scale, rows):
+    """o of the given query rows of one head [S, D] (left product per row)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    return np.stack([scale * ((k[:t + 1] @ q[t]) @ v[:t + 1]) for t in rows])
+
+
+def linear_dq_rows(q, k, v, do, scale, rows):
+    """dq of the given query rows of one head."""
+    k, v, do = _f64(k), _f64(v), _f64(do)
+    return np.stack([scale * ((v[:t + 1] @ do[t]) @ k[:t + 1]) for t in rows])
+
+
+def linear_dkv_rows(q, k, v, do, scale, cols):
+    """(dk, dv) of the given key rows of one head (every later query)."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    dk = np.stack([scale * ((do[s:] @ v[s]) @ q[s:]) for s in cols])
+    dv = np.stack([scale * ((q[s:] @ k[s]) @ do[s:]) for s in cols])
+    return dk, dv

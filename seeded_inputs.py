@@ -12,7 +12,9 @@ secuencia y tensor (TSP)", section "Resultados de memoria y rendimiento")
 uses as its reference model.  The grouped-query case stands for the 7B-GQA
 model of "Avances en la capacitacion de LLMs de secuencia larga" (section
 "Evaluacion y Comparacion con Sistemas Existentes"): 32 query heads; the page
-gives no key/value head count, 8 is the reading taken.
+gives no key/value head count, 8 is the reading taken.  The linear-attention
+case (LASP, "Effiziente Parallelisierung linearer Aufmerksamkeitssequenzen
+fuer skalierbare Sprachmodelle") takes the training shape of the softmax one.
 
 Recipe (fixed, so a reader can regenerate any case):
   g = torch.Generator('cpu').manual_seed(seed)
@@ -48,6 +50,7 @@ class Workload:
     sample_rows: int = 0        # 0: oracle checks every row
     description: str = ""
     kv_heads: int | None = None  # grouped-query attention: key/value heads
+    method: str = "softmax"      # "softmax" attention, or "lasp" (causal linear attention)
 
 
 WORKLOADS = {
@@ -78,6 +81,11 @@ WORKLOADS = {
         layout="zigzag", backward=True, sample_rows=256, kv_heads=8,
         description="grouped-query training step fwd+bwd B1 H32 (8 key/value heads) S32768 D128 bf16, "
                     "P=4 zigzag"),
+    "lasp_s32k": Workload(
+        "lasp_s32k", B=1, H=16, S=32768, D=128, dtype="bf16", seed=6, P=4, layout="contiguous",
+        backward=True, sample_rows=256, method="lasp",
+        description="linear attention (LASP) training step fwd+bwd B1 H16 S32768 D128 bf16, "
+                    "P=4 contiguous shards passing states point to point"),
 }
 
 

@@ -31,7 +31,9 @@ SCA_ALGO_TC = 2
 SCA_MAX_ITEMS = 32
 
 EXPORTED = ("attn_fwd_shard", "attn_merge_lse", "zigzag_permute", "ring_stage_block", "ring_stage_segments",
-            "attn_bwd_shard", "attn_bwd_delta", "sca_last_error", "sca_read_status", "sca_version")
+            "attn_bwd_shard", "attn_bwd_delta", "lasp_block_states", "lasp_scan", "lasp_exchange", "lasp_fwd",
+            "lasp_bwd", "sca_last_error", "sca_read_status", "sca_version")
+SCA_LASP_BLOCK = 64
 
 
 class ScaError(RuntimeError):
@@ -81,6 +83,13 @@ def _load():
         "ring_stage_segments": (c_int, [c_void_p, c_void_p, c_int64, c_int64, POINTER(sca_segs), c_int64, c_void_p]),
         "attn_bwd_shard": (c_int, [POINTER(sca_bwd_item), c_int, POINTER(sca_attn_dims), c_void_p, c_void_p]),
         "attn_bwd_delta": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int64, c_int, c_void_p]),
+        "lasp_block_states": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int64, c_int64, c_int, c_void_p]),
+        "lasp_scan": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int, c_int, c_int, c_void_p]),
+        "lasp_exchange": (c_int, [c_void_p, c_void_p, c_int64, c_int, c_int, c_int, c_void_p]),
+        "lasp_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int64, c_int64,
+                             c_int, c_int, c_float, c_void_p]),
+        "lasp_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                             c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int, c_int, c_float, c_void_p]),
         "sca_last_error": (c_char_p, []),
         "sca_read_status": (c_int, [c_void_p, c_void_p]),
         "sca_version": (c_int, []),
@@ -149,6 +158,29 @@ def ring_stage_block(src: int, dst: int, outer: int, S_src: int, row0: int, rows
 def ring_stage_segments(src: int, dst: int, outer: int, S_src: int, seg: sca_segs, row_bytes: int,
                         stream: int) -> int:
     return check(lib().ring_stage_segments(src, dst, outer, S_src, ctypes.byref(seg), row_bytes, stream))
+
+
+def lasp_block_states(a: int, b: int, dtype: int, st: int, BH: int, S: int, D: int, stream: int) -> int:
+    return check(lib().lasp_block_states(a, b, dtype, st, BH, S, D, stream))
+
+
+def lasp_scan(st: int, shard_total: int, BH: int, S: int, D: int, P: int, reverse: int, stream: int) -> int:
+    return check(lib().lasp_scan(st, shard_total, BH, S, D, P, reverse, stream))
+
+
+def lasp_exchange(shard_total: int, shard_in: int, BH: int, D: int, P: int, reverse: int, stream: int) -> int:
+    return check(lib().lasp_exchange(shard_total, shard_in, BH, D, P, reverse, stream))
+
+
+def lasp_fwd(q: int, k: int, v: int, dtype: int, st: int, shard_in: int, o: int, BH: int, S: int, D: int, P: int,
+             scale: float, stream: int) -> int:
+    return check(lib().lasp_fwd(q, k, v, dtype, st, shard_in, o, BH, S, D, P, scale, stream))
+
+
+def lasp_bwd(q: int, k: int, v: int, dout: int, dtype: int, st_fwd: int, in_fwd: int, st_bwd: int, in_bwd: int,
+             dq: int, dk: int, dv: int, BH: int, S: int, D: int, P: int, scale: float, stream: int) -> int:
+    return check(lib().lasp_bwd(q, k, v, dout, dtype, st_fwd, in_fwd, st_bwd, in_bwd, dq, dk, dv, BH, S, D, P,
+                                scale, stream))
 
 
 def attn_bwd_delta(o: int, dout: int, dout_dtype: int, delta: int, rows: int, D: int, stream: int) -> int:

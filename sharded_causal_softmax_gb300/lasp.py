@@ -1,0 +1,119 @@
+"""P virtual shards of causal linear attention on one GPU (linear attention
+sequence parallelism: "Effiziente Parallelisierung linearer
+Aufmerksamkeitssequenzen fuer skalierbare Sprachmodelle" - intermediate
+states exchanged point to point between shards, the right-product trick).
+
+    o_t = scale * sum_{s <= t} (q_t . k_s) v_s
+
+Forward: every shard sums k^T v over its blocks (``lasp_block_states`` then
+``lasp_scan``, which leaves each block the state of the shard's blocks
+before it), the shard totals travel from shard to shard
+(``lasp_exchange``: shard r receives the sum of everything before it from
+shard r-1), and ``lasp_fwd`` combines, per block, the masked left product
+inside the block with the right product of its queries and the state.
+Backward: the same with q^T dO states travelling from later shards to
+earlier ones.  The shards are contiguous (linear attention costs the same
+per row, so no zigzag).  PyTorch supplies device memory and streams only.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import capi
+
+_DT = {torch.bfloat16: capi.SCA_BF16, torch.float32: capi.SCA_F32}
+
+
+def _ptr(t: torch.Tensor) -> int:
+    return t.data_ptr()
+
+
+class ShardedLinearAttention:
+    """Buffers and launch schedule of one LASP configuration; inputs are
+    contiguous [B, H, S, D] tensors of ``dtype``, outputs fp32."""
+
+    def __init__(self, B, H, S, D, P, dtype=torch.bfloat16, scale=None, backward=False, device=None):
+        if dtype not in _DT:
+            raise ValueError(f"dtype {dtype}")
+        if D not in (64, 128):
+            raise ValueError(f"D={D}: only 64 and 128")
+        blk = capi.SCA_LASP_BLOCK
+        if S % (blk * P):
+            raise ValueError(f"S={S} must be a multiple of {blk}*P={blk * P}")
+        self.B, self.H, self.S, self.D, self.P, self.dtype = B, H, S, D, P, dtype
+        self.BH = B * H
+        self.scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+        self.backward_enabled = backward
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        self.device = dev
+        z = lambda *shape: torch.empty(shape, dtype=torch.float32, device=dev)
+        nblk = S // blk
+        self.st_f = z(self.BH, nblk, D, D)       # per block: k^T v of the shard's blocks before it
+        self.tot_f = z(self.BH, P, D, D)
+        self.in_f = z(self.BH, P, D, D)          # what each shard receives from the one before
+        self.o = z(B, H, S, D)
+        if backward:
+            self.st_b = z(self.BH, nblk, D, D)   # per block: q^T dO of the shard's blocks after it
+            self.tot_b = z(self.BH, P, D, D)
+            self.in_b = z(self.BH, P, D, D)
+            self.dq, self.dk, self.dv = z(B, H, S, D), z(B, H, S, D), z(B, H, S, D)
+        self._inputs = None
+        self.kernels = 0
+
+    def forward(self, q, k, v):
+        self._check(q, k, v)
+        self._inputs = (q, k, v)
+        st = torch.cuda.current_stream(self.device).cuda_stream
+        dt, BH, S, D, P = _DT[self.dtype], self.BH, self.S, self.D, self.P
+        capi.lasp_block_states(_ptr(k), _ptr(v), dt, _ptr(self.st_f), BH, S, D, st)
+        capi.lasp_scan(_ptr(self.st_f), _ptr(self.tot_f), BH, S, D, P, 0, st)
+        capi.lasp_exchange(_ptr(self.tot_f), _ptr(self.in_f), BH, D, P, 0, st)
+        capi.lasp_fwd(_ptr(q), _ptr(k), _ptr(v), dt, _ptr(self.st_f), _ptr(self.in_f), _ptr(self.o), BH, S, D, P,
+                      self.scale, st)
+        self.kernels = 4
+        return self.o
+
+    def backward(self, do):
+        if not self.backward_enabled:
+            raise RuntimeError("plan built without backward=True")
+        if self._inputs is None:
+            raise RuntimeError("backward before forward")
+        q, k, v = self._inputs
+        self._check(do)
+        st = torch.cuda.current_stream(self.device).cuda_stream
+        dt, BH, S, D, P = _DT[self.dtype], self.BH, self.S, self.D, self.P
+        capi.lasp_block_states(_ptr(q), _ptr(do), dt, _ptr(self.st_b), BH, S, D, st)
+        capi.lasp_scan(_ptr(self.st_b), _ptr(self.tot_b), BH, S, D, P, 1, st)
+        capi.lasp_exchange(_ptr(self.tot_b), _ptr(self.in_b), BH, D, P, 1, st)
+        capi.lasp_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), dt, _ptr(self.st_f), _ptr(self.in_f), _ptr(self.st_b),
+                      _ptr(self.in_b), _ptr(self.dq), _ptr(self.dk), _ptr(self.dv), BH, S, D, P, self.scale, st)
+        self.kernels = 5
+        return self.dq, self.dk, self.dv
+
+    # ---- the interface the benchmark reads (mirrors ShardedCausalAttention)
+
+    addressing = "contiguous shards"
+
+    def uses_tensor_cores(self, kind: str) -> bool:
+        return False
+
+    def kernel_name(self, kind: str) -> str:
+        return "lasp_fwd_kernel" if kind == "fwd" else "dq_kernel+dkdv_kernel"
+
+    def kernel_sources(self, kind: str):
+        return ["lasp.cu", "common.cuh"]
+
+    def read_status(self) -> int:
+        """Synchronise; the linear-attention kernels never wait, so there is no
+        device status word to read."""
+        torch.cuda.current_stream(self.device).synchronize()
+        return 0
+
+    def _check(self, *ts):
+        for t in ts:
+            if t.dtype != self.dtype or t.device != self.device or not t.is_contiguous() or \
+                    tuple(t.shape) != (self.B, self.H, self.S, self.D):
+                raise ValueError(f"expected contiguous {self.dtype} [{self.B},{self.H},{self.S},{self.D}] "
+                                 f"on {self.device}, got {t.dtype} {tuple(t.shape)} on {t.device}")

@@ -235,3 +235,14 @@ def test_binding_raises_with_message(lib):
     with pytest.raises(capi.ScaError) as e:
         capi.zigzag_permute(A, 2 * A, 4, 100, 256, 4, 0, 0)
     assert "SCA_ERR_ARG" in str(e.value) and "divisible" in str(e.value)
+
+
+def test_lasp_rejects_bad_arguments(lib):
+    bf = capi.SCA_BF16
+    assert lib.lasp_block_states(A, 2 * A, bf, 3 * A, 2, 1024, 96, None) == capi.SCA_ERR_UNSUPPORTED   # D = 96
+    assert lib.lasp_block_states(A, 2 * A, bf, 3 * A, 2, 1000, 128, None) == capi.SCA_ERR_ARG          # S % 64
+    assert lib.lasp_block_states(None, 2 * A, bf, 3 * A, 2, 1024, 128, None) == capi.SCA_ERR_ARG
+    assert lib.lasp_scan(A, 2 * A, 2, 1024, 128, 3, 0, None) == capi.SCA_ERR_ARG                       # 1024 % (64*3)
+    assert lib.lasp_exchange(A, 2 * A, 0, 128, 4, 0, None) == capi.SCA_ERR_ARG                         # BH = 0
+    assert lib.lasp_fwd(A, A, A, 7, A, A, A, 2, 1024, 128, 4, 0.1, None) == capi.SCA_ERR_ARG           # dtype
+    assert lib.lasp_bwd(A, A, A, A, bf, A, A, A, A, A, A, None, 2, 1024, 128, 4, 0.1, None) == capi.SCA_ERR_ARG

@@ -1,0 +1,89 @@
+"""GPU parity of causal linear attention over P contiguous shards passing
+states point to point (LASP) against the fp64 oracle: small cases in full
+(outputs, gradients and the states each shard receives), the 32K training
+workload at full size on sampled rows.  All arithmetic is fp32, and without
+normalisation the outputs grow like sqrt(t): the fp32 bounds (2e-4 max-abs,
+2e-5 mean-abs) apply relative to the largest reference magnitude."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs
+from seeded_inputs import WORKLOADS
+from tests.gpu_util import errors, scale_for
+
+pytestmark = pytest.mark.gpu
+REL = (2e-4, 2e-5)
+
+
+@pytest.fixture(scope="module")
+def sca():
+    import sharded_causal_softmax_gb300 as m
+    from sharded_causal_softmax_gb300 import build
+    build.build()
+    return m
+
+
+def assert_close_rel(name, got, ref, rel=REL):
+    ref = np.asarray(ref, dtype=np.float64)
+    mag = max(1.0, float(np.abs(ref).max()))
+    mx, mn = errors(got, ref)
+    assert mx <= rel[0] * mag and mn <= rel[1] * mag, \
+        f"{name}: max-abs {mx:.3e}, mean-abs {mn:.3e} against magnitude {mag:.3e}"
+
+
+@pytest.mark.parametrize("dtype,B,H,S,D,P", [
+    ("bf16", 1, 2, 1024, 128, 4), ("bf16", 2, 2, 512, 64, 2), ("f32", 1, 2, 256, 64, 1),
+    ("f32", 1, 3, 768, 128, 3), ("bf16", 1, 1, 2048, 128, 8)])
+def test_lasp_small_full_oracle(sca, dtype, B, H, S, D, P):
+    q, k, v, do = seeded_inputs.make_inputs(B, H, S, D, dtype, seed=500 + P + D, with_do=True)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    plan = sca.ShardedLinearAttention(B, H, S, D, P, dtype=tdt, backward=True)
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    o = plan.forward(qd, kd, vd)
+    dq, dk, dv = plan.backward(dod)
+    torch.cuda.synchronize()
+    scale = scale_for(D)
+    assert_close_rel("o", o, oracle.linear_attention(q, k, v, scale))
+    rq, rk, rv = oracle.linear_attention_backward(q, k, v, do, scale)
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        assert_close_rel(name, got, ref)
+    # the states the shards received, both directions, against the oracle's passes
+    in_f, in_b = plan.in_f.cpu().numpy(), plan.in_b.cpu().numpy()
+    for b in range(B):
+        for h in range(H):
+            _, recv_f = oracle.lasp_forward(q[b, h], k[b, h], v[b, h], scale, P, 64)
+            _, recv_b = oracle.lasp_backward(q[b, h], k[b, h], v[b, h], do[b, h], scale, P, 64)
+            for r in range(P):
+                assert_close_rel(f"fwd state b{b} h{h} r{r}", in_f[b * H + h, r], recv_f[r])
+                assert_close_rel(f"bwd state b{b} h{h} r{r}", in_b[b * H + h, r], recv_b[r])
+
+
+def test_lasp_repeat_is_deterministic(sca):
+    B, H, S, D, P = 1, 2, 1024, 128, 4
+    q, k, v, do = (x.cuda() for x in seeded_inputs.make_inputs(B, H, S, D, "bf16", seed=7, with_do=True))
+    plan = sca.ShardedLinearAttention(B, H, S, D, P, backward=True)
+    a = [plan.forward(q, k, v).clone()] + [t.clone() for t in plan.backward(do)]
+    b = [plan.forward(q, k, v)] + list(plan.backward(do))
+    assert all(torch.equal(x, y) for x, y in zip(a, b))
+
+
+def test_lasp_training_step_full_size_sampled(sca):
+    w = WORKLOADS["lasp_s32k"]
+    q, k, v, do = seeded_inputs.workload_inputs(w)
+    plan = sca.ShardedLinearAttention(w.B, w.H, w.S, w.D, w.P, backward=True)
+    o = plan.forward(q.cuda(), k.cuda(), v.cuda())
+    dq, dk, dv = plan.backward(do.cuda())
+    torch.cuda.synchronize()
+    scale = scale_for(w.D)
+    rows = seeded_inputs.sample_rows(w.B, w.H, w.S, w.sample_rows, w.seed).numpy()
+    o_c, dq_c, dk_c, dv_c = o.cpu(), dq.cpu(), dk.cpu(), dv.cpu()
+    for h in range(w.H):
+        r = rows[0, h]
+        assert_close_rel(f"o h{h}", o_c[0, h, r], oracle.linear_attention_rows(q[0, h], k[0, h], v[0, h], scale, r))
+        assert_close_rel(f"dq h{h}", dq_c[0, h, r],
+                         oracle.linear_dq_rows(q[0, h], k[0, h], v[0, h], do[0, h], scale, r))
+        rk, rv = oracle.linear_dkv_rows(q[0, h], k[0, h], v[0, h], do[0, h], scale, r)
+        assert_close_rel(f"dk h{h}", dk_c[0, h, r], rk)
+        assert_close_rel(f"dv h{h}", dv_c[0, h, r], rv)

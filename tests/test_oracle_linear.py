@@ -138,3 +138,16 @@ def test_planted_lasp_mistakes_are_caught(monkeypatch):
     monkeypatch.setattr(oracle, "linear_attention", _linear_strict_mask)
     with pytest.raises(AssertionError):
         test_forward_brute_force(9, 4)
+
+
+def test_row_helpers_match_full_functions():
+    S, D = 130, 5
+    q, k, v, do = (RNG.standard_normal((S, D)) for _ in range(4))
+    rows = np.array([0, 1, 63, 64, 129])
+    o = oracle.linear_attention(q, k, v, 0.4)
+    dq, dk, dv = oracle.linear_attention_backward(q, k, v, do, 0.4)
+    np.testing.assert_allclose(oracle.linear_attention_rows(q, k, v, 0.4, rows), o[rows], atol=1e-11)
+    np.testing.assert_allclose(oracle.linear_dq_rows(q, k, v, do, 0.4, rows), dq[rows], atol=1e-11)
+    rk, rv = oracle.linear_dkv_rows(q, k, v, do, 0.4, rows)
+    np.testing.assert_allclose(rk, dk[rows], atol=1e-11)
+    np.testing.assert_allclose(rv, dv[rows], atol=1e-11)
