@@ -291,6 +291,22 @@ int lasp_bwd(const void* q, const void* k, const void* v, const void* dout, int 
              const float* in_fwd, const float* st_bwd, const float* in_bwd, float* dq, float* dk, float* dv,
              int64_t BH, int64_t S, int D, int P, float scale, void* stream);
 
+/* lasp_fwd_noalloc - the whole LASP forward (lasp_block_states,
+ * lasp_scan, lasp_exchange, lasp_fwd) in one call, with its states in a
+ * fixed device array inside the library instead of caller buffers: the call
+ * allocates nothing.  The pages have no counterpart of this call; it exists
+ * for callers that cannot provide a workspace (e.g. a captured graph that
+ * must not allocate).  Limit: BH * (S / SCA_LASP_BLOCK) * D^2 + 2 * BH * P * D^2
+ * floats of state must fit the 8M-float (32 MB) array, else
+ * SCA_ERR_UNSUPPORTED before anything runs.  The array's device address is
+ * looked up once per device, on the first call: make that first call
+ * outside any stream capture.  All calls share the array: two calls in
+ * flight at once (other streams or threads, same device) race and must be
+ * serialised by the caller.  Nothing in the array must start at zero (every
+ * state is written before it is read).  o: fp32 [BH, S, D], overwritten. */
+int lasp_fwd_noalloc(const void* q, const void* k, const void* v, int dtype, float* o, int64_t BH, int64_t S,
+                     int D, int P, float scale, void* stream);
+
 /* Message of the last non-OK return on the calling thread ("" if none). */
 const char* sca_last_error(void);
 

@@ -32,7 +32,7 @@ SCA_MAX_ITEMS = 32
 
 EXPORTED = ("attn_fwd_shard", "attn_merge_lse", "zigzag_permute", "ring_stage_block", "ring_stage_segments",
             "attn_bwd_shard", "attn_bwd_delta", "lasp_block_states", "lasp_scan", "lasp_exchange", "lasp_fwd",
-            "lasp_bwd", "sca_last_error", "sca_read_status", "sca_version")
+            "lasp_bwd", "lasp_fwd_noalloc", "sca_last_error", "sca_read_status", "sca_version")
 SCA_LASP_BLOCK = 64
 
 
@@ -90,6 +90,8 @@ def _load():
                              c_int, c_int, c_float, c_void_p]),
         "lasp_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
                              c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int, c_int, c_float, c_void_p]),
+        "lasp_fwd_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_int64, c_int64, c_int, c_int,
+                                     c_float, c_void_p]),
         "sca_last_error": (c_char_p, []),
         "sca_read_status": (c_int, [c_void_p, c_void_p]),
         "sca_version": (c_int, []),
@@ -181,6 +183,11 @@ def lasp_bwd(q: int, k: int, v: int, dout: int, dtype: int, st_fwd: int, in_fwd:
              dq: int, dk: int, dv: int, BH: int, S: int, D: int, P: int, scale: float, stream: int) -> int:
     return check(lib().lasp_bwd(q, k, v, dout, dtype, st_fwd, in_fwd, st_bwd, in_bwd, dq, dk, dv, BH, S, D, P,
                                 scale, stream))
+
+
+def lasp_fwd_noalloc(q: int, k: int, v: int, dtype: int, o: int, BH: int, S: int, D: int, P: int, scale: float,
+                     stream: int) -> int:
+    return check(lib().lasp_fwd_noalloc(q, k, v, dtype, o, BH, S, D, P, scale, stream))
 
 
 def attn_bwd_delta(o: int, dout: int, dout_dtype: int, delta: int, rows: int, D: int, stream: int) -> int:

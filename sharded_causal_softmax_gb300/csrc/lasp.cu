@@ -21,6 +21,8 @@
 // stride (cols + 1), and a thread (ti, tj) of the 16 x 16 grid owns rows
 // ti*RM .. ti*RM+RM-1 and columns tj, tj+16, ...: row-wise and column-wise
 // operand reads are then free of bank conflicts.
+#include <mutex>
+
 #include "common.cuh"
 #include "host_common.h"
 
@@ -269,6 +271,29 @@ static cudaError_t allow_smem(K kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
+// Fixed state workspace of lasp_fwd_noalloc: 8M floats (32 MB) per device,
+// part of the module image, so that call allocates nothing.
+constexpr int64_t kScratchFloats = int64_t(8) << 20;
+__device__ __align__(256) float g_scratch[kScratchFloats];
+
+// Device address of g_scratch on the current device, looked up once per
+// device (the first call must not be inside a stream capture).
+static float* scratch_ptr(cudaError_t* err) {
+  static std::once_flag once[64];
+  static float* ptr[64];
+  static cudaError_t res[64];
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  std::call_once(once[dev & 63], [&] {
+    void* p = nullptr;
+    res[dev & 63] = cudaGetSymbolAddress(&p, g_scratch);
+    ptr[dev & 63] = static_cast<float*>(p);
+  });
+  *err = res[dev & 63];
+  return *err == cudaSuccess ? ptr[dev & 63] : nullptr;
+}
+
 }  // namespace lasp
 }  // namespace sca
 
@@ -385,4 +410,26 @@ extern "C" int lasp_bwd(const void* q, const void* k, const void* v, const void*
 #undef SCA_BWD
   if (e != cudaSuccess) return cuda_status(e, "lasp_bwd");
   return cuda_status(cudaGetLastError(), "lasp_bwd launch");
+}
+
+extern "C" int lasp_fwd_noalloc(const void* q, const void* k, const void* v, int dtype, float* o, int64_t BH,
+                                int64_t S, int D, int P, float scale, void* stream) {
+  int rc;
+  if ((rc = lasp_check(BH, S, D, P, dtype, "lasp_fwd_noalloc")) != SCA_OK) return rc;
+  SCA_REQUIRE(q && k && v && o, SCA_ERR_ARG, "lasp_fwd_noalloc: NULL pointer");
+  const int64_t nblk = S / kBlk, DD = static_cast<int64_t>(D) * D;
+  const int64_t need = BH * nblk * DD + 2 * BH * P * DD;   // block states, shard totals, shard inputs
+  SCA_REQUIRE(need <= kScratchFloats, SCA_ERR_UNSUPPORTED,
+              "lasp_fwd_noalloc: needs %lld floats of state, the fixed workspace holds %lld",
+              static_cast<long long>(need), static_cast<long long>(kScratchFloats));
+  cudaError_t e;
+  float* st = scratch_ptr(&e);
+  if (!st) return cuda_status(e, "lasp_fwd_noalloc workspace address");
+  float* tot = st + BH * nblk * DD;
+  float* in = tot + BH * P * DD;
+  // every state is written before it is read: nothing needs clearing
+  if ((rc = lasp_block_states(k, v, dtype, st, BH, S, D, stream)) != SCA_OK) return rc;
+  if ((rc = lasp_scan(st, tot, BH, S, D, P, 0, stream)) != SCA_OK) return rc;
+  if ((rc = lasp_exchange(tot, in, BH, D, P, 0, stream)) != SCA_OK) return rc;
+  return lasp_fwd(q, k, v, dtype, st, in, o, BH, S, D, P, scale, stream);
 }
