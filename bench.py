@@ -381,7 +381,13 @@ def run_gpu(args):
     # (P per direction on the ring, one when fused)
     launch_flops = flops(w, fwd=(kind == "fwd"), bwd=(kind == "bwd")) * args.steps / n
     tc = plan.uses_tensor_cores(kind)
-    if tc:
+    bound_of = getattr(plan, "roofline_bound", None)
+    if bound_of is not None and bound_of(kind) == "hbm":
+        # bytes-bound kernels: algorithmic bytes of one call over its time
+        peak = peaks.get("hbm_gbs", 6800.0)
+        bound, unit = "hbm", "GB/s"
+        peak_note = f"{peak_src} copy bandwidth"
+    elif tc:
         peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
         bound, unit = "tensor", "TFLOP/s"
         peak_note = f"{peak_src} bf16 sustained (kernel timed inside a long step)"
@@ -391,13 +397,20 @@ def run_gpu(args):
         peak = 152 * 128 * 2 * mhz * 1e6 / 1e12
         bound, unit = "alu", "TFLOP/s"
         peak_note = "derived fp32 FMA peak (152 SM x 128 FMA/clk x 2 x max SM clock)"
-    achieved = launch_flops / avg_s / 1e12
+    if bound == "hbm":
+        launch_bytes = plan.algorithmic_bytes(kind)
+        achieved = launch_bytes / avg_s / 1e9
+    else:
+        achieved = launch_flops / avg_s / 1e12
     src = plan.kernel_sources(kind)
     traffic = measured_traffic(plan.kernel_name(kind), src, w.name)
     roofline = {"kernel": plan.kernel_name(kind), "bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1),
                 "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": peak_note, "launches_timed": n, "avg_launch_ms": round(avg_s * 1e3, 4),
                 "flops_per_launch": launch_flops}
+    if bound == "hbm":
+        roofline["bytes_per_launch"] = launch_bytes
+        roofline["tflops"] = round(launch_flops / avg_s / 1e12, 2)
     permute_alone = not hbm["zigzag_permute_kernel"] and w.layout == "zigzag"
     if permute_alone:
         # the step addresses rows by position and runs no permute: time the

@@ -247,25 +247,39 @@ int attn_bwd_delta(const float* o, const void* dout, int dout_dtype, float* delt
  * ("Effiziente Parallelisierung linearer Aufmerksamkeitssequenzen fuer
  * skalierbare Sprachmodelle", the LASP summary; it prints no formula, this
  * is the plain reading).  Tensors q, k, v, dout are row-contiguous
- * [BH, S, D] (BH = batch x heads) of dtype bf16 or fp32; o, dq, dk, dv are
- * fp32 [BH, S, D], overwritten.  Rows go in blocks of SCA_LASP_BLOCK; S must
- * be a multiple of SCA_LASP_BLOCK * P.  States are fp32 D x D, row index the
- * first factor's column: per block st [BH, S/SCA_LASP_BLOCK, D, D], per
- * shard [BH, P, D, D]; the caller owns every buffer (no allocation).  All
- * arithmetic is fp32 on the CUDA cores.  Errors: SCA_ERR_ARG (NULL
- * pointers, sizes), SCA_ERR_UNSUPPORTED (D not 64 or 128), SCA_ERR_CUDA. */
-#define SCA_LASP_BLOCK 64
+ * [BH, S, D] (BH = batch x heads, at most 65535) of dtype bf16 or fp32,
+ * 16-byte aligned; o, dq, dk, dv are fp32 [BH, S, D], overwritten.
+ *
+ * Rows go in blocks of `block` rows, which also selects the kernels:
+ *   SCA_LASP_BLOCK_F32 (64): fp32 arithmetic on the CUDA cores; bf16 or
+ *     fp32 inputs, D 64 or 128;
+ *   SCA_LASP_BLOCK_TC (128): tcgen05 tensor cores with fp32 accumulation;
+ *     bf16 inputs and D = 128 only (else SCA_ERR_UNSUPPORTED).  The fp32
+ *     operands (states, masked block products) are split into two bf16
+ *     parts and multiplied twice, keeping about fp32 accuracy.
+ * S must be a multiple of block * P, and every call of one pass uses the
+ * same block.  States are fp32 D x D, row index the first factor's
+ * column: per block st [BH, S/block, D, D], per shard [BH, P, D, D]; the
+ * caller owns every buffer (no allocation).  `dev_status` (may be NULL) is
+ * the device status word the tensor-core kernels report a timed-out wait
+ * in (SCA_ERR_TIMEOUT); the CUDA-core kernels never wait.  Errors:
+ * SCA_ERR_ARG (NULL pointers, sizes, block), SCA_ERR_UNSUPPORTED (D not 64
+ * or 128, block 128 without bf16 and D = 128), SCA_ERR_ALIGN (an input the
+ * tensor-core path cannot address by TMA), SCA_ERR_CUDA. */
+#define SCA_LASP_BLOCK_F32 64
+#define SCA_LASP_BLOCK_TC 128
 
 /* lasp_block_states - st[bh][j] = A_j^T B_j over the rows of block j:
  * (A, B) = (k, v) for the forward, (q, dout) for the backward. */
-int lasp_block_states(const void* a, const void* b, int dtype, float* st, int64_t BH, int64_t S, int D,
-                      void* stream);
+int lasp_block_states(const void* a, const void* b, int dtype, float* st, int64_t BH, int64_t S, int D, int block,
+                      int* dev_status, void* stream);
 
 /* lasp_scan - within each of the P shards (contiguous runs of blocks),
  * replaces st[bh][j] by the sum over the shard's blocks before j
  * (reverse = 0) or after j (reverse = 1), in place, and writes the sum over
  * all the shard's blocks to shard_total[bh][r]. */
-int lasp_scan(float* st, float* shard_total, int64_t BH, int64_t S, int D, int P, int reverse, void* stream);
+int lasp_scan(float* st, float* shard_total, int64_t BH, int64_t S, int D, int P, int block, int reverse,
+              void* stream);
 
 /* lasp_exchange - the point-to-point pass of shard states, one hop at a
  * time along the ring: shard_in[bh][r] = sum of shard_total[bh][s] over
@@ -279,7 +293,7 @@ int lasp_exchange(const float* shard_total, float* shard_in, int64_t BH, int D, 
  * with st, shard_in from lasp_block_states(k, v) / lasp_scan(reverse = 0) /
  * lasp_exchange(reverse = 0). */
 int lasp_fwd(const void* q, const void* k, const void* v, int dtype, const float* st, const float* shard_in,
-             float* o, int64_t BH, int64_t S, int D, int P, float scale, void* stream);
+             float* o, int64_t BH, int64_t S, int D, int P, int block, float scale, int* dev_status, void* stream);
 
 /* lasp_bwd - for every block j of shard r, with F = st_fwd[j] + in_fwd[r]
  * (the forward states) and G = st_bwd[j] + in_bwd[r] (from
@@ -289,14 +303,15 @@ int lasp_fwd(const void* q, const void* k, const void* v, int dtype, const float
  *   dv_j = scale * (k_j G + tril(q_j k_j^T)^T dout_j) */
 int lasp_bwd(const void* q, const void* k, const void* v, const void* dout, int dtype, const float* st_fwd,
              const float* in_fwd, const float* st_bwd, const float* in_bwd, float* dq, float* dk, float* dv,
-             int64_t BH, int64_t S, int D, int P, float scale, void* stream);
+             int64_t BH, int64_t S, int D, int P, int block, float scale, int* dev_status, void* stream);
 
 /* lasp_fwd_noalloc - the whole LASP forward (lasp_block_states,
- * lasp_scan, lasp_exchange, lasp_fwd) in one call, with its states in a
+ * lasp_scan, lasp_exchange, lasp_fwd, blocks of SCA_LASP_BLOCK_F32 rows on
+ * the CUDA cores) in one call, with its states in a
  * fixed device array inside the library instead of caller buffers: the call
  * allocates nothing.  The pages have no counterpart of this call; it exists
  * for callers that cannot provide a workspace (e.g. a captured graph that
- * must not allocate).  Limit: BH * (S / SCA_LASP_BLOCK) * D^2 + 2 * BH * P * D^2
+ * must not allocate).  Limit: BH * (S / 64) * D^2 + 2 * BH * P * D^2
  * floats of state must fit the 8M-float (32 MB) array, else
  * SCA_ERR_UNSUPPORTED before anything runs.  The array's device address is
  * looked up once per device, on the first call: make that first call

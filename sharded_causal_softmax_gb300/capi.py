@@ -33,7 +33,8 @@ SCA_MAX_ITEMS = 32
 EXPORTED = ("attn_fwd_shard", "attn_merge_lse", "zigzag_permute", "ring_stage_block", "ring_stage_segments",
             "attn_bwd_shard", "attn_bwd_delta", "lasp_block_states", "lasp_scan", "lasp_exchange", "lasp_fwd",
             "lasp_bwd", "lasp_fwd_noalloc", "sca_last_error", "sca_read_status", "sca_version")
-SCA_LASP_BLOCK = 64
+SCA_LASP_BLOCK_F32 = 64    # blocks of the fp32 CUDA-core kernels
+SCA_LASP_BLOCK_TC = 128    # blocks of the tensor-core kernels (bf16, D = 128)
 
 
 class ScaError(RuntimeError):
@@ -83,13 +84,15 @@ def _load():
         "ring_stage_segments": (c_int, [c_void_p, c_void_p, c_int64, c_int64, POINTER(sca_segs), c_int64, c_void_p]),
         "attn_bwd_shard": (c_int, [POINTER(sca_bwd_item), c_int, POINTER(sca_attn_dims), c_void_p, c_void_p]),
         "attn_bwd_delta": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int64, c_int, c_void_p]),
-        "lasp_block_states": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int64, c_int64, c_int, c_void_p]),
-        "lasp_scan": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int, c_int, c_int, c_void_p]),
+        "lasp_block_states": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int64, c_int64, c_int, c_int, c_void_p,
+                                      c_void_p]),
+        "lasp_scan": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int, c_int, c_int, c_int, c_void_p]),
         "lasp_exchange": (c_int, [c_void_p, c_void_p, c_int64, c_int, c_int, c_int, c_void_p]),
         "lasp_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int64, c_int64,
-                             c_int, c_int, c_float, c_void_p]),
+                             c_int, c_int, c_int, c_float, c_void_p, c_void_p]),
         "lasp_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
-                             c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int, c_int, c_float, c_void_p]),
+                             c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int, c_int, c_int, c_float, c_void_p,
+                             c_void_p]),
         "lasp_fwd_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_int64, c_int64, c_int, c_int,
                                      c_float, c_void_p]),
         "sca_last_error": (c_char_p, []),
@@ -162,12 +165,14 @@ def ring_stage_segments(src: int, dst: int, outer: int, S_src: int, seg: sca_seg
     return check(lib().ring_stage_segments(src, dst, outer, S_src, ctypes.byref(seg), row_bytes, stream))
 
 
-def lasp_block_states(a: int, b: int, dtype: int, st: int, BH: int, S: int, D: int, stream: int) -> int:
-    return check(lib().lasp_block_states(a, b, dtype, st, BH, S, D, stream))
+def lasp_block_states(a: int, b: int, dtype: int, st: int, BH: int, S: int, D: int, block: int, dev_status: int,
+                      stream: int) -> int:
+    return check(lib().lasp_block_states(a, b, dtype, st, BH, S, D, block, dev_status, stream))
 
 
-def lasp_scan(st: int, shard_total: int, BH: int, S: int, D: int, P: int, reverse: int, stream: int) -> int:
-    return check(lib().lasp_scan(st, shard_total, BH, S, D, P, reverse, stream))
+def lasp_scan(st: int, shard_total: int, BH: int, S: int, D: int, P: int, block: int, reverse: int,
+              stream: int) -> int:
+    return check(lib().lasp_scan(st, shard_total, BH, S, D, P, block, reverse, stream))
 
 
 def lasp_exchange(shard_total: int, shard_in: int, BH: int, D: int, P: int, reverse: int, stream: int) -> int:
@@ -175,14 +180,15 @@ def lasp_exchange(shard_total: int, shard_in: int, BH: int, D: int, P: int, reve
 
 
 def lasp_fwd(q: int, k: int, v: int, dtype: int, st: int, shard_in: int, o: int, BH: int, S: int, D: int, P: int,
-             scale: float, stream: int) -> int:
-    return check(lib().lasp_fwd(q, k, v, dtype, st, shard_in, o, BH, S, D, P, scale, stream))
+             block: int, scale: float, dev_status: int, stream: int) -> int:
+    return check(lib().lasp_fwd(q, k, v, dtype, st, shard_in, o, BH, S, D, P, block, scale, dev_status, stream))
 
 
 def lasp_bwd(q: int, k: int, v: int, dout: int, dtype: int, st_fwd: int, in_fwd: int, st_bwd: int, in_bwd: int,
-             dq: int, dk: int, dv: int, BH: int, S: int, D: int, P: int, scale: float, stream: int) -> int:
+             dq: int, dk: int, dv: int, BH: int, S: int, D: int, P: int, block: int, scale: float, dev_status: int,
+             stream: int) -> int:
     return check(lib().lasp_bwd(q, k, v, dout, dtype, st_fwd, in_fwd, st_bwd, in_bwd, dq, dk, dv, BH, S, D, P,
-                                scale, stream))
+                                block, scale, dev_status, stream))
 
 
 def lasp_fwd_noalloc(q: int, k: int, v: int, dtype: int, o: int, BH: int, S: int, D: int, P: int, scale: float,

@@ -25,6 +25,7 @@
 
 #include "common.cuh"
 #include "host_common.h"
+#include "lasp_tc.h"
 
 namespace sca {
 namespace lasp {
@@ -136,19 +137,32 @@ __global__ void __launch_bounds__(kThreads) states_kernel(const T* a, const T* b
 // Exclusive prefix (reverse: suffix) of the states over each shard's blocks,
 // in place; the shard's total into tot[bh][r].
 __global__ void scan_kernel(float* st, float* tot, int64_t nblk, int DD, int P, int reverse) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= DD) return;
+  const int e4 = blockIdx.x * blockDim.x + threadIdx.x;   // four consecutive entries per thread
+  const int DD4 = DD / 4;
+  if (e4 >= DD4) return;
   const int bh = blockIdx.y, r = blockIdx.z;
   const int64_t nb = nblk / P;
-  float* base = st + (static_cast<int64_t>(bh) * nblk + r * nb) * DD + e;
-  float run = 0.f;
-  for (int64_t i = 0; i < nb; ++i) {
-    const int64_t j = reverse ? nb - 1 - i : i;
-    const float v = base[j * DD];
-    base[j * DD] = run;
-    run += v;
+  float4* base = reinterpret_cast<float4*>(st + (static_cast<int64_t>(bh) * nblk + r * nb) * DD) + e4;
+  float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+  // eight independent 16-byte loads in flight, then their exclusive prefix
+  for (int64_t i0 = 0; i0 < nb; i0 += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t i = i0 + u, j = reverse ? nb - 1 - i : i;
+      v[u] = i < nb ? base[j * DD4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t i = i0 + u, j = reverse ? nb - 1 - i : i;
+      if (i < nb) base[j * DD4] = run;
+      run.x += v[u].x;
+      run.y += v[u].y;
+      run.z += v[u].z;
+      run.w += v[u].w;
+    }
   }
-  tot[(static_cast<int64_t>(bh) * P + r) * DD + e] = run;
+  reinterpret_cast<float4*>(tot + (static_cast<int64_t>(bh) * P + r) * DD)[e4] = run;
 }
 
 // The pass of states along the ring of shards, one hop at a time.
@@ -300,12 +314,18 @@ static float* scratch_ptr(cudaError_t* err) {
 using namespace sca;
 using namespace sca::lasp;
 
-static int lasp_check(int64_t BH, int64_t S, int D, int P, int dtype, const char* who) {
+// block: 64 = the fp32 CUDA-core kernels below, 128 = the tensor-core
+// kernels of lasp_tc.cu (bf16, D = 128)
+static int lasp_check(int64_t BH, int64_t S, int D, int P, int dtype, int block, const char* who) {
   SCA_REQUIRE(BH >= 1 && BH <= 65535, SCA_ERR_ARG, "%s: BH=%lld outside [1, 65535]", who, static_cast<long long>(BH));
   SCA_REQUIRE(D == 64 || D == 128, SCA_ERR_UNSUPPORTED, "%s: D=%d: only 64 and 128", who, D);
-  SCA_REQUIRE(P >= 1 && S > 0 && S % (static_cast<int64_t>(kBlk) * P) == 0, SCA_ERR_ARG,
-              "%s: S=%lld must be a positive multiple of %d*P (P=%d)", who, static_cast<long long>(S), kBlk, P);
   SCA_REQUIRE(dtype == SCA_BF16 || dtype == SCA_F32, SCA_ERR_ARG, "%s: dtype=%d unknown", who, dtype);
+  SCA_REQUIRE(block == kBlk || block == kLaspTcBlock, SCA_ERR_ARG, "%s: block=%d: only %d or %d", who, block, kBlk,
+              kLaspTcBlock);
+  SCA_REQUIRE(block == kBlk || (dtype == SCA_BF16 && D == 128), SCA_ERR_UNSUPPORTED,
+              "%s: blocks of %d rows (tensor cores) need bf16 inputs and D = 128", who, kLaspTcBlock);
+  SCA_REQUIRE(P >= 1 && S > 0 && S % (static_cast<int64_t>(block) * P) == 0, SCA_ERR_ARG,
+              "%s: S=%lld must be a positive multiple of %d*P (P=%d)", who, static_cast<long long>(S), block, P);
   return SCA_OK;
 }
 
@@ -318,10 +338,11 @@ static int lasp_check(int64_t BH, int64_t S, int D, int P, int dtype, const char
   } while (0)
 
 extern "C" int lasp_block_states(const void* a, const void* b, int dtype, float* st, int64_t BH, int64_t S, int D,
-                                 void* stream) {
+                                 int block, int* dev_status, void* stream) {
   int rc;
-  if ((rc = lasp_check(BH, S, D, 1, dtype, "lasp_block_states")) != SCA_OK) return rc;
+  if ((rc = lasp_check(BH, S, D, 1, dtype, block, "lasp_block_states")) != SCA_OK) return rc;
   SCA_REQUIRE(a && b && st, SCA_ERR_ARG, "lasp_block_states: NULL pointer");
+  if (block == kLaspTcBlock) return lasp_tc_states(a, b, st, BH, S, dev_status, as_stream(stream));
   const dim3 grid(static_cast<unsigned>(S / kBlk), static_cast<unsigned>(BH));
   cudaError_t e = cudaSuccess;
 #define SCA_STATES(DD, TT)                                                                               \
@@ -338,14 +359,16 @@ extern "C" int lasp_block_states(const void* a, const void* b, int dtype, float*
   return cuda_status(cudaGetLastError(), "lasp_block_states launch");
 }
 
-extern "C" int lasp_scan(float* st, float* shard_total, int64_t BH, int64_t S, int D, int P, int reverse,
+extern "C" int lasp_scan(float* st, float* shard_total, int64_t BH, int64_t S, int D, int P, int block, int reverse,
                          void* stream) {
   int rc;
-  if ((rc = lasp_check(BH, S, D, P, SCA_F32, "lasp_scan")) != SCA_OK) return rc;
+  if ((rc = lasp_check(BH, S, D, P, block == kBlk ? SCA_F32 : SCA_BF16, block, "lasp_scan")) != SCA_OK) return rc;
   SCA_REQUIRE(st && shard_total, SCA_ERR_ARG, "lasp_scan: NULL pointer");
+  SCA_REQUIRE(reinterpret_cast<uintptr_t>(st) % 16 == 0 && reinterpret_cast<uintptr_t>(shard_total) % 16 == 0,
+              SCA_ERR_ALIGN, "lasp_scan: st and shard_total must be 16-byte aligned");
   const int DD = D * D;
-  const dim3 grid((DD + 255) / 256, static_cast<unsigned>(BH), static_cast<unsigned>(P));
-  scan_kernel<<<grid, 256, 0, as_stream(stream)>>>(st, shard_total, S / kBlk, DD, P, reverse ? 1 : 0);
+  const dim3 grid((DD / 4 + 255) / 256, static_cast<unsigned>(BH), static_cast<unsigned>(P));
+  scan_kernel<<<grid, 256, 0, as_stream(stream)>>>(st, shard_total, S / block, DD, P, reverse ? 1 : 0);
   return cuda_status(cudaGetLastError(), "lasp_scan launch");
 }
 
@@ -361,11 +384,13 @@ extern "C" int lasp_exchange(const float* shard_total, float* shard_in, int64_t 
 }
 
 extern "C" int lasp_fwd(const void* q, const void* k, const void* v, int dtype, const float* st,
-                        const float* shard_in, float* o, int64_t BH, int64_t S, int D, int P, float scale,
-                        void* stream) {
+                        const float* shard_in, float* o, int64_t BH, int64_t S, int D, int P, int block, float scale,
+                        int* dev_status, void* stream) {
   int rc;
-  if ((rc = lasp_check(BH, S, D, P, dtype, "lasp_fwd")) != SCA_OK) return rc;
+  if ((rc = lasp_check(BH, S, D, P, dtype, block, "lasp_fwd")) != SCA_OK) return rc;
   SCA_REQUIRE(q && k && v && st && shard_in && o, SCA_ERR_ARG, "lasp_fwd: NULL pointer");
+  if (block == kLaspTcBlock)
+    return lasp_tc_fwd(q, k, v, st, shard_in, o, BH, S, P, scale, dev_status, as_stream(stream));
   const dim3 grid(static_cast<unsigned>(S / kBlk), static_cast<unsigned>(BH));
   cudaError_t e = cudaSuccess;
 #define SCA_FWD(DD, TT)                                                                                    \
@@ -385,11 +410,15 @@ extern "C" int lasp_fwd(const void* q, const void* k, const void* v, int dtype, 
 
 extern "C" int lasp_bwd(const void* q, const void* k, const void* v, const void* dout, int dtype,
                         const float* st_fwd, const float* in_fwd, const float* st_bwd, const float* in_bwd, float* dq,
-                        float* dk, float* dv, int64_t BH, int64_t S, int D, int P, float scale, void* stream) {
+                        float* dk, float* dv, int64_t BH, int64_t S, int D, int P, int block, float scale,
+                        int* dev_status, void* stream) {
   int rc;
-  if ((rc = lasp_check(BH, S, D, P, dtype, "lasp_bwd")) != SCA_OK) return rc;
+  if ((rc = lasp_check(BH, S, D, P, dtype, block, "lasp_bwd")) != SCA_OK) return rc;
   SCA_REQUIRE(q && k && v && dout && st_fwd && in_fwd && st_bwd && in_bwd && dq && dk && dv, SCA_ERR_ARG,
               "lasp_bwd: NULL pointer");
+  if (block == kLaspTcBlock)
+    return lasp_tc_bwd(q, k, v, dout, st_fwd, in_fwd, st_bwd, in_bwd, dq, dk, dv, BH, S, P, scale, dev_status,
+                       as_stream(stream));
   const dim3 grid(static_cast<unsigned>(S / kBlk), static_cast<unsigned>(BH));
   cudaError_t e = cudaSuccess;
 #define SCA_BWD(DD, TT)                                                                                     \
@@ -415,7 +444,7 @@ extern "C" int lasp_bwd(const void* q, const void* k, const void* v, const void*
 extern "C" int lasp_fwd_noalloc(const void* q, const void* k, const void* v, int dtype, float* o, int64_t BH,
                                 int64_t S, int D, int P, float scale, void* stream) {
   int rc;
-  if ((rc = lasp_check(BH, S, D, P, dtype, "lasp_fwd_noalloc")) != SCA_OK) return rc;
+  if ((rc = lasp_check(BH, S, D, P, dtype, kBlk, "lasp_fwd_noalloc")) != SCA_OK) return rc;
   SCA_REQUIRE(q && k && v && o, SCA_ERR_ARG, "lasp_fwd_noalloc: NULL pointer");
   const int64_t nblk = S / kBlk, DD = static_cast<int64_t>(D) * D;
   const int64_t need = BH * nblk * DD + 2 * BH * P * DD;   // block states, shard totals, shard inputs
@@ -428,8 +457,8 @@ extern "C" int lasp_fwd_noalloc(const void* q, const void* k, const void* v, int
   float* tot = st + BH * nblk * DD;
   float* in = tot + BH * P * DD;
   // every state is written before it is read: nothing needs clearing
-  if ((rc = lasp_block_states(k, v, dtype, st, BH, S, D, stream)) != SCA_OK) return rc;
-  if ((rc = lasp_scan(st, tot, BH, S, D, P, 0, stream)) != SCA_OK) return rc;
+  if ((rc = lasp_block_states(k, v, dtype, st, BH, S, D, kBlk, nullptr, stream)) != SCA_OK) return rc;
+  if ((rc = lasp_scan(st, tot, BH, S, D, P, kBlk, 0, stream)) != SCA_OK) return rc;
   if ((rc = lasp_exchange(tot, in, BH, D, P, 0, stream)) != SCA_OK) return rc;
-  return lasp_fwd(q, k, v, dtype, st, in, o, BH, S, D, P, scale, stream);
+  return lasp_fwd(q, k, v, dtype, st, in, o, BH, S, D, P, kBlk, scale, nullptr, stream);
 }

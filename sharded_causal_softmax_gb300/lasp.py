@@ -13,7 +13,10 @@ shard r-1), and ``lasp_fwd`` combines, per block, the masked left product
 inside the block with the right product of its queries and the state.
 Backward: the same with q^T dO states travelling from later shards to
 earlier ones.  The shards are contiguous (linear attention costs the same
-per row, so no zigzag).  PyTorch supplies device memory and streams only.
+per row, so no zigzag).  bf16 inputs with D = 128 run on the tensor-core
+kernels (blocks of 128 rows); fp32 inputs and D = 64 on the fp32 CUDA-core
+kernels (blocks of 64 rows).  PyTorch supplies device memory and streams
+only.
 """
 from __future__ import annotations
 
@@ -34,12 +37,19 @@ class ShardedLinearAttention:
     """Buffers and launch schedule of one LASP configuration; inputs are
     contiguous [B, H, S, D] tensors of ``dtype``, outputs fp32."""
 
-    def __init__(self, B, H, S, D, P, dtype=torch.bfloat16, scale=None, backward=False, device=None):
+    def __init__(self, B, H, S, D, P, dtype=torch.bfloat16, scale=None, backward=False, device=None,
+                 block=None):
         if dtype not in _DT:
             raise ValueError(f"dtype {dtype}")
         if D not in (64, 128):
             raise ValueError(f"D={D}: only 64 and 128")
-        blk = capi.SCA_LASP_BLOCK
+        tc_ok = dtype == torch.bfloat16 and D == 128
+        if block is None:
+            block = capi.SCA_LASP_BLOCK_TC if tc_ok else capi.SCA_LASP_BLOCK_F32
+        if block not in (capi.SCA_LASP_BLOCK_F32, capi.SCA_LASP_BLOCK_TC) or \
+                (block == capi.SCA_LASP_BLOCK_TC and not tc_ok):
+            raise ValueError(f"block={block}: 64, or 128 for bf16 inputs with D = 128")
+        blk = self.block = block
         if S % (blk * P):
             raise ValueError(f"S={S} must be a multiple of {blk}*P={blk * P}")
         self.B, self.H, self.S, self.D, self.P, self.dtype = B, H, S, D, P, dtype
@@ -54,6 +64,7 @@ class ShardedLinearAttention:
         self.tot_f = z(self.BH, P, D, D)
         self.in_f = z(self.BH, P, D, D)          # what each shard receives from the one before
         self.o = z(B, H, S, D)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         if backward:
             self.st_b = z(self.BH, nblk, D, D)   # per block: q^T dO of the shard's blocks after it
             self.tot_b = z(self.BH, P, D, D)
@@ -67,11 +78,12 @@ class ShardedLinearAttention:
         self._inputs = (q, k, v)
         st = torch.cuda.current_stream(self.device).cuda_stream
         dt, BH, S, D, P = _DT[self.dtype], self.BH, self.S, self.D, self.P
-        capi.lasp_block_states(_ptr(k), _ptr(v), dt, _ptr(self.st_f), BH, S, D, st)
-        capi.lasp_scan(_ptr(self.st_f), _ptr(self.tot_f), BH, S, D, P, 0, st)
+        blk, sp = self.block, _ptr(self.status)
+        capi.lasp_block_states(_ptr(k), _ptr(v), dt, _ptr(self.st_f), BH, S, D, blk, sp, st)
+        capi.lasp_scan(_ptr(self.st_f), _ptr(self.tot_f), BH, S, D, P, blk, 0, st)
         capi.lasp_exchange(_ptr(self.tot_f), _ptr(self.in_f), BH, D, P, 0, st)
         capi.lasp_fwd(_ptr(q), _ptr(k), _ptr(v), dt, _ptr(self.st_f), _ptr(self.in_f), _ptr(self.o), BH, S, D, P,
-                      self.scale, st)
+                      blk, self.scale, sp, st)
         self.kernels = 4
         return self.o
 
@@ -84,32 +96,56 @@ class ShardedLinearAttention:
         self._check(do)
         st = torch.cuda.current_stream(self.device).cuda_stream
         dt, BH, S, D, P = _DT[self.dtype], self.BH, self.S, self.D, self.P
-        capi.lasp_block_states(_ptr(q), _ptr(do), dt, _ptr(self.st_b), BH, S, D, st)
-        capi.lasp_scan(_ptr(self.st_b), _ptr(self.tot_b), BH, S, D, P, 1, st)
+        blk, sp = self.block, _ptr(self.status)
+        capi.lasp_block_states(_ptr(q), _ptr(do), dt, _ptr(self.st_b), BH, S, D, blk, sp, st)
+        capi.lasp_scan(_ptr(self.st_b), _ptr(self.tot_b), BH, S, D, P, blk, 1, st)
         capi.lasp_exchange(_ptr(self.tot_b), _ptr(self.in_b), BH, D, P, 1, st)
         capi.lasp_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), dt, _ptr(self.st_f), _ptr(self.in_f), _ptr(self.st_b),
-                      _ptr(self.in_b), _ptr(self.dq), _ptr(self.dk), _ptr(self.dv), BH, S, D, P, self.scale, st)
-        self.kernels = 5
+                      _ptr(self.in_b), _ptr(self.dq), _ptr(self.dk), _ptr(self.dv), BH, S, D, P, blk, self.scale,
+                      sp, st)
+        self.kernels = 6 if blk == capi.SCA_LASP_BLOCK_TC else 5
         return self.dq, self.dk, self.dv
 
     # ---- the interface the benchmark reads (mirrors ShardedCausalAttention)
 
-    addressing = "contiguous shards"
+    @property
+    def addressing(self):
+        return "contiguous shards, blocks of %d rows" % self.block
+
+    def roofline_bound(self, kind: str) -> str:
+        """The tensor-core kernels move ~224 (forward) and ~448 (backward)
+        bytes per 128-row block for ~94 FLOP of tcgen05 work per byte, under
+        the bf16 ridge (~290 FLOP/B): bytes bound.  The CUDA-core kernels are
+        bound by fp32 FMA issue."""
+        return "hbm" if self.block == capi.SCA_LASP_BLOCK_TC else "alu"
+
+    def algorithmic_bytes(self, kind: str) -> int:
+        """Bytes one lasp_fwd / lasp_bwd call must move: per block its input
+        tiles (bf16), its fp32 D x D state(s) and its fp32 output tiles (the
+        per-shard inputs are shared by a shard's blocks and stay in L2)."""
+        nb = self.BH * (self.S // self.block)
+        rows, D = self.block, self.D
+        if kind == "fwd":
+            return nb * (3 * rows * D * 2 + D * D * 4 + rows * D * 4)
+        return nb * (4 * rows * D * 2 + 2 * D * D * 4 + 3 * rows * D * 4)
 
     def uses_tensor_cores(self, kind: str) -> bool:
-        return False
+        return self.block == capi.SCA_LASP_BLOCK_TC
 
     def kernel_name(self, kind: str) -> str:
-        return "lasp_fwd_kernel" if kind == "fwd" else "dq_kernel+dkdv_kernel"
+        if self.block == capi.SCA_LASP_BLOCK_TC:
+            return "block_kernel<kFwd>" if kind == "fwd" else "block_kernel<kDq,kDk,kDv>"
+        return "fwd_kernel" if kind == "fwd" else "dq_kernel+dkdv_kernel"
 
     def kernel_sources(self, kind: str):
+        if self.block == capi.SCA_LASP_BLOCK_TC:
+            return ["lasp_tc.cu", "lasp.cu", "ptx.cuh", "common.cuh"]
         return ["lasp.cu", "common.cuh"]
 
     def read_status(self) -> int:
-        """Synchronise; the linear-attention kernels never wait, so there is no
-        device status word to read."""
-        torch.cuda.current_stream(self.device).synchronize()
-        return 0
+        """Synchronise and return the device status word (0 = OK; the
+        tensor-core kernels record a timed-out wait there)."""
+        return capi.sca_read_status(_ptr(self.status), torch.cuda.current_stream(self.device).cuda_stream)
 
     def _check(self, *ts):
         for t in ts:

@@ -238,11 +238,18 @@ def test_binding_raises_with_message(lib):
 
 
 def test_lasp_rejects_bad_arguments(lib):
-    bf = capi.SCA_BF16
-    assert lib.lasp_block_states(A, 2 * A, bf, 3 * A, 2, 1024, 96, None) == capi.SCA_ERR_UNSUPPORTED   # D = 96
-    assert lib.lasp_block_states(A, 2 * A, bf, 3 * A, 2, 1000, 128, None) == capi.SCA_ERR_ARG          # S % 64
-    assert lib.lasp_block_states(None, 2 * A, bf, 3 * A, 2, 1024, 128, None) == capi.SCA_ERR_ARG
-    assert lib.lasp_scan(A, 2 * A, 2, 1024, 128, 3, 0, None) == capi.SCA_ERR_ARG                       # 1024 % (64*3)
+    bf, f32, F, T = capi.SCA_BF16, capi.SCA_F32, capi.SCA_LASP_BLOCK_F32, capi.SCA_LASP_BLOCK_TC
+    assert lib.lasp_block_states(A, 2 * A, bf, 3 * A, 2, 1024, 96, F, None, None) == capi.SCA_ERR_UNSUPPORTED  # D
+    assert lib.lasp_block_states(A, 2 * A, bf, 3 * A, 2, 1000, 128, F, None, None) == capi.SCA_ERR_ARG   # S % 64
+    assert lib.lasp_block_states(A, 2 * A, bf, 3 * A, 2, 1088, 128, T, None, None) == capi.SCA_ERR_ARG   # S % 128
+    assert lib.lasp_block_states(None, 2 * A, bf, 3 * A, 2, 1024, 128, F, None, None) == capi.SCA_ERR_ARG
+    assert lib.lasp_block_states(A, 2 * A, bf, 3 * A, 2, 1024, 128, 96, None, None) == capi.SCA_ERR_ARG  # block
+    # tensor-core blocks need bf16 and D = 128
+    assert lib.lasp_block_states(A, 2 * A, f32, 3 * A, 2, 1024, 128, T, None, None) == capi.SCA_ERR_UNSUPPORTED
+    assert lib.lasp_fwd(A, A, A, bf, A, A, A, 2, 1024, 64, 4, T, 0.1, None, None) == capi.SCA_ERR_UNSUPPORTED
+    assert lib.lasp_scan(A, 2 * A, 2, 1024, 128, 3, F, 0, None) == capi.SCA_ERR_ARG                    # 1024 % (64*3)
+    assert lib.lasp_scan(A, 2 * A, 2, 1024, 128, 16, T, 0, None) == capi.SCA_ERR_ARG                   # 1024 % (128*16)
     assert lib.lasp_exchange(A, 2 * A, 0, 128, 4, 0, None) == capi.SCA_ERR_ARG                         # BH = 0
-    assert lib.lasp_fwd(A, A, A, 7, A, A, A, 2, 1024, 128, 4, 0.1, None) == capi.SCA_ERR_ARG           # dtype
-    assert lib.lasp_bwd(A, A, A, A, bf, A, A, A, A, A, A, None, 2, 1024, 128, 4, 0.1, None) == capi.SCA_ERR_ARG
+    assert lib.lasp_fwd(A, A, A, 7, A, A, A, 2, 1024, 128, 4, F, 0.1, None, None) == capi.SCA_ERR_ARG  # dtype
+    assert lib.lasp_bwd(A, A, A, A, bf, A, A, A, A, A, A, None, 2, 1024, 128, 4, T, 0.1, None, None) == \
+        capi.SCA_ERR_ARG

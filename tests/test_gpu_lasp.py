@@ -1,7 +1,9 @@
 """GPU parity of causal linear attention over P contiguous shards passing
-states point to point (LASP) against the fp64 oracle: small cases in full
-(outputs, gradients and the states each shard receives), the 32K training
-workload at full size on sampled rows.  All arithmetic is fp32, and without
+states point to point (LASP) against the fp64 oracle, on the fp32 CUDA-core
+kernels (blocks of 64 rows) and the tensor-core kernels (blocks of 128 rows,
+fp32 operands split into two bf16 parts): small cases in full (outputs,
+gradients and the states each shard receives), the 32K training workload at
+full size on sampled rows.  Both keep about fp32 accuracy, and without
 normalisation the outputs grow like sqrt(t): the fp32 bounds (2e-4 max-abs,
 2e-5 mean-abs) apply relative to the largest reference magnitude."""
 import numpy as np
@@ -33,17 +35,19 @@ def assert_close_rel(name, got, ref, rel=REL):
         f"{name}: max-abs {mx:.3e}, mean-abs {mn:.3e} against magnitude {mag:.3e}"
 
 
-@pytest.mark.parametrize("dtype,B,H,S,D,P", [
-    ("bf16", 1, 2, 1024, 128, 4), ("bf16", 2, 2, 512, 64, 2), ("f32", 1, 2, 256, 64, 1),
-    ("f32", 1, 3, 768, 128, 3), ("bf16", 1, 1, 2048, 128, 8)])
-def test_lasp_small_full_oracle(sca, dtype, B, H, S, D, P):
+@pytest.mark.parametrize("dtype,B,H,S,D,P,block", [
+    ("bf16", 1, 2, 1024, 128, 4, 64), ("bf16", 2, 2, 512, 64, 2, 64), ("f32", 1, 2, 256, 64, 1, 64),
+    ("f32", 1, 3, 768, 128, 3, 64), ("bf16", 1, 1, 2048, 128, 8, 64),
+    ("bf16", 1, 2, 1024, 128, 4, 128), ("bf16", 2, 3, 768, 128, 3, 128), ("bf16", 1, 1, 128, 128, 1, 128),
+    ("bf16", 1, 1, 2048, 128, 8, 128)])
+def test_lasp_small_full_oracle(sca, dtype, B, H, S, D, P, block):
     q, k, v, do = seeded_inputs.make_inputs(B, H, S, D, dtype, seed=500 + P + D, with_do=True)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
-    plan = sca.ShardedLinearAttention(B, H, S, D, P, dtype=tdt, backward=True)
+    plan = sca.ShardedLinearAttention(B, H, S, D, P, dtype=tdt, backward=True, block=block)
     qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
     o = plan.forward(qd, kd, vd)
     dq, dk, dv = plan.backward(dod)
-    torch.cuda.synchronize()
+    assert plan.read_status() == 0
     scale = scale_for(D)
     assert_close_rel("o", o, oracle.linear_attention(q, k, v, scale))
     rq, rk, rv = oracle.linear_attention_backward(q, k, v, do, scale)
@@ -60,22 +64,24 @@ def test_lasp_small_full_oracle(sca, dtype, B, H, S, D, P):
                 assert_close_rel(f"bwd state b{b} h{h} r{r}", in_b[b * H + h, r], recv_b[r])
 
 
-def test_lasp_repeat_is_deterministic(sca):
+@pytest.mark.parametrize("block", [64, 128])
+def test_lasp_repeat_is_deterministic(sca, block):
     B, H, S, D, P = 1, 2, 1024, 128, 4
     q, k, v, do = (x.cuda() for x in seeded_inputs.make_inputs(B, H, S, D, "bf16", seed=7, with_do=True))
-    plan = sca.ShardedLinearAttention(B, H, S, D, P, backward=True)
+    plan = sca.ShardedLinearAttention(B, H, S, D, P, backward=True, block=block)
     a = [plan.forward(q, k, v).clone()] + [t.clone() for t in plan.backward(do)]
     b = [plan.forward(q, k, v)] + list(plan.backward(do))
     assert all(torch.equal(x, y) for x, y in zip(a, b))
 
 
-def test_lasp_training_step_full_size_sampled(sca):
+@pytest.mark.parametrize("block", [128, 64])
+def test_lasp_training_step_full_size_sampled(sca, block):
     w = WORKLOADS["lasp_s32k"]
     q, k, v, do = seeded_inputs.workload_inputs(w)
-    plan = sca.ShardedLinearAttention(w.B, w.H, w.S, w.D, w.P, backward=True)
+    plan = sca.ShardedLinearAttention(w.B, w.H, w.S, w.D, w.P, backward=True, block=block)
     o = plan.forward(q.cuda(), k.cuda(), v.cuda())
     dq, dk, dv = plan.backward(do.cuda())
-    torch.cuda.synchronize()
+    assert plan.read_status() == 0
     scale = scale_for(w.D)
     rows = seeded_inputs.sample_rows(w.B, w.H, w.S, w.sample_rows, w.seed).numpy()
     o_c, dq_c, dk_c, dv_c = o.cpu(), dq.cpu(), dk.cpu(), dv.cpu()

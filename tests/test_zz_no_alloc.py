@@ -39,7 +39,7 @@ def test_noalloc_rejects_oversize_before_any_device_work():
 @pytest.mark.parametrize("B,H,S,D,P,dtype", CASES)
 def test_noalloc_matches_buffered_forward_twice(sca, B, H, S, D, P, dtype):
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
-    plan = sca.ShardedLinearAttention(B, H, S, D, P, dtype=tdt)
+    plan = sca.ShardedLinearAttention(B, H, S, D, P, dtype=tdt, block=sca.capi.SCA_LASP_BLOCK_F32)
     st = torch.cuda.current_stream().cuda_stream
     for seed in (41, 42):
         q, k, v = (x.cuda() for x in seeded_inputs.make_inputs(B, H, S, D, dtype, seed=seed))
