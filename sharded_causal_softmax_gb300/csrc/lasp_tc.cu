@@ -27,14 +27,14 @@
 //   M[s][t] = x_s . y_t  (t >= s, else 0): A = X (K-major), B = Y (K-major)
 //   out^T   = A1 B1 + Z^T M-or-M^T
 //
-//   kernel  X  Y   Z   state term A1 (tile = state, row-major)  B1   mask as B
-//   fwd     k  q   v   F[b][a]: MN-major                         q    MN-major (k = s)
-//   dq      v  dO  k   F[a][b]: K-major                          dO   MN-major (k = s)
-//   dk      v  dO  q   G[a][b]: K-major                          v    K-major  (k = t)
-//   dv      k  q   dO  G[b][a]: MN-major                         k    K-major  (k = t)
+//   kernel  X  Y   Z   state term A1 (in tensor memory)   B1   mask as B
+//   fwd     k  q   v   A1[a][b] = F[b][a]                  q    MN-major (k = s)
+//   dq      v  dO  k   A1[a][b] = F[a][b]                  dO   MN-major (k = s)
+//   dk      v  dO  q   A1[a][b] = G[a][b]                  v    K-major  (k = t)
+//   dv      k  q   dO  A1[a][b] = G[b][a]                  k    K-major  (k = t)
 //
 // Shared-memory tiles are [128 rows][128 bf16] as two 128-byte-swizzled
-// panels of 64 columns (the layout TMA writes); the state and the mask are
+// panels of 64 columns (the layout TMA writes); the masked product is
 // written there by the threads in the same layout.
 #include <cuda.h>
 
@@ -51,7 +51,6 @@ constexpr int kBlk = 128;
 constexpr int kD = 128;
 constexpr int PANEL = 128 * 128;      // 128 rows x 64 bf16
 constexpr int TILE = 2 * PANEL;       // 128 x 128 bf16
-constexpr int kThreads = 256;
 
 SCA_INLINE void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -93,10 +92,11 @@ struct Bars {
 // states and shard inputs, the output.
 struct Args {
   CUtensorMap mx, my, mz;
-  const float* st;     // [BH, S/kBlk, D, D]
+  const float* st;         // [BH, S/kBlk, D, D]
   const float* shard_in;   // [BH, P, D, D]
-  float* out;          // [BH, S, D]
+  float* out;              // [BH, S, D]
   int64_t S;
+  int BH;
   int P;
   float scale;
   int* status;
@@ -104,178 +104,268 @@ struct Args {
 
 enum Mode { kFwd = 0, kDq = 1, kDk = 2, kDv = 3 };
 
-constexpr int X_OFF = 0, Y_OFF = TILE, Z_OFF = 2 * TILE, W0_OFF = 3 * TILE, W1_OFF = 4 * TILE, BAR_OFF = 5 * TILE;
-constexpr int kSmem = BAR_OFF + 1024 + 1024;   // bars, alignment slack
+// Persistent, pipelined block kernel: one CTA per SM walks blocks n =
+// blockIdx.x, + gridDim.x, ...  Roles: warp 8 loads X, Y, Z by TMA into two
+// shared-memory stages; one thread of warp 9 issues the MMAs; warps 0-7 put
+// each block's state into tensor memory (the A operand of the state term),
+// turn the masked product into shared-memory operands and write the output.
+// Tensor memory (512 columns): M (128), two output accumulators (2 x 128),
+// the state's hi and lo parts (64 + 64, bf16 pairs).  Shared memory: two
+// stages of X, Y, Z; the masked product's hi and lo parts overwrite X and Y
+// of their stage once the products that read them are done.
+constexpr int kPThreads = 320;
+constexpr int kConv = 256;                  // converter / epilogue threads (warps 0-7)
+constexpr int kProdWarp = 8, kMmaWarp = 9;
+constexpr int STAGE = 3 * TILE;             // X, Y, Z
+constexpr int P_BAR_OFF = 2 * STAGE;
+constexpr int kSmem = P_BAR_OFF + 1024 + 1024;
+
+struct PBars {
+  uint64_t in_full[2], stage_free[2];
+  uint64_t mask_full, tm_free, state_full, t1_done, m_full;
+  uint64_t o_full[2], o_free[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// The block's state (st[j] + shard_in[r]) as the A operand in tensor memory:
+// lane a holds A[a][b] for b in [64 half, 64 half + 64) as bf16 pairs, hi
+// and lo parts.  ROWWISE: A[a][b] = state[a][b] (a row per thread, 16-byte
+// loads); else A[a][b] = state[b][a] (a column per thread; each load
+// instruction reads 32 consecutive floats of one row).
+template <bool ROWWISE>
+SCA_INLINE void load_state(const float* st, const float* sin, uint32_t t_hi, uint32_t t_lo, int a, int half) {
+  float x[64];
+  if (ROWWISE) {
+    const float4* p = reinterpret_cast<const float4*>(st + a * kD + 64 * half);
+    const float4* q = reinterpret_cast<const float4*>(sin + a * kD + 64 * half);
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const float4 s4 = p[u], i4 = q[u];
+      x[4 * u] = s4.x + i4.x;
+      x[4 * u + 1] = s4.y + i4.y;
+      x[4 * u + 2] = s4.z + i4.z;
+      x[4 * u + 3] = s4.w + i4.w;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < 64; ++u) x[u] = st[(64 * half + u) * kD + a] + sin[(64 * half + u) * kD + a];
+  }
+  uint32_t hi[32], lo[32];
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const __nv_bfloat162 hv = __floats2bfloat162_rn(x[2 * c], x[2 * c + 1]);
+    const float2 hf = __bfloat1622float2(hv);
+    const __nv_bfloat162 lv = __floats2bfloat162_rn(x[2 * c] - hf.x, x[2 * c + 1] - hf.y);
+    hi[c] = *reinterpret_cast<const uint32_t*>(&hv);
+    lo[c] = *reinterpret_cast<const uint32_t*>(&lv);
+  }
+  tmem_st32(t_hi + 32 * half, hi);
+  tmem_st32(t_lo + 32 * half, lo);
+  tmem_wait_st();
+}
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) block_kernel(const __grid_constant__ Args a) {
-  constexpr bool kStateMN = MODE == kFwd || MODE == kDv;   // A1 = state, MN-major (else K-major)
-  constexpr bool kB1isY = MODE == kFwd || MODE == kDq;     // B1 = Y (else X)
-  constexpr bool kMaskMN = MODE == kFwd || MODE == kDq;    // mask as B: MN-major (else K-major)
+__global__ void __launch_bounds__(kPThreads, 1) block_kernel(const __grid_constant__ Args a) {
+  constexpr bool kRowwise = MODE == kDq || MODE == kDk;   // state term A = state (else its transpose)
+  constexpr bool kB1isY = MODE == kFwd || MODE == kDq;    // B1 = Y (else X)
+  constexpr bool kMaskMN = MODE == kFwd || MODE == kDq;   // mask as B: MN-major (else K-major)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Bars* bars = reinterpret_cast<Bars*>(smem + BAR_OFF);
-  const int j = blockIdx.x, bh = blockIdx.y;
+  PBars* bars = reinterpret_cast<PBars*>(smem + P_BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nblk = a.S / kBlk;
-  const int r = static_cast<int>(j / (nblk / a.P));
-  const int row0 = j * kBlk;
+  const int64_t total = static_cast<int64_t>(a.BH) * nblk;
+  const int64_t per_shard = nblk / a.P;
+  // local block i of this CTA -> global block n
+  auto block_of = [&](int i) { return static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(i) * gridDim.x; };
+  int n_local = 0;
+  if (blockIdx.x < total) n_local = static_cast<int>((total - 1 - blockIdx.x) / gridDim.x) + 1;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->in_full, 1);
-    mbar_init(&bars->mask_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->in_full[i], 1);
+      mbar_init(&bars->stage_free[i], 1);
+      mbar_init(&bars->o_full[i], 1);
+      mbar_init(&bars->o_free[i], kConv);
+    }
+    mbar_init(&bars->mask_full, 1);
+    mbar_init(&bars->tm_free, kConv);
+    mbar_init(&bars->state_full, kConv);
     mbar_init(&bars->t1_done, 1);
-    mbar_init(&bars->t2_done, 1);
+    mbar_init(&bars->m_full, kConv);
+    mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
-    tmem_alloc(&bars->tmem_base, 256);
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tM = bars->tmem_base, tO = tM + 128;
+  const uint32_t tmem = bars->tmem_base;
+  const uint32_t tM = tmem, tO0 = tmem + 128, tA_hi = tmem + 384, tA_lo = tmem + 448;
   volatile int* abort = &bars->abort;
-  const uint32_t sX = smem_u32(smem + X_OFF), sY = smem_u32(smem + Y_OFF), sZ = smem_u32(smem + Z_OFF);
-  const uint32_t sW0 = smem_u32(smem + W0_OFF), sW1 = smem_u32(smem + W1_OFF);
+  int* status = a.status;
+  const uint32_t s0 = smem_u32(smem);
 
-  if (threadIdx.x == 0) {
-    tma_prefetch_map(&a.mx);
-    tma_prefetch_map(&a.my);
-    tma_prefetch_map(&a.mz);
-    mbar_arrive_expect_tx(&bars->in_full, 3 * TILE);
-    for (int p = 0; p < 2; ++p) {
-      tma_load_4d(smem + X_OFF + p * PANEL, &a.mx, &bars->in_full, 64 * p, row0, bh, 0);
-      tma_load_4d(smem + Y_OFF + p * PANEL, &a.my, &bars->in_full, 64 * p, row0, bh, 0);
-      tma_load_4d(smem + Z_OFF + p * PANEL, &a.mz, &bars->in_full, 64 * p, row0, bh, 0);
-    }
-  }
-
-  // the state st[j] + sin[r] into W0 (hi) and W1 (lo), row-major: 16
-  // threads per row, 8 columns each (coalesced 512-byte rows)
-  {
-    const float* s0 = a.st + (static_cast<int64_t>(bh) * nblk + j) * kD * kD;
-    const float* s1 = a.shard_in + (static_cast<int64_t>(bh) * a.P + r) * kD * kD;
-    const int c = threadIdx.x & 15;
-#pragma unroll 2
-    for (int row = threadIdx.x >> 4; row < kD; row += kThreads / 16) {
-      const float4* p0 = reinterpret_cast<const float4*>(s0 + row * kD + 8 * c);
-      const float4* p1 = reinterpret_cast<const float4*>(s1 + row * kD + 8 * c);
-      const float4 u0 = p0[0], u1 = p0[1], v0 = p1[0], v1 = p1[1];
-      const float x[8] = {u0.x + v0.x, u0.y + v0.y, u0.z + v0.z, u0.w + v0.w,
-                          u1.x + v1.x, u1.y + v1.y, u1.z + v1.z, u1.w + v1.w};
-      uint4 hi, lo;
-      split8(x, hi, lo);
-      *reinterpret_cast<uint4*>(smem + W0_OFF + chunk_off(row, c)) = hi;
-      *reinterpret_cast<uint4*>(smem + W1_OFF + chunk_off(row, c)) = lo;
-    }
-  }
-  fence_async_smem();
-  tc_fence_before();
-  __syncthreads();
-
-  bool ok = true;
-  int issued = 0;   // MMA groups committed by thread 0 (for the abort drain)
-  if (threadIdx.x == 0) {
-    tc_fence_after();
-    ok = mbar_wait(&bars->in_full, 0, abort, a.status);
-    if (ok) {
-      constexpr uint32_t id_m = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t id_1 = idesc_bf16_f32(128, 128, kStateMN, false);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) umma_ss(tM, kmajor(sX, kk), kmajor(sY, kk), id_m, kk > 0 ? 1u : 0u);
-      umma_commit(&bars->mask_done);
-      const uint32_t sB1 = kB1isY ? sY : sX;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t b1 = kmajor(sB1, kk);
-        umma_ss(tO, kStateMN ? mnmajor(sW0, kk) : kmajor(sW0, kk), b1, id_1, kk > 0 ? 1u : 0u);
-        umma_ss(tO, kStateMN ? mnmajor(sW1, kk) : kmajor(sW1, kk), b1, id_1, 1u);
+  if (warp == kProdWarp) {
+    // ---------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_map(&a.mx);
+      tma_prefetch_map(&a.my);
+      tma_prefetch_map(&a.mz);
+      int i = 0;
+      for (; i < n_local; ++i) {
+        const int s = i & 1;
+        if (i >= 2 && !mbar_wait(&bars->stage_free[s], ((i >> 1) + 1) & 1, abort, status)) break;
+        const int64_t n = block_of(i);
+        const int bh = static_cast<int>(n / nblk), row0 = static_cast<int>((n % nblk) * kBlk);
+        uint8_t* st = smem + s * STAGE;
+        mbar_arrive_expect_tx(&bars->in_full[s], 3 * TILE);
+        for (int p = 0; p < 2; ++p) {
+          tma_load_4d(st + p * PANEL, &a.mx, &bars->in_full[s], 64 * p, row0, bh, 0);
+          tma_load_4d(st + TILE + p * PANEL, &a.my, &bars->in_full[s], 64 * p, row0, bh, 0);
+          tma_load_4d(st + 2 * TILE + p * PANEL, &a.mz, &bars->in_full[s], 64 * p, row0, bh, 0);
+        }
       }
-      umma_commit(&bars->t1_done);
-      issued = 2;
+      if (*abort)   // let the copies in flight land before the CTA goes away
+        for (int j = (i > 2 ? i - 2 : 0); j < i; ++j) mbar_wait_drain(&bars->in_full[j & 1], (j >> 1) & 1);
     }
-  }
-
-  // the masked block product M[s][t] (t >= s) into W0/W1 (hi, lo) once the
-  // state products have read them: warp w reads lanes 32 (w & 3) .. + 31
-  // (rows s) and columns 64 (w >> 2) .. + 63 (t)
-  const int q4 = warp & 3, half = warp >> 2;
-  const int lrow = q4 * 32 + lane;
-  const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-  // (every thread takes part in each vote; a failed wait has set *abort,
-  // so the later waits return at once)
-  ok = __all_sync(0xffffffffu, mbar_wait(&bars->mask_done, 0, abort, a.status) && ok);
-  ok = __all_sync(0xffffffffu, mbar_wait(&bars->t1_done, 0, abort, a.status) && ok);
-  if (ok) {
-    tc_fence_after();
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_m = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t id_1 = idesc_bf16_f32(128, 128, false, false);   // A (state) from tensor memory
+      constexpr uint32_t id_2 = idesc_bf16_f32(128, 128, true, kMaskMN);
+      for (int i = 0; i < n_local; ++i) {
+        const int s = i & 1;
+        const uint32_t sX = s0 + s * STAGE, sY = sX + TILE, sZ = sX + 2 * TILE;
+        const uint32_t tO = tO0 + 128 * s;
+        if (!mbar_wait(&bars->in_full[s], (i >> 1) & 1, abort, status)) break;
+        if (i >= 1 && !mbar_wait(&bars->tm_free, (i - 1) & 1, abort, status)) break;
+        tc_fence_after();
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      uint32_t v[32];
-      tmem_ld32(tM + lane_off + 64 * half + 32 * cc, v);
+        for (int kk = 0; kk < 8; ++kk) umma_ss(tM, kmajor(sX, kk), kmajor(sY, kk), id_m, kk > 0 ? 1u : 0u);
+        umma_commit(&bars->mask_full);
+        if (!mbar_wait(&bars->state_full, i & 1, abort, status)) break;
+        if (i >= 2 && !mbar_wait(&bars->o_free[s], ((i >> 1) + 1) & 1, abort, status)) break;
+        tc_fence_after();
+        const uint32_t sB1 = kB1isY ? sY : sX;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t b1 = kmajor(sB1, kk);
+          umma_ts(tO, tA_hi + 8 * kk, b1, id_1, kk > 0 ? 1u : 0u);
+          umma_ts(tO, tA_lo + 8 * kk, b1, id_1, 1u);
+        }
+        umma_commit(&bars->t1_done);
+        if (!mbar_wait(&bars->m_full, i & 1, abort, status)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a2 = mnmajor(sZ, kk);
+          umma_ss(tO, a2, kMaskMN ? mnmajor(sX, kk) : kmajor(sX, kk), id_2, 1u);   // hi part (over X)
+          umma_ss(tO, a2, kMaskMN ? mnmajor(sY, kk) : kmajor(sY, kk), id_2, 1u);   // lo part (over Y)
+        }
+        umma_commit(&bars->o_full[s]);
+        umma_commit(&bars->stage_free[s]);
+      }
+      if (*abort) {   // every MMA issued has finished before the memory goes
+        umma_commit(&bars->drain);
+        mbar_wait_drain(&bars->drain, 0);
+      }
+    }
+  } else {
+    // ---------------------------------------------------- warps 0-7
+    const int q4 = warp & 3, half = warp >> 2;
+    const int lrow = q4 * 32 + lane;   // tensor-memory lane: row s of M, feature a of the output
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    auto state_ptrs = [&](int i, const float*& st, const float*& sin) {
+      const int64_t n = block_of(i);
+      const int64_t bh = n / nblk, j = n % nblk;
+      st = a.st + (bh * nblk + j) * kD * kD;
+      sin = a.shard_in + (bh * a.P + j / per_shard) * kD * kD;
+    };
+    bool ok = true;
+    if (n_local > 0) {
+      const float *st, *sin;
+      state_ptrs(0, st, sin);
+      load_state<kRowwise>(st, sin, tA_hi + lane_off, tA_lo + lane_off, lrow, half);
+      tc_fence_before();
+      mbar_arrive(&bars->state_full);
+    }
+    for (int i = 0; ok && i < n_local; ++i) {
+      const int s = i & 1;
+      uint8_t* sX = smem + s * STAGE;
+      uint8_t* sY = sX + TILE;
+      // the masked block product out of tensor memory
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->mask_full, i & 1, abort, status));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[64];
+      tmem_ld32(tM + lane_off + 64 * half, v);
+      tmem_ld32(tM + lane_off + 64 * half + 32, v + 32);
       tmem_wait_ld32(v);
+      tmem_wait_ld32(v + 32);
+      tc_fence_before();
+      mbar_arrive(&bars->tm_free);
+      // X and Y of this stage are free once the state term has read them
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->t1_done, i & 1, abort, status));
+      if (!ok) break;
+      tc_fence_after();
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
         float x[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int t = 64 * half + 32 * cc + 8 * u + i;
-          x[i] = t >= lrow ? __uint_as_float(v[8 * u + i]) : 0.f;
+        for (int e = 0; e < 8; ++e) {
+          const int t = 64 * half + 8 * u + e;
+          x[e] = t >= lrow ? __uint_as_float(v[8 * u + e]) : 0.f;
         }
         uint4 hi, lo;
         split8(x, hi, lo);
-        const int c = 8 * half + 4 * cc + u;
-        *reinterpret_cast<uint4*>(smem + W0_OFF + chunk_off(lrow, c)) = hi;
-        *reinterpret_cast<uint4*>(smem + W1_OFF + chunk_off(lrow, c)) = lo;
+        const int c = 8 * half + u;
+        *reinterpret_cast<uint4*>(sX + chunk_off(lrow, c)) = hi;
+        *reinterpret_cast<uint4*>(sY + chunk_off(lrow, c)) = lo;
       }
-    }
-    fence_async_smem();
-  }
-  tc_fence_before();
-  __syncthreads();
-  ok = ok && !*abort;
-  if (threadIdx.x == 0 && ok) {
-    tc_fence_after();
-    constexpr uint32_t id_2 = idesc_bf16_f32(128, 128, true, kMaskMN);
+      fence_async_smem();
+      mbar_arrive(&bars->m_full);
+      // the next block's state (its tensor memory is free after t1_done)
+      if (i + 1 < n_local) {
+        const float *st, *sin;
+        state_ptrs(i + 1, st, sin);
+        load_state<kRowwise>(st, sin, tA_hi + lane_off, tA_lo + lane_off, lrow, half);
+        tc_fence_before();
+        mbar_arrive(&bars->state_full);
+      }
+      // out[row0 + r][a] = scale * out^T[a][r]: lanes are features, so each
+      // store instruction writes 32 consecutive floats of one row
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full[s], (i >> 1) & 1, abort, status));
+      if (!ok) break;
+      tc_fence_after();
+      const int64_t n = block_of(i);
+      float* out = a.out + (n / nblk * a.S + (n % nblk) * kBlk) * kD + lrow;
+      const uint32_t tO = tO0 + 128 * s;
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint64_t a2 = mnmajor(sZ, kk);
-      umma_ss(tO, a2, kMaskMN ? mnmajor(sW0, kk) : kmajor(sW0, kk), id_2, 1u);
-      umma_ss(tO, a2, kMaskMN ? mnmajor(sW1, kk) : kmajor(sW1, kk), id_2, 1u);
-    }
-    umma_commit(&bars->t2_done);
-    issued = 3;
-  }
-
-  // out[row0 + r][a] = scale * out^T[a][r]: lanes are features, so each
-  // store instruction writes 32 consecutive floats of one row
-  ok = __all_sync(0xffffffffu, mbar_wait(&bars->t2_done, 0, abort, a.status) && ok);
-  if (ok) {
-    tc_fence_after();
-    float* out = a.out + (static_cast<int64_t>(bh) * a.S + row0) * kD + lrow;
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t w[32];
+        tmem_ld32(tO + lane_off + 64 * half + 32 * cc, w);
+        tmem_wait_ld32(w);
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      uint32_t v[32];
-      tmem_ld32(tO + lane_off + 64 * half + 32 * cc, v);
-      tmem_wait_ld32(v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) out[(64 * half + 32 * cc + i) * kD] = a.scale * __uint_as_float(v[i]);
+        for (int e = 0; e < 32; ++e) out[(64 * half + 32 * cc + e) * kD] = a.scale * __uint_as_float(w[e]);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->o_free[s]);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0 && *abort) {   // let issued copies and MMAs finish before the memory goes
-    mbar_wait_drain(&bars->in_full, 0);
-    if (issued >= 2) mbar_wait_drain(&bars->t1_done, 0);
-    if (issued >= 3) mbar_wait_drain(&bars->t2_done, 0);
-  }
-  __syncthreads();
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tM, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -393,10 +483,24 @@ int lasp_tc_states(const void* a, const void* b, float* st, int64_t BH, int64_t 
   return cuda_status(cudaGetLastError(), "lasp_block_states launch");
 }
 
+static int sm_count() {
+  static int n[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (n[dev & 63] == 0) {
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) c = 148;
+    n[dev & 63] = c;
+  }
+  return n[dev & 63];
+}
+
 template <int MODE>
 static int launch_block(const void* x, const void* y, const void* z, const float* st, const float* shard_in, float* out,
                         int64_t BH, int64_t S, int P, float scale, int* status, cudaStream_t stream,
                         const char* who) {
+  SCA_REQUIRE(reinterpret_cast<uintptr_t>(st) % 16 == 0 && reinterpret_cast<uintptr_t>(shard_in) % 16 == 0,
+              SCA_ERR_ALIGN, "%s: states must be 16-byte aligned", who);
   Args a;
   cudaError_t e = map_of(&a.mx, x, BH, S);
   if (e == cudaSuccess) e = map_of(&a.my, y, BH, S);
@@ -406,11 +510,14 @@ static int launch_block(const void* x, const void* y, const void* z, const float
   a.shard_in = shard_in;
   a.out = out;
   a.S = S;
+  a.BH = static_cast<int>(BH);
   a.P = P;
   a.scale = scale;
   a.status = status;
   if ((e = allow(block_kernel<MODE>, kSmem)) != cudaSuccess) return cuda_status(e, who);
-  block_kernel<MODE><<<dim3(static_cast<unsigned>(S / kBlk), static_cast<unsigned>(BH)), kThreads, kSmem, stream>>>(a);
+  const int64_t total = BH * (S / kBlk);
+  const int grid = static_cast<int>(total < sm_count() ? total : sm_count());
+  block_kernel<MODE><<<grid, kPThreads, kSmem, stream>>>(a);
   return cuda_status(cudaGetLastError(), who);
 }
 
