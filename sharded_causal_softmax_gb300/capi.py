@@ -34,7 +34,7 @@ EXPORTED = ("attn_fwd_shard", "attn_merge_lse", "zigzag_permute", "ring_stage_bl
             "attn_bwd_shard", "attn_bwd_delta", "lasp_block_states", "lasp_scan", "lasp_exchange", "lasp_fwd",
             "lasp_bwd", "lasp_fwd_noalloc", "sca_last_error", "sca_read_status", "sca_version")
 SCA_LASP_BLOCK_F32 = 64    # blocks of the fp32 CUDA-core kernels
-SCA_LASP_BLOCK_TC = 128    # blocks of the tensor-core kernels (bf16, D = 128)
+SCA_LASP_BLOCK_TC = 128    # tensor-core kernels (bf16, D = 128): blocks of a multiple of this, up to 4096
 
 
 class ScaError(RuntimeError):

@@ -314,16 +314,17 @@ static float* scratch_ptr(cudaError_t* err) {
 using namespace sca;
 using namespace sca::lasp;
 
-// block: 64 = the fp32 CUDA-core kernels below, 128 = the tensor-core
-// kernels of lasp_tc.cu (bf16, D = 128)
+// block: 64 = the fp32 CUDA-core kernels below; a multiple of 128 (up to
+// 4096) = the tensor-core kernels of lasp_tc.cu (bf16, D = 128)
 static int lasp_check(int64_t BH, int64_t S, int D, int P, int dtype, int block, const char* who) {
   SCA_REQUIRE(BH >= 1 && BH <= 65535, SCA_ERR_ARG, "%s: BH=%lld outside [1, 65535]", who, static_cast<long long>(BH));
   SCA_REQUIRE(D == 64 || D == 128, SCA_ERR_UNSUPPORTED, "%s: D=%d: only 64 and 128", who, D);
   SCA_REQUIRE(dtype == SCA_BF16 || dtype == SCA_F32, SCA_ERR_ARG, "%s: dtype=%d unknown", who, dtype);
-  SCA_REQUIRE(block == kBlk || block == kLaspTcBlock, SCA_ERR_ARG, "%s: block=%d: only %d or %d", who, block, kBlk,
-              kLaspTcBlock);
-  SCA_REQUIRE(block == kBlk || (dtype == SCA_BF16 && D == 128), SCA_ERR_UNSUPPORTED,
-              "%s: blocks of %d rows (tensor cores) need bf16 inputs and D = 128", who, kLaspTcBlock);
+  const bool tc = block != kBlk;
+  SCA_REQUIRE(!tc || (block > 0 && block % kLaspTcSub == 0 && block <= kLaspTcMaxBlock), SCA_ERR_ARG,
+              "%s: block=%d: %d, or a multiple of %d up to %d", who, block, kBlk, kLaspTcSub, kLaspTcMaxBlock);
+  SCA_REQUIRE(!tc || (dtype == SCA_BF16 && D == 128), SCA_ERR_UNSUPPORTED,
+              "%s: blocks of a multiple of %d rows (tensor cores) need bf16 inputs and D = 128", who, kLaspTcSub);
   SCA_REQUIRE(P >= 1 && S > 0 && S % (static_cast<int64_t>(block) * P) == 0, SCA_ERR_ARG,
               "%s: S=%lld must be a positive multiple of %d*P (P=%d)", who, static_cast<long long>(S), block, P);
   return SCA_OK;
@@ -342,7 +343,7 @@ extern "C" int lasp_block_states(const void* a, const void* b, int dtype, float*
   int rc;
   if ((rc = lasp_check(BH, S, D, 1, dtype, block, "lasp_block_states")) != SCA_OK) return rc;
   SCA_REQUIRE(a && b && st, SCA_ERR_ARG, "lasp_block_states: NULL pointer");
-  if (block == kLaspTcBlock) return lasp_tc_states(a, b, st, BH, S, dev_status, as_stream(stream));
+  if (block != kBlk) return lasp_tc_states(a, b, st, BH, S, block, dev_status, as_stream(stream));
   const dim3 grid(static_cast<unsigned>(S / kBlk), static_cast<unsigned>(BH));
   cudaError_t e = cudaSuccess;
 #define SCA_STATES(DD, TT)                                                                               \
@@ -389,8 +390,7 @@ extern "C" int lasp_fwd(const void* q, const void* k, const void* v, int dtype, 
   int rc;
   if ((rc = lasp_check(BH, S, D, P, dtype, block, "lasp_fwd")) != SCA_OK) return rc;
   SCA_REQUIRE(q && k && v && st && shard_in && o, SCA_ERR_ARG, "lasp_fwd: NULL pointer");
-  if (block == kLaspTcBlock)
-    return lasp_tc_fwd(q, k, v, st, shard_in, o, BH, S, P, scale, dev_status, as_stream(stream));
+  if (block != kBlk) return lasp_tc_fwd(q, k, v, st, shard_in, o, BH, S, P, block, scale, dev_status, as_stream(stream));
   const dim3 grid(static_cast<unsigned>(S / kBlk), static_cast<unsigned>(BH));
   cudaError_t e = cudaSuccess;
 #define SCA_FWD(DD, TT)                                                                                    \
@@ -416,8 +416,8 @@ extern "C" int lasp_bwd(const void* q, const void* k, const void* v, const void*
   if ((rc = lasp_check(BH, S, D, P, dtype, block, "lasp_bwd")) != SCA_OK) return rc;
   SCA_REQUIRE(q && k && v && dout && st_fwd && in_fwd && st_bwd && in_bwd && dq && dk && dv, SCA_ERR_ARG,
               "lasp_bwd: NULL pointer");
-  if (block == kLaspTcBlock)
-    return lasp_tc_bwd(q, k, v, dout, st_fwd, in_fwd, st_bwd, in_bwd, dq, dk, dv, BH, S, P, scale, dev_status,
+  if (block != kBlk)
+    return lasp_tc_bwd(q, k, v, dout, st_fwd, in_fwd, st_bwd, in_bwd, dq, dk, dv, BH, S, P, block, scale, dev_status,
                        as_stream(stream));
   const dim3 grid(static_cast<unsigned>(S / kBlk), static_cast<unsigned>(BH));
   cudaError_t e = cudaSuccess;

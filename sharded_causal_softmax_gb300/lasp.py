@@ -14,9 +14,9 @@ inside the block with the right product of its queries and the state.
 Backward: the same with q^T dO states travelling from later shards to
 earlier ones.  The shards are contiguous (linear attention costs the same
 per row, so no zigzag).  bf16 inputs with D = 128 run on the tensor-core
-kernels (blocks of 128 rows); fp32 inputs and D = 64 on the fp32 CUDA-core
-kernels (blocks of 64 rows).  PyTorch supplies device memory and streams
-only.
+kernels (blocks of up to 512 rows, carried through in sub-blocks of 128);
+fp32 inputs and D = 64 on the fp32 CUDA-core kernels (blocks of 64 rows).
+PyTorch supplies device memory and streams only.
 """
 from __future__ import annotations
 
@@ -44,12 +44,16 @@ class ShardedLinearAttention:
         if D not in (64, 128):
             raise ValueError(f"D={D}: only 64 and 128")
         tc_ok = dtype == torch.bfloat16 and D == 128
+        sub = capi.SCA_LASP_BLOCK_TC
         if block is None:
-            block = capi.SCA_LASP_BLOCK_TC if tc_ok else capi.SCA_LASP_BLOCK_F32
-        if block not in (capi.SCA_LASP_BLOCK_F32, capi.SCA_LASP_BLOCK_TC) or \
-                (block == capi.SCA_LASP_BLOCK_TC and not tc_ok):
-            raise ValueError(f"block={block}: 64, or 128 for bf16 inputs with D = 128")
+            block = capi.SCA_LASP_BLOCK_F32
+            if tc_ok:   # the largest of 512, 256, 128 rows that tiles every shard
+                block = next((b for b in (4 * sub, 2 * sub, sub) if S % (b * P) == 0), sub)
+        tc = block != capi.SCA_LASP_BLOCK_F32
+        if tc and (block % sub or not sub <= block <= 4096 or not tc_ok):
+            raise ValueError(f"block={block}: 64, or a multiple of {sub} up to 4096 for bf16 inputs with D = 128")
         blk = self.block = block
+        self.tensor_cores = tc
         if S % (blk * P):
             raise ValueError(f"S={S} must be a multiple of {blk}*P={blk * P}")
         self.B, self.H, self.S, self.D, self.P, self.dtype = B, H, S, D, P, dtype
@@ -103,7 +107,7 @@ class ShardedLinearAttention:
         capi.lasp_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), dt, _ptr(self.st_f), _ptr(self.in_f), _ptr(self.st_b),
                       _ptr(self.in_b), _ptr(self.dq), _ptr(self.dk), _ptr(self.dv), BH, S, D, P, blk, self.scale,
                       sp, st)
-        self.kernels = 6 if blk == capi.SCA_LASP_BLOCK_TC else 5
+        self.kernels = 6 if self.tensor_cores else 5
         return self.dq, self.dk, self.dv
 
     # ---- the interface the benchmark reads (mirrors ShardedCausalAttention)
@@ -113,16 +117,18 @@ class ShardedLinearAttention:
         return "contiguous shards, blocks of %d rows" % self.block
 
     def roofline_bound(self, kind: str) -> str:
-        """The tensor-core kernels move ~224 (forward) and ~448 (backward)
-        bytes per 128-row block for ~94 FLOP of tcgen05 work per byte, under
-        the bf16 ridge (~290 FLOP/B): bytes bound.  The CUDA-core kernels are
+        """The tensor-core kernels do six 128x128x128 MMA groups per 128-row
+        sub-block (25 MFLOP) against ~180 KB moved (input and output rows,
+        a share of the block state): ~140 FLOP per byte, under the bf16
+        ridge (~290 FLOP/B), so bytes bound.  The CUDA-core kernels are
         bound by fp32 FMA issue."""
-        return "hbm" if self.block == capi.SCA_LASP_BLOCK_TC else "alu"
+        return "hbm" if self.tensor_cores else "alu"
 
     def algorithmic_bytes(self, kind: str) -> int:
-        """Bytes one lasp_fwd / lasp_bwd call must move: per block its input
-        tiles (bf16), its fp32 D x D state(s) and its fp32 output tiles (the
-        per-shard inputs are shared by a shard's blocks and stay in L2)."""
+        """Bytes one lasp_fwd / lasp_bwd call must move: its input rows
+        (bf16), per block its fp32 D x D state(s), and its fp32 output rows
+        (the per-shard inputs are shared by a shard's blocks and stay in
+        L2)."""
         nb = self.BH * (self.S // self.block)
         rows, D = self.block, self.D
         if kind == "fwd":
@@ -130,15 +136,15 @@ class ShardedLinearAttention:
         return nb * (4 * rows * D * 2 + 2 * D * D * 4 + 3 * rows * D * 4)
 
     def uses_tensor_cores(self, kind: str) -> bool:
-        return self.block == capi.SCA_LASP_BLOCK_TC
+        return self.tensor_cores
 
     def kernel_name(self, kind: str) -> str:
-        if self.block == capi.SCA_LASP_BLOCK_TC:
+        if self.tensor_cores:
             return "block_kernel<kFwd>" if kind == "fwd" else "block_kernel<kDq,kDk,kDv>"
         return "fwd_kernel" if kind == "fwd" else "dq_kernel+dkdv_kernel"
 
     def kernel_sources(self, kind: str):
-        if self.block == capi.SCA_LASP_BLOCK_TC:
+        if self.tensor_cores:
             return ["lasp_tc.cu", "lasp.cu", "ptx.cuh", "common.cuh"]
         return ["lasp.cu", "common.cuh"]
 

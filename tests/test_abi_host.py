@@ -244,6 +244,8 @@ def test_lasp_rejects_bad_arguments(lib):
     assert lib.lasp_block_states(A, 2 * A, bf, 3 * A, 2, 1088, 128, T, None, None) == capi.SCA_ERR_ARG   # S % 128
     assert lib.lasp_block_states(None, 2 * A, bf, 3 * A, 2, 1024, 128, F, None, None) == capi.SCA_ERR_ARG
     assert lib.lasp_block_states(A, 2 * A, bf, 3 * A, 2, 1024, 128, 96, None, None) == capi.SCA_ERR_ARG  # block
+    assert lib.lasp_block_states(A, 2 * A, bf, 3 * A, 2, 8192, 128, 8192, None, None) == capi.SCA_ERR_ARG  # > 4096
+    assert lib.lasp_scan(A, 2 * A, 2, 1024, 128, 4, 512, 0, None) == capi.SCA_ERR_ARG                  # 1024 % (512*4)
     # tensor-core blocks need bf16 and D = 128
     assert lib.lasp_block_states(A, 2 * A, f32, 3 * A, 2, 1024, 128, T, None, None) == capi.SCA_ERR_UNSUPPORTED
     assert lib.lasp_fwd(A, A, A, bf, A, A, A, 2, 1024, 64, 4, T, 0.1, None, None) == capi.SCA_ERR_UNSUPPORTED

@@ -39,7 +39,8 @@ def assert_close_rel(name, got, ref, rel=REL):
     ("bf16", 1, 2, 1024, 128, 4, 64), ("bf16", 2, 2, 512, 64, 2, 64), ("f32", 1, 2, 256, 64, 1, 64),
     ("f32", 1, 3, 768, 128, 3, 64), ("bf16", 1, 1, 2048, 128, 8, 64),
     ("bf16", 1, 2, 1024, 128, 4, 128), ("bf16", 2, 3, 768, 128, 3, 128), ("bf16", 1, 1, 128, 128, 1, 128),
-    ("bf16", 1, 1, 2048, 128, 8, 128)])
+    ("bf16", 1, 1, 2048, 128, 8, 128), ("bf16", 1, 2, 1024, 128, 4, 256), ("bf16", 2, 2, 2048, 128, 2, 512),
+    ("bf16", 1, 3, 1536, 128, 1, 1536), ("bf16", 3, 1, 2304, 128, 3, 384)])
 def test_lasp_small_full_oracle(sca, dtype, B, H, S, D, P, block):
     q, k, v, do = seeded_inputs.make_inputs(B, H, S, D, dtype, seed=500 + P + D, with_do=True)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
@@ -64,7 +65,7 @@ def test_lasp_small_full_oracle(sca, dtype, B, H, S, D, P, block):
                 assert_close_rel(f"bwd state b{b} h{h} r{r}", in_b[b * H + h, r], recv_b[r])
 
 
-@pytest.mark.parametrize("block", [64, 128])
+@pytest.mark.parametrize("block", [64, 128, 256])
 def test_lasp_repeat_is_deterministic(sca, block):
     B, H, S, D, P = 1, 2, 1024, 128, 4
     q, k, v, do = (x.cuda() for x in seeded_inputs.make_inputs(B, H, S, D, "bf16", seed=7, with_do=True))
@@ -74,7 +75,7 @@ def test_lasp_repeat_is_deterministic(sca, block):
     assert all(torch.equal(x, y) for x, y in zip(a, b))
 
 
-@pytest.mark.parametrize("block", [128, 64])
+@pytest.mark.parametrize("block", [512, 128, 64])
 def test_lasp_training_step_full_size_sampled(sca, block):
     w = WORKLOADS["lasp_s32k"]
     q, k, v, do = seeded_inputs.workload_inputs(w)
