@@ -253,8 +253,10 @@ int attn_bwd_delta(const float* o, const void* dout, int dout_dtype, float* delt
  * Rows go in blocks of `block` rows, which also selects the kernels:
  *   SCA_LASP_BLOCK_F32 (64): fp32 arithmetic on the CUDA cores; bf16 or
  *     fp32 inputs, D 64 or 128;
- *   SCA_LASP_BLOCK_TC (128): tcgen05 tensor cores with fp32 accumulation;
- *     bf16 inputs and D = 128 only (else SCA_ERR_UNSUPPORTED).  The fp32
+ *   a multiple of SCA_LASP_BLOCK_TC (128) up to 4096: tcgen05 tensor cores
+ *     with fp32 accumulation, each block taken as sub-blocks of 128 rows
+ *     with the state carried from one to the next inside the kernel; bf16
+ *     inputs and D = 128 only (else SCA_ERR_UNSUPPORTED).  The fp32
  *     operands (states, masked block products) are split into two bf16
  *     parts and multiplied twice, keeping about fp32 accuracy.
  * S must be a multiple of block * P, and every call of one pass uses the

@@ -79,24 +79,28 @@ def counters(path: str) -> str:
     return "\n".join(out)
 
 
-def traffic(path: str, kernel: str, workload: str, scale: float, sources) -> dict:
+def traffic(path: str, kernel: str, workload: str, scale: float, sources, match: str | None = None) -> dict:
     """Record dram read+write bytes of the captured launch of `kernel`,
     scaled by `scale` (units of the bench launch / units of the captured
     launch), with a hash of the kernel's sources (the bench reports the
-    figure only while the sources are unchanged)."""
+    figure only while the sources are unchanged).  With `match`, the bytes
+    of every captured launch whose kernel name matches that regex are added
+    up (one library call made of several kernels); else the first launch."""
     import hashlib
     import json
     import os
     raw = subprocess.run(["ncu", "-i", path, "--page", "raw", "--csv"], capture_output=True, text=True).stdout
     rows = list(csv.reader(io.StringIO(raw)))
-    hdr, units, vals = rows[0], rows[1], rows[2]
+    hdr, units = rows[0], rows[1]
     mult = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    ki = hdr.index("Kernel Name")
+    picked = [v for v in rows[2:] if re.search(match, v[ki])] if match else rows[2:3]
 
-    def get(name):
+    def get(vals, name):
         i = hdr.index(name)
         return float(vals[i].replace(",", "")) * mult.get(units[i], 1)
 
-    bytes_ = get("dram__bytes_read.sum") + get("dram__bytes_write.sum")
+    bytes_ = sum(get(v, "dram__bytes_read.sum") + get(v, "dram__bytes_write.sum") for v in picked)
     csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc")
     h = hashlib.sha256()
     for n in sources:
@@ -122,5 +126,11 @@ if __name__ == "__main__":
     elif what == "counters":
         print(counters(path))
     elif what == "traffic":
-        # traffic <report> <kernel> <workload> <scale> <source files...>
-        print(traffic(path, sys.argv[3], sys.argv[4], float(sys.argv[5]), sys.argv[6:]))
+        # traffic <report> <kernel> <workload> <scale> <source files...> [--match <regex>]
+        rest = sys.argv[6:]
+        match = None
+        if "--match" in rest:
+            i = rest.index("--match")
+            match = rest[i + 1]
+            rest = rest[:i] + rest[i + 2:]
+        print(traffic(path, sys.argv[3], sys.argv[4], float(sys.argv[5]), rest, match))
