@@ -208,7 +208,8 @@ def run_gpu(args):
         w = dataclasses.replace(w, schedule=args.schedule)
     def make_plan():
         if w.method == "lasp":
-            return sca.ShardedLinearAttention(w.B, w.H, w.S, w.D, w.P, dtype=dtype, backward=w.backward)
+            return sca.ShardedLinearAttention(w.B, w.H, w.S, w.D, w.P, dtype=dtype, backward=w.backward,
+                                              block=args.lasp_block or None)
         return sca.ShardedCausalAttention(w.B, w.H, w.S, w.D, w.P, layout=w.layout, dtype=dtype,
                                           head_groups=w.head_groups, schedule=w.schedule, backward=w.backward,
                                           addressing=args.addressing, kv_heads=w.kv_heads)
@@ -567,6 +568,8 @@ def main():
     ap.add_argument("--schedule", choices=["ring", "direct", "fused"], default=None,
                     help="override the workload's schedule")
     ap.add_argument("--addressing", choices=["auto", "position", "permuted"], default="auto")
+    ap.add_argument("--lasp-block", type=int, default=0,
+                    help="linear attention: rows per stored state (64: CUDA cores; a multiple of 128: tensor cores)")
     ap.add_argument("--heads", type=int, default=0,
                     help="override the head count (profiler captures of a smaller case; not a bench line)")
     args = ap.parse_args()

@@ -108,11 +108,12 @@ enum Mode { kFwd = 0, kDq = 1, kDk = 2, kDv = 3 };
 // issues the MMAs; warps 0-7 keep the running state (fp32, in registers:
 // lane a, half of the b range each), put it into tensor memory as the A
 // operand of the state term, turn the masked product into shared-memory
-// operands and write the output.  Tensor memory (512 columns): M, then the
-// sub-block's own state product U (128); two output accumulators (2 x 128);
-// the state's hi and lo parts (64 + 64, bf16 pairs).  The masked product's
-// hi and lo parts overwrite X and Y of their stage once the products that
-// read them are done.
+// operands and write the output.  Tensor memory (512 columns): M (128);
+// two output accumulators (2 x 128); the state's hi and lo parts (64 + 64,
+// bf16 pairs), which the sub-block's own state product U (fp32, 128)
+// overwrites once the state term has read them (MMAs from one thread run
+// in order).  The masked product's hi and lo parts overwrite X and Y of
+// their stage once the products that read them are done.
 constexpr int kThreads = 320;
 constexpr int kConv = 256;                  // warps 0-7
 constexpr int kProdWarp = 8, kMmaWarp = 9;
@@ -123,9 +124,9 @@ constexpr int kSmem = BAR_OFF + 1024 + 1024;
 struct Bars {
   uint64_t in_full[2], stage_free[2];
   uint64_t mask_full;    // M of sub-block c in tM
-  uint64_t tm_free;      // converters done with tM: twice per sub-block (after M, after U)
+  uint64_t tm_free;      // converters done with M of sub-block c
   uint64_t state_full;   // A1 of sub-block c in tensor memory
-  uint64_t t1u_done;     // state term and U of sub-block c done: X, Y, A1 free, U in tM
+  uint64_t t1u_done;     // state term and U of sub-block c done: X, Y free, U over A1
   uint64_t m_full;       // masked product of sub-block c in X, Y
   uint64_t o_full[2], o_free[2];
   uint64_t drain;
@@ -144,7 +145,7 @@ SCA_INLINE void load_state(float (&run)[64], const float* st, const float* sin, 
     const float4* q = reinterpret_cast<const float4*>(sin + a * kD + 64 * half);
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
-      const float4 s4 = p[u], i4 = q[u];
+      const float4 s4 = __ldg(p + u), i4 = __ldg(q + u);
       run[4 * u] = s4.x + i4.x;
       run[4 * u + 1] = s4.y + i4.y;
       run[4 * u + 2] = s4.z + i4.z;
@@ -251,17 +252,25 @@ __global__ void __launch_bounds__(kThreads, 1) block_kernel(const __grid_constan
       constexpr uint32_t id_1 = idesc_bf16_f32(128, 128, false, false);   // A1 from tensor memory
       constexpr uint32_t id_2 = idesc_bf16_f32(128, 128, true, kMaskMN);
       constexpr uint32_t id_u = idesc_bf16_f32(128, 128, true, true);
-      for (int c = 0; c < n_sub; ++c) {
+      // M of sub-block c into tM once its tiles have landed and the
+      // converters hold M of sub-block c - 1
+      auto issue_mask = [&](int c) -> bool {
         const int s = c & 1;
-        const bool last = c % nsub == nsub - 1;   // no U: the next block starts from its stored state
-        const uint32_t sX = s0 + s * STAGE, sY = sX + TILE, sZ = sX + 2 * TILE;
-        const uint32_t tO = tO0 + 128 * s;
-        if (!mbar_wait(&bars->in_full[s], (c >> 1) & 1, abort, status)) break;
-        if (c >= 1 && !mbar_wait(&bars->tm_free, 1, abort, status)) break;   // completion 2c - 1
+        const uint32_t sX = s0 + s * STAGE, sY = sX + TILE;
+        if (!mbar_wait(&bars->in_full[s], (c >> 1) & 1, abort, status)) return false;
+        if (c >= 1 && !mbar_wait(&bars->tm_free, (c - 1) & 1, abort, status)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) umma_ss(tM, kmajor(sX, kk), kmajor(sY, kk), id_m, kk > 0 ? 1u : 0u);
         umma_commit(&bars->mask_full);
+        return true;
+      };
+      bool ok = n_sub == 0 || issue_mask(0);
+      for (int c = 0; ok && c < n_sub; ++c) {
+        const int s = c & 1;
+        const bool last = c % nsub == nsub - 1;   // no U: the next block starts from its stored state
+        const uint32_t sX = s0 + s * STAGE, sY = sX + TILE, sZ = sX + 2 * TILE;
+        const uint32_t tO = tO0 + 128 * s;
         if (!mbar_wait(&bars->state_full, c & 1, abort, status)) break;
         if (c >= 2 && !mbar_wait(&bars->o_free[s], ((c >> 1) + 1) & 1, abort, status)) break;
         tc_fence_after();
@@ -272,14 +281,17 @@ __global__ void __launch_bounds__(kThreads, 1) block_kernel(const __grid_constan
           umma_ts(tO, tA_hi + 8 * kk, b1, id_1, kk > 0 ? 1u : 0u);
           umma_ts(tO, tA_lo + 8 * kk, b1, id_1, 1u);
         }
-        if (!last) {   // U into tM once the converters hold M (completion 2c)
-          if (!mbar_wait(&bars->tm_free, 0, abort, status)) break;
-          tc_fence_after();
+        if (!last) {   // U over the state's columns, after the state term has read them
           const uint32_t sW = kWisX ? sX : sY;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) umma_ss(tM, mnmajor(sZ, kk), mnmajor(sW, kk), id_u, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) umma_ss(tA_hi, mnmajor(sZ, kk), mnmajor(sW, kk), id_u, kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars->t1u_done);
+        // the next masked product fills the wait for m_full when its tiles
+        // are already there; otherwise it follows this sub-block's products
+        const int cn = c + 1;
+        const bool early = cn < n_sub && mbar_try_wait(&bars->in_full[cn & 1], (cn >> 1) & 1);
+        if (early && !issue_mask(cn)) break;
         if (!mbar_wait(&bars->m_full, c & 1, abort, status)) break;
         tc_fence_after();
 #pragma unroll
@@ -290,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_kernel(const __grid_constan
         }
         umma_commit(&bars->o_full[s]);
         umma_commit(&bars->stage_free[s]);
+        if (cn < n_sub && !early && !issue_mask(cn)) break;
       }
       if (*abort) {   // every MMA issued has finished before the memory goes
         umma_commit(&bars->drain);
@@ -330,8 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1) block_kernel(const __grid_constan
       tmem_wait_ld32(v);
       tmem_wait_ld32(v + 32);
       tc_fence_before();
-      mbar_arrive(&bars->tm_free);   // completion 2c
-      // X, Y and A1 are free, U is in tM
+      mbar_arrive(&bars->tm_free);
+      // X and Y are free, U is over the state's columns
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->t1u_done, c & 1, abort, status));
       if (!ok) break;
       tc_fence_after();
@@ -350,21 +363,24 @@ __global__ void __launch_bounds__(kThreads, 1) block_kernel(const __grid_constan
       }
       fence_async_smem();
       mbar_arrive(&bars->m_full);
-      // the state of the next sub-block: add U, or the next block's stored state
+      // the state of the next sub-block: run + U, or the next block's
+      // stored state
       if (!last) {
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t w[32];
-          tmem_ld32(tM + lane_off + 64 * half + 32 * cc, w);
+          tmem_ld32(tA_hi + lane_off + 64 * half + 32 * cc, w);
           tmem_wait_ld32(w);
 #pragma unroll
           for (int e = 0; e < 32; ++e) run[32 * cc + e] += __uint_as_float(w[e]);
         }
+        // every warp has read its part of U before any overwrites it
+        tc_fence_before();
+        asm volatile("bar.sync 1, %0;" ::"n"(kConv) : "memory");
+        tc_fence_after();
       } else if (c + 1 < n_sub) {
         load_block_state(c / nsub + 1, run);
       }
-      tc_fence_before();
-      mbar_arrive(&bars->tm_free);   // completion 2c + 1
       if (c + 1 < n_sub) {
         put_state(run, tA_hi + lane_off, tA_lo + lane_off, half);
         tc_fence_before();

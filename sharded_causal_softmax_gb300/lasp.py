@@ -14,7 +14,7 @@ inside the block with the right product of its queries and the state.
 Backward: the same with q^T dO states travelling from later shards to
 earlier ones.  The shards are contiguous (linear attention costs the same
 per row, so no zigzag).  bf16 inputs with D = 128 run on the tensor-core
-kernels (blocks of up to 512 rows, carried through in sub-blocks of 128);
+kernels (blocks of up to 4096 rows, carried through in sub-blocks of 128);
 fp32 inputs and D = 64 on the fp32 CUDA-core kernels (blocks of 64 rows).
 PyTorch supplies device memory and streams only.
 """
@@ -47,8 +47,11 @@ class ShardedLinearAttention:
         sub = capi.SCA_LASP_BLOCK_TC
         if block is None:
             block = capi.SCA_LASP_BLOCK_F32
-            if tc_ok:   # the largest of 512, 256, 128 rows that tiles every shard
-                block = next((b for b in (4 * sub, 2 * sub, sub) if S % (b * P) == 0), sub)
+            if tc_ok:
+                # the largest block (up to 4096 rows) that tiles every shard and
+                # still gives at least 128 blocks to spread over the SMs
+                fits = [b for b in (4096, 2048, 1024, 512, 256, 128) if S % (b * P) == 0]
+                block = next((b for b in fits if B * H * (S // b) >= 128), fits[-1] if fits else sub)
         tc = block != capi.SCA_LASP_BLOCK_F32
         if tc and (block % sub or not sub <= block <= 4096 or not tc_ok):
             raise ValueError(f"block={block}: 64, or a multiple of {sub} up to 4096 for bf16 inputs with D = 128")
