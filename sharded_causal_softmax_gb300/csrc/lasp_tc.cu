@@ -135,22 +135,14 @@ struct Bars {
 };
 
 // run[u] = A1[a][64 half + u] of block state st + shard input sin.
-// ROWWISE: A1[a][b] = state[a][b] (a row per thread, 16-byte loads); else
+// ROWWISE: A1[a][b] = state[a][b] (a row per thread); else
 // A1[a][b] = state[b][a] (a column per thread; each load instruction reads
 // 32 consecutive floats of one row).
 template <bool ROWWISE>
 SCA_INLINE void load_state(float (&run)[64], const float* st, const float* sin, int a, int half) {
   if (ROWWISE) {
-    const float4* p = reinterpret_cast<const float4*>(st + a * kD + 64 * half);
-    const float4* q = reinterpret_cast<const float4*>(sin + a * kD + 64 * half);
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const float4 s4 = __ldg(p + u), i4 = __ldg(q + u);
-      run[4 * u] = s4.x + i4.x;
-      run[4 * u + 1] = s4.y + i4.y;
-      run[4 * u + 2] = s4.z + i4.z;
-      run[4 * u + 3] = s4.w + i4.w;
-    }
+    for (int u = 0; u < 64; ++u) run[u] = st[a * kD + 64 * half + u] + sin[a * kD + 64 * half + u];
   } else {
 #pragma unroll
     for (int u = 0; u < 64; ++u) run[u] = st[(64 * half + u) * kD + a] + sin[(64 * half + u) * kD + a];
