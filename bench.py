@@ -62,6 +62,14 @@ def flops(w, fwd=True, bwd=True):
     return f
 
 
+def workload_config(w, ws: int) -> dict:
+    """The `config` object both arms print for a workload."""
+    return {"workload": w.description, "name": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "P": w.P,
+            "method": w.method, "layout": w.layout, "schedule": w.schedule, "kv_heads": w.kv_heads or w.H,
+            "head_groups": w.head_groups, "step": "fwd+bwd" if w.backward else "fwd", "flops_per_step": flops(w),
+            "parallelism": f"{ws} independent replica(s), one per GPU"}
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -455,14 +463,9 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded N(0,1))",
-        "config": {"workload": w.description, "name": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "P": w.P,
-                   "method": w.method, "layout": w.layout, "schedule": w.schedule, "addressing": plan.addressing,
-                   "kv_heads": w.kv_heads or w.H,
-                   "head_groups": w.head_groups,
-                   "step": "fwd+bwd" if w.backward else "fwd",
-                   "flops_per_step": step_flops, "l2": "inputs larger than L2 (no flush)"
-                   if sum(x.numel() * x.element_size() for x in inputs) > L2_BYTES else "inputs fit in L2",
-                   "parallelism": f"{ws} independent replica(s), one per GPU"},
+        "config": dict(workload_config(w, ws), addressing=plan.addressing,
+                       l2="inputs larger than L2 (no flush)"
+                       if sum(x.numel() * x.element_size() for x in inputs) > L2_BYTES else "inputs fit in L2"),
         "clocks": clocks.summary(h0, h1),
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
@@ -533,6 +536,8 @@ def run_reference(args):
     if rank != 0:
         return
     w = WORKLOADS[args.workload]
+    if args.schedule:   # the same config object as the GPU arm (the oracle's math does not depend on it)
+        w = dataclasses.replace(w, schedule=args.schedule)
     S2 = pick_sample(w, budget_s=min(12.0, 150.0 / max(1, args.steps + args.warmup)))
     head, f = oracle_sample(w, S2)
     for _ in range(args.warmup):
@@ -548,8 +553,7 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
             "impl": "reference",
-            "config": {"workload": w.description, "name": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
-                       "P": w.P, "layout": w.layout},
+            "config": workload_config(w, ws),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
