@@ -33,6 +33,17 @@ def _ptr(t: torch.Tensor) -> int:
     return t.data_ptr()
 
 
+def default_block(B: int, H: int, S: int, D: int, P: int, dtype) -> int:
+    """Rows per stored state: 64 on the CUDA-core path (fp32 inputs or
+    D = 64); on the tensor cores the largest block (up to 4096 rows) that
+    tiles every shard and still gives at least 128 blocks to spread over
+    the SMs (the smallest that tiles, else 128)."""
+    if dtype != torch.bfloat16 or D != 128:
+        return capi.SCA_LASP_BLOCK_F32
+    fits = [b for b in (4096, 2048, 1024, 512, 256, 128) if S % (b * P) == 0]
+    return next((b for b in fits if B * H * (S // b) >= 128), fits[-1] if fits else capi.SCA_LASP_BLOCK_TC)
+
+
 class ShardedLinearAttention:
     """Buffers and launch schedule of one LASP configuration; inputs are
     contiguous [B, H, S, D] tensors of ``dtype``, outputs fp32."""
@@ -46,12 +57,7 @@ class ShardedLinearAttention:
         tc_ok = dtype == torch.bfloat16 and D == 128
         sub = capi.SCA_LASP_BLOCK_TC
         if block is None:
-            block = capi.SCA_LASP_BLOCK_F32
-            if tc_ok:
-                # the largest block (up to 4096 rows) that tiles every shard and
-                # still gives at least 128 blocks to spread over the SMs
-                fits = [b for b in (4096, 2048, 1024, 512, 256, 128) if S % (b * P) == 0]
-                block = next((b for b in fits if B * H * (S // b) >= 128), fits[-1] if fits else sub)
+            block = default_block(B, H, S, D, P, dtype)
         tc = block != capi.SCA_LASP_BLOCK_F32
         if tc and (block % sub or not sub <= block <= 4096 or not tc_ok):
             raise ValueError(f"block={block}: 64, or a multiple of {sub} up to 4096 for bf16 inputs with D = 128")

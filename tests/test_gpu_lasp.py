@@ -75,11 +75,12 @@ def test_lasp_repeat_is_deterministic(sca, block):
     assert all(torch.equal(x, y) for x, y in zip(a, b))
 
 
-@pytest.mark.parametrize("block", [512, 128, 64])
+@pytest.mark.parametrize("block", [None, 512, 128, 64])   # None: the plan's default (4096 rows here)
 def test_lasp_training_step_full_size_sampled(sca, block):
     w = WORKLOADS["lasp_s32k"]
     q, k, v, do = seeded_inputs.workload_inputs(w)
     plan = sca.ShardedLinearAttention(w.B, w.H, w.S, w.D, w.P, backward=True, block=block)
+    assert block is not None or plan.block == 4096
     o = plan.forward(q.cuda(), k.cuda(), v.cuda())
     dq, dk, dv = plan.backward(do.cuda())
     assert plan.read_status() == 0

@@ -31,3 +31,17 @@ def test_ring_order_and_zigzag_segments():
     assert (s.n, s.len, s.start[0], s.start[1]) == (2, 128, 128, 768)
     s = shard_segs(1024, P, "contiguous", 3)
     assert (s.n, s.len, s.start[0]) == (1, 256, 768)
+
+
+def test_linear_attention_default_block():
+    import torch
+    from sharded_causal_softmax_gb300.lasp import default_block
+    bf = torch.bfloat16
+    assert default_block(1, 16, 32768, 128, 4, bf) == 4096      # 128 blocks of 4096 rows
+    assert default_block(1, 4, 32768, 128, 4, bf) == 1024       # at least 128 blocks
+    assert default_block(1, 2, 1024, 128, 4, bf) == 128         # too small for 128 blocks: the smallest
+    assert default_block(1, 16, 32768, 128, 4, torch.float32) == 64   # fp32 inputs: CUDA cores
+    assert default_block(1, 16, 32768, 64, 4, bf) == 64         # D = 64: CUDA cores
+    for args in [(1, 16, 32768, 128, 4), (2, 3, 2304, 128, 3), (1, 1, 128, 128, 1)]:
+        b = default_block(*args, bf)
+        assert b % 128 == 0 and args[2] % (b * args[4]) == 0
