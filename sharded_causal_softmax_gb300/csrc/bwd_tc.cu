@@ -359,11 +359,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         if (n == 0 && !mbar_wait(&bars->k_conv, 0, abort, status)) { ok = false; break; }
         if (!mbar_wait(&bars->q_conv, n & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
+        const uint64_t kdk = sdesc_sw128(sK, 16, 1024), qdk = sdesc_sw128(sQ, 16, 1024);
+        const uint64_t vdk = sdesc_sw128(sV, 16, 1024), odk = sdesc_sw128(sO, 16, 1024);
+        const uint64_t odm = sdesc_sw128(sO, PANEL, 1024), qdm = sdesc_sw128(sQ, PANEL, 1024);
+        const uint64_t sdm = sdesc_sw128(sDS, PANEL, 1024), kdm = sdesc_sw128(sK, PANEL, 1024);
+        const uint32_t acc0 = n > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;
-          umma_ss(tS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idesc_s,
-                  kk > 0 ? 1u : 0u);
+          umma_ss(tS, sdesc_step(kdk, off), sdesc_step(qdk, off), idesc_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars->s_full);
         // dP^T = V dO^T over the dP^T columns, which hold the previous dQ
@@ -378,8 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;
-          umma_ss(tdP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sO + off, 16, 1024), idesc_dp,
-                  kk > 0 ? 1u : 0u);
+          umma_ss(tdP, sdesc_step(vdk, off), sdesc_step(odk, off), idesc_dp, kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars->dp_full);
         // dV += P^T dO, then dK += dS^T Q (A from tensor memory).  Query
@@ -394,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           for (int q = 0; q < 4; ++q) {
             const int kk = 4 * (q >> 1) + 2 * c + (q & 1);
             const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
-            umma_ts(tdV, tS + acol, sdesc_sw128(sO + kk * 2048, PANEL, 1024), idesc_dv, (n > 0 || kk > 0) ? 1u : 0u);
+            umma_ts(tdV, tS + acol, sdesc_step(odm, kk * 2048), idesc_dv, kk > 0 ? 1u : acc0);
           }
         }
         if (!ok) break;
@@ -406,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           for (int q = 0; q < 4; ++q) {
             const int kk = 4 * (q >> 1) + 2 * c + (q & 1);
             const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
-            umma_ts(tdK, tdP + acol, sdesc_sw128(sQ + kk * 2048, PANEL, 1024), idesc_dk, (n > 0 || kk > 0) ? 1u : 0u);
+            umma_ts(tdK, tdP + acol, sdesc_step(qdm, kk * 2048), idesc_dk, kk > 0 ? 1u : acc0);
           }
         }
         if (!ok) break;
@@ -415,8 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         // 64-column panels LBO apart
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          umma_ss(tdP, sdesc_sw128(sDS + kk * 2048, PANEL, 1024), sdesc_sw128(sK + kk * 2048, PANEL, 1024),
-                  idesc_dq, kk > 0 ? 1u : 0u);
+          umma_ss(tdP, sdesc_step(sdm, kk * 2048), sdesc_step(kdm, kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars->q_empty[st]);
         umma_commit(&bars->dq_full);

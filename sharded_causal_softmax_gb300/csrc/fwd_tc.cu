@@ -246,11 +246,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         if (!mbar_wait(&bars->k_full[ks], (j / KST) & 1, abort, status)) return false;
         tc_fence_after();
         const uint32_t tS = tmem + (j % SBUF) * 128;
-        const uint32_t kbase = sK + ks * L::TILE;
+        const uint64_t kd = sdesc_sw128(sK + ks * L::TILE, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;   // K-major: panel, then 32 B steps
-          umma_ts(tS, tQ + kk * 8, sdesc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          umma_ts(tS, tQ + kk * 8, sdesc_step(kd, off), idesc_qk, kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars->s_full[j % SBUF]);
         umma_commit(&bars->k_empty[ks]);
@@ -264,12 +264,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         if (!mbar_wait(&bars->v_full[vs], (j / VST) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tP = tmem + (j % SBUF) * 128;
-        const uint32_t vbase = sV + vs * L::TILE;
+        const uint64_t vd = sdesc_sw128(sV + vs * L::TILE, PANEL, 1024);
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
         // keys [16kk, 16kk+16) of P live in warpgroup kk/4's packed columns
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          umma_ts(tO, tP + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_sw128(vbase + kk * 2048, PANEL, 1024), idesc_pv,
-                  (j > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tO, tP + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_step(vd, kk * 2048), idesc_pv, kk > 0 ? 1u : acc0);
         umma_commit(&bars->v_empty[vs]);
         umma_commit(&bars->pv_done[j & 1]);
         // S[j%3] is free once PV_j has read P_j (MMAs execute in order)

@@ -69,11 +69,12 @@ SCA_INLINE uint32_t chunk_off(int row, int c) {
 }
 
 // operand descriptors of k-step kk (16 elements of the contraction)
+// (the base descriptor is common to a loop's k-steps, which only add)
 SCA_INLINE uint64_t kmajor(uint32_t base, int kk) {   // tile rows = M or N, K along the row
-  return sdesc_sw128(base + (kk >> 2) * PANEL + (kk & 3) * 32, 16, 1024);
+  return sdesc_step(sdesc_sw128(base, 16, 1024), (kk >> 2) * PANEL + (kk & 3) * 32);
 }
 SCA_INLINE uint64_t mnmajor(uint32_t base, int kk) {  // tile rows = K, M or N along the row
-  return sdesc_sw128(base + kk * 2048, PANEL, 1024);
+  return sdesc_step(sdesc_sw128(base, PANEL, 1024), kk * 2048);
 }
 
 // x = hi + lo, both bf16 (round to nearest even), for a pair

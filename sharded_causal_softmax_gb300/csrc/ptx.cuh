@@ -205,6 +205,12 @@ SCA_INLINE uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
+// The descriptor of addr + bytes from that of addr: the address field is
+// addr >> 4 in the low 14 bits, and shared-memory addresses stay below
+// 2^18, so adding never carries out of it.  Lets an MMA loop build one
+// descriptor per operand and step it with a constant add.
+SCA_INLINE uint64_t sdesc_step(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // --- tensor memory loads / stores, 32 lanes x 32 bit, 32 columns per call.
 
 #define SCA_R8(a, i) "=r"(a[i]), "=r"(a[i + 1]), "=r"(a[i + 2]), "=r"(a[i + 3]), \
