@@ -324,6 +324,15 @@ int lasp_bwd(const void* q, const void* k, const void* v, const void* dout, int 
 int lasp_fwd_noalloc(const void* q, const void* k, const void* v, int dtype, float* o, int64_t BH, int64_t S,
                      int D, int P, float scale, void* stream);
 
+/* sca_selftest_wait_timeout - runs, on one thread, the bounded mbarrier
+ * wait every tensor-core kernel uses, on a barrier nothing completes.  After
+ * the library's wait limit (2 s) it gives up and records SCA_ERR_TIMEOUT in
+ * *dev_status, exactly as a kernel whose pipeline stalled would; the kernel
+ * returns and the context stays usable.  For testing the failure path; the
+ * pages have no counterpart.  Errors: SCA_ERR_ARG (NULL status word),
+ * SCA_ERR_CUDA. */
+int sca_selftest_wait_timeout(int* dev_status, void* stream);
+
 /* Message of the last non-OK return on the calling thread ("" if none). */
 const char* sca_last_error(void);
 

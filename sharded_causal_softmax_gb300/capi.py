@@ -32,7 +32,8 @@ SCA_MAX_ITEMS = 32
 
 EXPORTED = ("attn_fwd_shard", "attn_merge_lse", "zigzag_permute", "ring_stage_block", "ring_stage_segments",
             "attn_bwd_shard", "attn_bwd_delta", "lasp_block_states", "lasp_scan", "lasp_exchange", "lasp_fwd",
-            "lasp_bwd", "lasp_fwd_noalloc", "sca_last_error", "sca_read_status", "sca_version")
+            "lasp_bwd", "lasp_fwd_noalloc", "sca_selftest_wait_timeout", "sca_last_error", "sca_read_status",
+            "sca_version")
 SCA_LASP_BLOCK_F32 = 64    # blocks of the fp32 CUDA-core kernels
 SCA_LASP_BLOCK_TC = 128    # tensor-core kernels (bf16, D = 128): blocks of a multiple of this, up to 4096
 
@@ -95,6 +96,7 @@ def _load():
                              c_void_p]),
         "lasp_fwd_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_int64, c_int64, c_int, c_int,
                                      c_float, c_void_p]),
+        "sca_selftest_wait_timeout": (c_int, [c_void_p, c_void_p]),
         "sca_last_error": (c_char_p, []),
         "sca_read_status": (c_int, [c_void_p, c_void_p]),
         "sca_version": (c_int, []),
@@ -189,6 +191,10 @@ def lasp_bwd(q: int, k: int, v: int, dout: int, dtype: int, st_fwd: int, in_fwd:
              stream: int) -> int:
     return check(lib().lasp_bwd(q, k, v, dout, dtype, st_fwd, in_fwd, st_bwd, in_bwd, dq, dk, dv, BH, S, D, P,
                                 block, scale, dev_status, stream))
+
+
+def sca_selftest_wait_timeout(dev_status: int, stream: int) -> int:
+    return check(lib().sca_selftest_wait_timeout(dev_status, stream))
 
 
 def lasp_fwd_noalloc(q: int, k: int, v: int, dtype: int, o: int, BH: int, S: int, D: int, P: int, scale: float,

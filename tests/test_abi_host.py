@@ -255,3 +255,6 @@ def test_lasp_rejects_bad_arguments(lib):
     assert lib.lasp_fwd(A, A, A, 7, A, A, A, 2, 1024, 128, 4, F, 0.1, None, None) == capi.SCA_ERR_ARG  # dtype
     assert lib.lasp_bwd(A, A, A, A, bf, A, A, A, A, A, A, None, 2, 1024, 128, 4, T, 0.1, None, None) == \
         capi.SCA_ERR_ARG
+
+def test_selftest_wait_rejects_null_status(lib):
+    assert lib.sca_selftest_wait_timeout(None, None) == capi.SCA_ERR_ARG
