@@ -31,9 +31,12 @@ def sca():
     ("bf16", "simt", "zigzag", 4, 1, 4, 2, 1024, {}),
     ("f32", "auto", "contiguous", 2, 1, 4, 2, 256, {}),
     ("f32", "auto", "zigzag", 2, 1, 4, 2, 256, {"schedule": "fused"}),
+    ("bf16", "auto", "zigzag", 2, 1, 4, 1, 1024, {"D": 64}),                 # fp16 P/V/dO variant at D = 64
+    ("bf16", "auto", "contiguous", 2, 1, 8, 2, 640, {"D": 64, "schedule": "fused"}),
 ])
 def test_gqa_small_full_oracle(sca, dtype, algo, layout, P, G, H, Hkv, S, kw):
-    B, D = 1, 128 if dtype == "bf16" else 64
+    kw = dict(kw)
+    B, D = 1, kw.pop("D", 128 if dtype == "bf16" else 64)
     q, k, v, do = seeded_inputs.make_inputs(B, H, S, D, dtype, seed=300 + H + Hkv, with_do=True, kv_heads=Hkv)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     a = sca.capi.SCA_ALGO_SIMT if algo == "simt" else sca.capi.SCA_ALGO_AUTO
