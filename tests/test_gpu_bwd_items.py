@@ -167,3 +167,20 @@ def test_long_block_tensor_cores_vs_fp32_kernel(sca):
     for name, x, y in zip(("dq", "dk", "dv"), a, b):
         assert_close(name + " tc vs simt", x, y.double().numpy(), (1e-2, 1e-3))
     check(s, a, dtype, D)
+
+
+@pytest.mark.parametrize("accumulate", [0, 1])
+def test_most_items_one_call(sca, accumulate):
+    # SCA_MAX_ITEMS items in one call (the tensor-core launcher splits them
+    # into launches of 28): every (query shard, key block) pair of P = 4
+    # zigzag shards twice over, each with its own inputs and gradients
+    D, P, c = 128, 4, 64
+    specs = []
+    for n in range(sca.capi.SCA_MAX_ITEMS):
+        r, j = (n // P) % P, n % P
+        qs = (2, c, (r * c, (2 * P - 1 - r) * c))
+        ks = (2, c, (j * c, (2 * P - 1 - j) * c))
+        specs.append(Spec(1, 1, D, 2 * c, 2 * c, qs, ks, torch.bfloat16, 1000 + 10 * n))
+    got = run(sca, specs, torch.bfloat16, sca.capi.SCA_ALGO_TC, D, 1, 1, accumulate=accumulate)
+    for spec, g in zip(specs, got):
+        check(spec, g, torch.bfloat16, D, accumulate=accumulate)

@@ -187,3 +187,20 @@ def test_tensor_cores_agree_with_fp32_kernel(sca):
     b = run_items(sca, [(q, k, v, qs, ks)], dtype, sca.capi.SCA_ALGO_SIMT, D, H=4)[0]
     assert_close("o tc vs simt", a[0], b[0].double().numpy(), (1e-2, 1e-3))
     assert_close("lse tc vs simt", a[1], b[1].double().numpy(), (1e-2, 1e-3))
+
+
+@pytest.mark.parametrize("algo,dtype", [("tc", torch.bfloat16), ("simt", torch.float32)])
+def test_most_items_one_launch(sca, algo, dtype):
+    # SCA_MAX_ITEMS items in one call: every (query shard, key block) pair of
+    # P = 4 zigzag shards twice over, with different inputs
+    D, P, c = 128 if dtype == torch.bfloat16 else 64, 4, 64
+    specs = []
+    for n in range(sca.capi.SCA_MAX_ITEMS):
+        r, j = (n // P) % P, n % P
+        qs = (2, c, (r * c, (2 * P - 1 - r) * c))
+        ks = (2, c, (j * c, (2 * P - 1 - j) * c))
+        specs.append((make((1, 1, 2 * c, D), dtype, 100 + n), make((1, 1, 2 * c, D), dtype, 200 + n),
+                      make((1, 1, 2 * c, D), dtype, 300 + n), qs, ks))
+    got = run_items(sca, specs, dtype, _algo(sca, algo), D, H=1)
+    for (q, k, v, qs, ks), g in zip(specs, got):
+        check_item(q, k, v, qs, ks, g, dtype, D)
