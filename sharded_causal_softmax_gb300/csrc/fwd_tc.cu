@@ -60,6 +60,7 @@ struct Bars {
   uint64_t v_full[VST], v_empty[VST];
   uint64_t s_full[SBUF], p_full[SBUF];
   uint64_t pv_done[2];   // PV_j completes phase j/2 of pv_done[j%2]
+  uint64_t o_full;       // every PV has completed
   uint64_t red_full[2];  // both warpgroups published their row maxima (per tile parity)
   uint64_t lsum_full;    // both warpgroups published their row sums
   uint64_t drain;
@@ -102,6 +103,32 @@ SCA_INLINE TileInfo tile_info(const ItemGeom& g, int kt, bool causal, int64_t qm
   t.full = t.nk == BN && (!causal || kmax <= qmin);
   return t;
 }
+
+// Walks the visible tiles like TileCursor, and also returns whether each is
+// fully visible: both flags come from one pair of ballots per 32 tiles.
+struct InfoCursor {
+  int base = -32;
+  uint32_t mask = 0, fmask = 0;
+  template <typename Info>
+  __device__ __forceinline__ int next(int n, int lane, const Info& info, bool& full) {
+    while (mask == 0) {
+      base += 32;
+      if (base >= n) return -1;
+      bool vis = false, fl = false;
+      if (base + lane < n) {
+        const TileInfo t = info(base + lane);
+        vis = t.visible;
+        fl = t.full;
+      }
+      mask = __ballot_sync(0xffffffffu, vis);
+      fmask = __ballot_sync(0xffffffffu, fl);
+    }
+    const int b = __ffs(mask) - 1;
+    full = (fmask >> b) & 1u;
+    mask &= mask - 1;
+    return base + b;
+  }
+};
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ TcArgs ta) {
@@ -158,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     }
     mbar_init(&bars->pv_done[0], 1);
     mbar_init(&bars->pv_done[1], 1);
+    mbar_init(&bars->o_full, 1);
     mbar_init(&bars->red_full[0], 2 * BM);
     mbar_init(&bars->red_full[1], 2 * BM);
     mbar_init(&bars->lsum_full, 2 * BM);
@@ -275,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         // S[j%3] is free once PV_j has read P_j (MMAs execute in order)
         if (j + SBUF < n_vis) ok = issue_qk(j + SBUF);
       }
+      if (ok) umma_commit(&bars->o_full);
       if (!ok) {  // make sure no MMA still writes tensor memory
         umma_commit(&bars->drain);
         mbar_wait_drain(&bars->drain, 0);
@@ -311,14 +340,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     }
     tc_fence_before();
     mbar_arrive(&bars->q_tmem);
-    TileCursor cur;
-    for (int kt; ok && (kt = cur.next(nkt, lane, kvis)) >= 0;) {
-      const TileInfo ti = tile_info(gm, kt, causal, qmin, qmax);
+    InfoCursor cur;
+    auto kinfo = [&](int t) { return tile_info(gm, t, causal, qmin, qmax); };
+    bool full_tile = false;
+    for (int kt; ok && (kt = cur.next(nkt, lane, kinfo, full_tile)) >= 0;) {
+      TileInfo ti;
+      ti.full = full_tile;
+      ti.k0 = static_cast<int64_t>(kt) * BN;
+      ti.nk = static_cast<int>(min64(BN, gm.Skv - ti.k0));
       const int sb = n % SBUF;
-      // observe PV_{n-2}: each pv_done barrier is then at most one phase ahead
-      // of the phase this thread waits for next (a parity wait needs that)
-      bool w = n < 2 || mbar_wait(&bars->pv_done[n & 1], ((n - 2) >> 1) & 1, abort, status);
-      w = w && mbar_wait(&bars->s_full[sb], (n / SBUF) & 1, abort, status);
+      bool w = mbar_wait(&bars->s_full[sb], (n / SBUF) & 1, abort, status);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[64];
@@ -354,15 +385,22 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       auto exps = [&](float m_ref) {
         const float msub = (m_ref == -INFINITY) ? 0.f : m_ref;
         const float2 nm2 = make_float2(-msub, -msub);
-        sum = make_float2(0.f, 0.f);
+        // two partial sums, two column pairs per step: the sum's add chain
+        // sat on the tile's critical path (this order measured 5% faster)
+        float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < 32; i += 2) {
           // two columns per packed instruction: p = 2^(s * scale * log2e - m)
           const float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), sc2, nm2);
+          const float2 y = ffma2(make_float2(s[2 * i + 2], s[2 * i + 3]), sc2, nm2);
           const float2 p = make_float2(ex2(x.x), ex2(x.y));
-          sum = fadd2(sum, p);
+          const float2 q = make_float2(ex2(y.x), ex2(y.y));
+          s0 = fadd2(s0, p);
+          s1 = fadd2(s1, q);
           pk[i] = pack_bf16x2(p.x, p.y);
+          pk[i + 1] = pack_bf16x2(q.x, q.y);
         }
+        sum = fadd2(s0, s1);
       };
       exps(m_used);
       w = mbar_wait(&bars->red_full[n & 1], (n >> 1) & 1, abort, status);
@@ -375,6 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         if (need) m_used = m_new;
         l *= alpha;
         if (n > 0) {
+          // S_n is complete, so QK_n and the PV_{n-2} issued before it are:
+          // the phase this parity names on pv_done[(n-1)%2] is PV_{n-1}'s
           const bool w1 = mbar_wait(&bars->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort, status);
           if (!__all_sync(0xffffffffu, w1)) { ok = false; break; }
           tc_fence_after();
@@ -400,9 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       mbar_arrive(&bars->p_full[sb]);
       ++n;
     }
-    // epilogue: observe PV_{n-2}, then PV_{n-1}
-    if (ok && n >= 2) ok = mbar_wait(&bars->pv_done[n & 1], ((n - 2) >> 1) & 1, abort, status);
-    if (ok && n >= 1) ok = mbar_wait(&bars->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort, status);
+    // epilogue: every PV has completed
+    if (ok) ok = mbar_wait(&bars->o_full, 0, abort, status);
     bars->lsum[g][row] = l;
     mbar_arrive(&bars->lsum_full);
     if (ok) ok = mbar_wait(&bars->lsum_full, 0, abort, status);
