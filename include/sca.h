@@ -105,7 +105,17 @@ typedef struct {
    * head h reads key/value head h / (H / kv_heads); k, v (and dk, dv, which
    * then sum over the group) have kv_heads heads in the kv / dkv views. */
   int32_t kv_heads;
+  /* Backward, bf16 on the tensor cores only (SCA_ERR_ARG otherwise): inputs
+   * the caller has already converted to fp16 with cast_bf16_to_f16, so the
+   * kernel skips converting them tile by tile.  Bit 0 (SCA_F16_Q): each
+   * item's q holds fp16.  Bit 1 (SCA_F16_DOUT): each item's dout holds
+   * fp16; only with grouped key/value heads (0 < kv_heads < H), the one
+   * case where the backward runs dP and dV as fp16 products.  0: bf16. */
+  int32_t f16_inputs;
 } sca_attn_dims;
+
+#define SCA_F16_Q 1
+#define SCA_F16_DOUT 2
 
 /* One (query shard, key/value block) work item of the forward. */
 typedef struct {
@@ -223,7 +233,9 @@ typedef struct {
  * products (q and k are converted to fp16 inside the kernel, dS is rounded
  * to fp16), and with grouped-query heads dP and dV too (v and dout
  * converted, P rounded to fp16): |q|, |k| (and |v|, |dout|) must stay below
- * 65504.  dq is summed over key tiles
+ * 65504.  dims->f16_inputs lets the caller pass q (and, grouped, dout)
+ * already converted by cast_bf16_to_f16: the same values, converted once
+ * per call instead of once per key tile that reads them.  dq is summed over key tiles
  * by fp32 reduce-adds in no fixed order, so it is reproducible only up to
  * rounding order; dk and dv have one writer per row.  The tensor-core path
  * needs dq, dk, dv rows 16-byte aligned with strides that are multiples of
@@ -231,6 +243,16 @@ typedef struct {
  * contiguous (dims->o.s == D).  Errors as attn_fwd_shard. */
 int attn_bwd_shard(const sca_bwd_item* items, int n_items, const sca_attn_dims* dims,
                    int* dev_status, void* stream);
+
+/* cast_bf16_to_f16 - dst[i] = src[i] rounded from bf16 to fp16 (round to
+ * nearest even), for i < n: exact for |x| in [2^-14, 65504], fp16
+ * subnormals below, +-inf above.  No counterpart on the pages: the staging
+ * step that gives attn_bwd_shard (dims->f16_inputs) its fp16 queries once
+ * per call.  src and dst may not overlap; n a multiple of 8 and both
+ * pointers 16-byte aligned (whole 16-byte vectors).
+ * Errors: SCA_ERR_ARG for NULL pointers, n < 0, n % 8 != 0, overlap;
+ * SCA_ERR_ALIGN for misaligned pointers. */
+int cast_bf16_to_f16(const void* src, void* dst, int64_t n, void* stream);
 
 /* attn_bwd_delta - delta_i = sum_d dO_id * O_id for `rows` contiguous rows:
  * o fp32 [rows, D], dout [rows, D] of dtype `dout_dtype`, delta fp32 [rows].

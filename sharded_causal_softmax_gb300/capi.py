@@ -29,11 +29,13 @@ SCA_ALGO_AUTO = 0
 SCA_ALGO_SIMT = 1
 SCA_ALGO_TC = 2
 SCA_MAX_ITEMS = 32
+SCA_F16_Q = 1
+SCA_F16_DOUT = 2
 
 EXPORTED = ("attn_fwd_shard", "attn_merge_lse", "zigzag_permute", "ring_stage_block", "ring_stage_segments",
-            "attn_bwd_shard", "attn_bwd_delta", "lasp_block_states", "lasp_scan", "lasp_exchange", "lasp_fwd",
-            "lasp_bwd", "lasp_fwd_noalloc", "sca_selftest_wait_timeout", "sca_last_error", "sca_read_status",
-            "sca_version")
+            "attn_bwd_shard", "attn_bwd_delta", "cast_bf16_to_f16", "lasp_block_states", "lasp_scan",
+            "lasp_exchange", "lasp_fwd", "lasp_bwd", "lasp_fwd_noalloc", "sca_selftest_wait_timeout",
+            "sca_last_error", "sca_read_status", "sca_version")
 SCA_LASP_BLOCK_F32 = 64    # blocks of the fp32 CUDA-core kernels
 SCA_LASP_BLOCK_TC = 128    # tensor-core kernels (bf16, D = 128): blocks of a multiple of this, up to 4096
 
@@ -56,7 +58,8 @@ class sca_attn_dims(ctypes.Structure):
     _fields_ = [("B", c_int32), ("H", c_int32), ("D", c_int32), ("dtype", c_int32), ("causal", c_int32),
                 ("algo", c_int32), ("scale", c_float), ("accumulate", c_int32), ("q", sca_view), ("kv", sca_view),
                 ("o", sca_view), ("dkv", sca_view), ("lse_b", c_int64), ("lse_h", c_int64),
-                ("q_by_pos", c_int32), ("kv_by_pos", c_int32), ("dkv_by_pos", c_int32), ("kv_heads", c_int32)]
+                ("q_by_pos", c_int32), ("kv_by_pos", c_int32), ("dkv_by_pos", c_int32), ("kv_heads", c_int32),
+                ("f16_inputs", c_int32)]
 
 
 class sca_fwd_item(ctypes.Structure):
@@ -85,6 +88,7 @@ def _load():
         "ring_stage_segments": (c_int, [c_void_p, c_void_p, c_int64, c_int64, POINTER(sca_segs), c_int64, c_void_p]),
         "attn_bwd_shard": (c_int, [POINTER(sca_bwd_item), c_int, POINTER(sca_attn_dims), c_void_p, c_void_p]),
         "attn_bwd_delta": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int64, c_int, c_void_p]),
+        "cast_bf16_to_f16": (c_int, [c_void_p, c_void_p, c_int64, c_void_p]),
         "lasp_block_states": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int64, c_int64, c_int, c_int, c_void_p,
                                       c_void_p]),
         "lasp_scan": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int, c_int, c_int, c_int, c_void_p]),
@@ -204,6 +208,10 @@ def lasp_fwd_noalloc(q: int, k: int, v: int, dtype: int, o: int, BH: int, S: int
 
 def attn_bwd_delta(o: int, dout: int, dout_dtype: int, delta: int, rows: int, D: int, stream: int) -> int:
     return check(lib().attn_bwd_delta(o, dout, dout_dtype, delta, rows, D, stream))
+
+
+def cast_bf16_to_f16(src: int, dst: int, n: int, stream: int) -> int:
+    return check(lib().cast_bf16_to_f16(src, dst, n, stream))
 
 
 def sca_read_status(dev_status: int, stream: int) -> int:

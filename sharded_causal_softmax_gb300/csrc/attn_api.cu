@@ -48,6 +48,12 @@ static int check_dims(const sca_attn_dims* d, bool bwd) {
   SCA_REQUIRE(bwd || d->dkv_by_pos == 0, SCA_ERR_ARG, "dkv_by_pos applies to the backward only");
   SCA_REQUIRE(d->kv_heads >= 0 && (d->kv_heads == 0 || d->H % d->kv_heads == 0), SCA_ERR_ARG,
               "kv_heads=%d must be 0 or divide H=%d", d->kv_heads, d->H);
+  SCA_REQUIRE((d->f16_inputs & ~(SCA_F16_Q | SCA_F16_DOUT)) == 0, SCA_ERR_ARG, "f16_inputs=%d has unknown bits",
+              d->f16_inputs);
+  SCA_REQUIRE(d->f16_inputs == 0 || (bwd && d->dtype == SCA_BF16 && d->algo != SCA_ALGO_SIMT), SCA_ERR_ARG,
+              "f16_inputs applies to the bf16 tensor-core backward only");
+  SCA_REQUIRE(!(d->f16_inputs & SCA_F16_DOUT) || (d->kv_heads > 0 && d->kv_heads < d->H), SCA_ERR_ARG,
+              "f16_inputs: fp16 dout needs grouped key/value heads (0 < kv_heads < H)");
   return SCA_OK;
 }
 
@@ -84,6 +90,7 @@ static void fill_common(AttnArgs& a, const sca_attn_dims* d, int n_items, int* d
   a.dkv_by_pos = d->dkv_by_pos;
   a.Hkv = d->kv_heads > 0 ? d->kv_heads : d->H;
   a.group = d->H / a.Hkv;
+  a.f16_inputs = d->f16_inputs;
 }
 
 static bool use_tc(const sca_attn_dims* d) {

@@ -446,9 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     }
     mbar_arrive(&bars->k_conv);
     // Q of the j-th visible tile to fp16, once its TMA load has landed
+    // (unless the caller passed fp16 queries)
+    const bool q_is_f16 = (a.f16_inputs & SCA_F16_Q) != 0, do_is_f16 = (a.f16_inputs & SCA_F16_DOUT) != 0;
     auto convert_q = [&](int j) -> bool {
       const bool w = __all_sync(0xffffffffu, mbar_wait(&bars->q_full[j & 1], (j >> 1) & 1, abort, status));
-      if (w) {
+      if (w && !q_is_f16) {
         smem_bf16_to_f16<L::TILE, 256>(smem + L::Q_OFF + (j & 1) * L::TILE, threadIdx.x);
         fence_async_smem();
       }
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     // dO of the j-th visible tile to fp16 (F16PV only)
     auto convert_do = [&](int j) -> bool {
       const bool w = __all_sync(0xffffffffu, mbar_wait(&bars->do_full[j & 1], (j >> 1) & 1, abort, status));
-      if (w) {
+      if (w && !do_is_f16) {
         smem_bf16_to_f16<L::TILE, 256>(smem + L::DO_OFF + (j & 1) * L::TILE, threadIdx.x);
         fence_async_smem();
       }
@@ -724,10 +726,14 @@ cudaError_t tc_backward(AttnArgs& a, cudaStream_t st) {
       cudaError_t e;
       const int64_t qr = slab_extent(it.qs, a.q_by_pos), kr = slab_extent(it.ks, a.kv_by_pos),
                     dkr = slab_extent(it.ks, a.dkv_by_pos);
-      if ((e = make_tmap_bf16(&m[0], it.q, a.D, qr, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
+      if ((e = (a.f16_inputs & SCA_F16_Q ? make_tmap_f16 : make_tmap_bf16)(&m[0], it.q, a.D, qr, a.H, a.B, a.q, 64,
+                                                                            BM)) != cudaSuccess)
+        return e;
       if ((e = make_tmap_bf16(&m[1], it.k, a.D, kr, a.Hkv, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
       if ((e = make_tmap_bf16(&m[2], it.v, a.D, kr, a.Hkv, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
-      if ((e = make_tmap_bf16(&m[3], it.dout, a.D, qr, a.H, a.B, a.q, 64, BM)) != cudaSuccess) return e;
+      if ((e = (a.f16_inputs & SCA_F16_DOUT ? make_tmap_f16 : make_tmap_bf16)(&m[3], it.dout, a.D, qr, a.H, a.B, a.q,
+                                                                               64, BM)) != cudaSuccess)
+        return e;
       if ((e = make_tmap_f32(&m[4], it.o, a.D, qr, a.H, a.B, a.o, 32, BM)) != cudaSuccess) return e;
       if ((e = make_tmap_f32(&m[5], it.dk, a.D, dkr, a.Hkv, a.B, a.dkv, 32, BN)) != cudaSuccess) return e;
       if ((e = make_tmap_f32(&m[6], it.dv, a.D, dkr, a.Hkv, a.B, a.dkv, 32, BN)) != cudaSuccess) return e;

@@ -1,7 +1,9 @@
-// HBM-bound kernels: zigzag permute, ring staging copy, exact lse merge and
-// the backward's delta = rowsum(dO * O).  All move 16-byte vectors where the
-// layout allows; none allocates.
+// HBM-bound kernels: zigzag permute, ring staging copy, exact lse merge, the
+// backward's delta = rowsum(dO * O) and its bf16 -> fp16 input cast.  All
+// move 16-byte vectors where the layout allows; none allocates.
 #include <cmath>
+
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "host_common.h"
@@ -165,6 +167,30 @@ __global__ void __launch_bounds__(kMergeThreads) delta_kernel(const float* __res
   }
 }
 
+// ------------------------------------------------------- bf16 -> fp16 cast
+//
+// Eight values per 16-byte vector; grid-stride over the vectors.  Each bf16
+// is widened exactly to fp32 (its bits in the high half) and rounded to fp16
+// by the hardware conversion.
+
+constexpr int kCastThreads = 256;
+
+__global__ void __launch_bounds__(kCastThreads) cast_bf16_f16_kernel(const uint4* __restrict__ src,
+                                                                     uint4* __restrict__ dst, int64_t nvec) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(kCastThreads) + threadIdx.x; i < nvec;
+       i += static_cast<int64_t>(gridDim.x) * kCastThreads) {
+    const uint4 v = src[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u));
+      o[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 static int grid_for(int64_t work_items, int per_block) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -184,6 +210,19 @@ static bool overlap(const void* a, int64_t a_bytes, const void* b, int64_t b_byt
 }  // namespace sca
 
 using namespace sca;
+
+extern "C" int cast_bf16_to_f16(const void* src, void* dst, int64_t n, void* stream) {
+  SCA_REQUIRE(src && dst, SCA_ERR_ARG, "cast_bf16_to_f16: NULL pointer");
+  SCA_REQUIRE(n >= 0 && n % 8 == 0, SCA_ERR_ARG, "cast_bf16_to_f16: n=%lld must be a non-negative multiple of 8",
+              static_cast<long long>(n));
+  SCA_REQUIRE(aligned(src, 16) && aligned(dst, 16), SCA_ERR_ALIGN, "cast_bf16_to_f16: pointers not 16-byte aligned");
+  SCA_REQUIRE(!overlap(src, 2 * n, dst, 2 * n), SCA_ERR_ARG, "cast_bf16_to_f16: src and dst overlap");
+  if (n == 0) return SCA_OK;
+  const int64_t nvec = n / 8;
+  cast_bf16_f16_kernel<<<grid_for(nvec, kCastThreads * 4), kCastThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(src), static_cast<uint4*>(dst), nvec);
+  return cuda_status(cudaGetLastError(), "cast_bf16_to_f16 launch");
+}
 
 extern "C" int zigzag_permute(const void* src, void* dst, int64_t outer, int64_t S, int64_t row_bytes, int P,
                               int inverse, void* stream) {

@@ -47,6 +47,11 @@ cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, int D, int64_t ro
   return make_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, D, rows, H, B, v, box_d, box_rows);
 }
 
+cudaError_t make_tmap_f16(CUtensorMap* map, const void* base, int D, int64_t rows, int H, int B,
+                          const View& v, int box_d, int box_rows) {
+  return make_tmap(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, D, rows, H, B, v, box_d, box_rows);
+}
+
 cudaError_t make_tmap_f32(CUtensorMap* map, const void* base, int D, int64_t rows, int H, int B,
                           const View& v, int box_d, int box_rows) {
   return make_tmap(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, D, rows, H, B, v, box_d, box_rows);

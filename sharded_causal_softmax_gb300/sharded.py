@@ -82,7 +82,7 @@ class ShardedCausalAttention:
 
     def __init__(self, B, H, S, D, P, layout="zigzag", dtype=torch.bfloat16, head_groups=1,
                  schedule="ring", scale=None, causal=True, algo=capi.SCA_ALGO_AUTO, backward=False,
-                 bf16_out=False, device=None, addressing="auto", kv_heads=None):
+                 bf16_out=False, device=None, addressing="auto", kv_heads=None, f16_staging=True):
         if layout not in ("zigzag", "contiguous"):
             raise ValueError(f"layout {layout!r}")
         if schedule not in ("ring", "direct", "fused"):
@@ -144,6 +144,14 @@ class ShardedCausalAttention:
             self.dq_p = z(B, H, S, D) if self.perm else None
             self.dk_p = z(B, Hkv, S, D) if self.perm else None
             self.dv_p = z(B, Hkv, S, D) if self.perm else None
+        # the tensor-core backward runs S, dK, dQ (and, grouped, dP, dV) as
+        # fp16 products: its fp16 queries (and grouped dO) are cast once per
+        # backward here rather than tile by tile in every key-tile CTA
+        self.f16_in = 0
+        if backward and f16_staging and dtype == torch.bfloat16 and algo != capi.SCA_ALGO_SIMT:
+            self.f16_in = capi.SCA_F16_Q | (capi.SCA_F16_DOUT if Hkv < H else 0)
+        self.q16 = z(B, H, S, D, dt=torch.float16) if self.f16_in else None
+        self.do16 = z(B, H, S, D, dt=torch.float16) if self.f16_in & capi.SCA_F16_DOUT else None
         self.copy_stream = torch.cuda.Stream(device=dev) if ring else None
         self.ev_ready = torch.cuda.Event()
         self.ev_staged = [torch.cuda.Event() for _ in range(P)]
@@ -209,6 +217,7 @@ class ShardedCausalAttention:
         d.dkv = capi.view(self.Hkv * S * D, S * D, D)
         d.lse_b, d.lse_h = H * S, S
         d.q_by_pos, d.kv_by_pos, d.dkv_by_pos = int(q_by_pos), int(kv_by_pos), int(dkv_by_pos)
+        d.f16_inputs = self.f16_in if backward else 0
         return d
 
     def _home_kv_view(self):
@@ -378,6 +387,7 @@ class ShardedCausalAttention:
         self.launches += 1
         self.kernels += 1
         if self.schedule == "fused":
+            q, do = self._cast_f16(q, do, stream)
             return self._backward_fused(do, q, k, v, stream)
         if self.perm:
             self._permute(do, self.dop, D * eb, 0, stream)
@@ -390,6 +400,7 @@ class ShardedCausalAttention:
             qh, kh, vh, doh = q, k, v, do
             lse_h, dl_h = self.lse, self.delta
             dq, dk, dv = self.dq, self.dk, self.dv
+        qh, doh = self._cast_f16(qh, doh, stream)
         st_ptr = _ptr(self.status)
 
         def step(t, kv_ptrs, kv_view, home):
@@ -422,6 +433,21 @@ class ShardedCausalAttention:
             self._permute(dk, self.dk, D * 4, 1, stream)
             self._permute(dv, self.dv, D * 4, 1, stream)
         return self.dq, self.dk, self.dv
+
+    def _cast_f16(self, q, do, stream):
+        """The backward's query (and grouped dO) tensors: fp16 copies when the
+        plan stages them, else the inputs themselves."""
+        if self.f16_in & capi.SCA_F16_Q:
+            capi.cast_bf16_to_f16(_ptr(q), _ptr(self.q16), q.numel(), stream)
+            q = self.q16
+            self.launches += 1
+            self.kernels += 1
+        if self.f16_in & capi.SCA_F16_DOUT:
+            capi.cast_bf16_to_f16(_ptr(do), _ptr(self.do16), do.numel(), stream)
+            do = self.do16
+            self.launches += 1
+            self.kernels += 1
+        return q, do
 
     def _backward_fused(self, do, q, k, v, stream):
         """Every shard in one launch: each head group is one item over the

@@ -198,6 +198,35 @@ def test_bwd_rejects_bad_arguments(lib):
     assert lib.attn_bwd_shard(arr, 1, ctypes.byref(_dims(dkv_by_pos=1)), None, None) == capi.SCA_ERR_UNSUPPORTED
     arr = (capi.sca_bwd_item * 1)(_bwd_item(delta=None))
     assert lib.attn_bwd_shard(arr, 1, ctypes.byref(_dims()), None, None) == capi.SCA_ERR_ARG
+
+
+@pytest.mark.parametrize("case", ["unknown_bit", "forward", "f32_inputs", "simt_algo", "dout_without_groups"])
+def test_f16_inputs_flag_rejected_outside_the_tensor_core_backward(lib, case):
+    bwd = (capi.sca_bwd_item * 1)(_bwd_item())
+    if case == "unknown_bit":
+        rc = lib.attn_bwd_shard(bwd, 1, ctypes.byref(_dims(f16_inputs=4)), None, None)
+    elif case == "forward":
+        rc = _fwd_rc(lib, [_item()], _dims(f16_inputs=capi.SCA_F16_Q))
+    elif case == "f32_inputs":
+        rc = lib.attn_bwd_shard(bwd, 1, ctypes.byref(_dims(f16_inputs=capi.SCA_F16_Q, dtype=capi.SCA_F32)),
+                                None, None)
+    elif case == "simt_algo":
+        rc = lib.attn_bwd_shard(bwd, 1, ctypes.byref(_dims(f16_inputs=capi.SCA_F16_Q, algo=capi.SCA_ALGO_SIMT)),
+                                None, None)
+    else:   # H = 2 query heads over 2 key/value heads: no groups, dO stays bf16
+        rc = lib.attn_bwd_shard(bwd, 1, ctypes.byref(_dims(f16_inputs=capi.SCA_F16_DOUT, kv_heads=2)), None, None)
+    assert rc == capi.SCA_ERR_ARG, (case, rc, capi.last_error())
+    assert "f16_inputs" in capi.last_error()
+
+
+def test_cast_rejects_bad_arguments(lib):
+    f = lib.cast_bf16_to_f16
+    assert f(None, A, 8, None) == capi.SCA_ERR_ARG
+    assert f(A, 2 * A, 12, None) == capi.SCA_ERR_ARG          # not whole 16-byte vectors
+    assert f(A, 2 * A, -8, None) == capi.SCA_ERR_ARG
+    assert f(A + 8, 2 * A, 8, None) == capi.SCA_ERR_ALIGN
+    assert f(A, A + 16, 64, None) == capi.SCA_ERR_ARG         # overlapping ranges
+    assert f(A, 2 * A, 0, None) == capi.SCA_OK                # nothing to do, no launch
     arr = (capi.sca_bwd_item * 1)(_bwd_item(dk=A + 4))
     assert lib.attn_bwd_shard(arr, 1, ctypes.byref(_dims()), None, None) == capi.SCA_ERR_ALIGN
     assert lib.attn_bwd_shard(arr, 0, ctypes.byref(_dims()), None, None) == capi.SCA_ERR_ARG
