@@ -90,7 +90,6 @@ static void fill_common(AttnArgs& a, const sca_attn_dims* d, int n_items, int* d
   a.dkv_by_pos = d->dkv_by_pos;
   a.Hkv = d->kv_heads > 0 ? d->kv_heads : d->H;
   a.group = d->H / a.Hkv;
-  a.f16_inputs = d->f16_inputs;
 }
 
 static bool use_tc(const sca_attn_dims* d) {
@@ -192,7 +191,7 @@ extern "C" int attn_bwd_shard(const sca_bwd_item* items, int n_items, const sca_
   cudaStream_t st = as_stream(stream);
   cudaError_t e;
   if (use_tc(dims)) {
-    e = tc_backward(a, st);
+    e = tc_backward(a, dims->f16_inputs, st);
     if (e == cudaErrorNotSupported)
       return fail(SCA_ERR_ALIGN, "attn_bwd_shard: layout not expressible as a TMA tensor map "
                                  "(or dq rows not contiguous in overwrite mode)");

@@ -108,6 +108,7 @@ struct TcArgs {
   // q, k, v, dO (bf16); dq, dk, dv (fp32, TMA reduce-add / store targets)
   CUtensorMap maps[kItemsPerLaunch][7];
   AttnArgs a;
+  int32_t f16_inputs;   // SCA_F16_Q / SCA_F16_DOUT: those inputs arrive as fp16
 };
 static_assert(sizeof(TcArgs) <= 32764, "kernel parameters");
 
@@ -447,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     mbar_arrive(&bars->k_conv);
     // Q of the j-th visible tile to fp16, once its TMA load has landed
     // (unless the caller passed fp16 queries)
-    const bool q_is_f16 = (a.f16_inputs & SCA_F16_Q) != 0, do_is_f16 = (a.f16_inputs & SCA_F16_DOUT) != 0;
+    const bool q_is_f16 = (ta.f16_inputs & SCA_F16_Q) != 0, do_is_f16 = (ta.f16_inputs & SCA_F16_DOUT) != 0;
     auto convert_q = [&](int j) -> bool {
       const bool w = __all_sync(0xffffffffu, mbar_wait(&bars->q_full[j & 1], (j >> 1) & 1, abort, status));
       if (w && !q_is_f16) {
@@ -683,7 +684,7 @@ static cudaError_t launch(TcArgs& ta, cudaStream_t st) {
 
 }  // namespace bwdtc
 
-cudaError_t tc_backward(AttnArgs& a, cudaStream_t st) {
+cudaError_t tc_backward(AttnArgs& a, int f16_inputs, cudaStream_t st) {
   using namespace bwdtc;
   static TcArgs ta;
   static std::mutex mu;
@@ -715,6 +716,7 @@ cudaError_t tc_backward(AttnArgs& a, cudaStream_t st) {
   for (int first = 0; first < a.n_items; first += kItemsPerLaunch) {
     const int cnt = a.n_items - first < kItemsPerLaunch ? a.n_items - first : kItemsPerLaunch;
     ta.a = a;
+    ta.f16_inputs = f16_inputs;
     ta.a.n_items = cnt;
     int64_t mt = 0;
     for (int i = 0; i < cnt; ++i) {
@@ -726,12 +728,12 @@ cudaError_t tc_backward(AttnArgs& a, cudaStream_t st) {
       cudaError_t e;
       const int64_t qr = slab_extent(it.qs, a.q_by_pos), kr = slab_extent(it.ks, a.kv_by_pos),
                     dkr = slab_extent(it.ks, a.dkv_by_pos);
-      if ((e = (a.f16_inputs & SCA_F16_Q ? make_tmap_f16 : make_tmap_bf16)(&m[0], it.q, a.D, qr, a.H, a.B, a.q, 64,
+      if ((e = (f16_inputs & SCA_F16_Q ? make_tmap_f16 : make_tmap_bf16)(&m[0], it.q, a.D, qr, a.H, a.B, a.q, 64,
                                                                             BM)) != cudaSuccess)
         return e;
       if ((e = make_tmap_bf16(&m[1], it.k, a.D, kr, a.Hkv, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
       if ((e = make_tmap_bf16(&m[2], it.v, a.D, kr, a.Hkv, a.B, a.kv, 64, BN)) != cudaSuccess) return e;
-      if ((e = (a.f16_inputs & SCA_F16_DOUT ? make_tmap_f16 : make_tmap_bf16)(&m[3], it.dout, a.D, qr, a.H, a.B, a.q,
+      if ((e = (f16_inputs & SCA_F16_DOUT ? make_tmap_f16 : make_tmap_bf16)(&m[3], it.dout, a.D, qr, a.H, a.B, a.q,
                                                                                64, BM)) != cudaSuccess)
         return e;
       if ((e = make_tmap_f32(&m[4], it.o, a.D, qr, a.H, a.B, a.o, 32, BM)) != cudaSuccess) return e;

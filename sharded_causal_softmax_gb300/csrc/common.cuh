@@ -144,7 +144,6 @@ struct AttnArgs {
   int32_t max_k_tiles;
   int32_t q_by_pos, kv_by_pos, dkv_by_pos;   // row addressing (see sca_attn_dims)
   int32_t Hkv, group;   // key/value heads; query heads per key/value head
-  int32_t f16_inputs;   // backward: SCA_F16_Q / SCA_F16_DOUT inputs already fp16
   int* status;
 };
 
