@@ -23,7 +23,9 @@ The schedule (host logic only; every byte is moved or computed by libsca):
   engine on a side stream into the spare one of two staging buffers while
   step t computes (the double buffer of the METP abstract, FITEE
   10.1631/FITEE.2400602).  The "direct" schedule reads every block from its
-  home rows (the K/V all-gather reading of the TSP page).
+  home rows (the K/V all-gather reading of the TSP page); its forward
+  partials of all P steps are independent and go out together, up to
+  SCA_MAX_ITEMS (query shard, block) items per launch.
 * Merge: the P partials of every row are combined exactly by log-sum-exp
   rescaling (``attn_merge_lse``), fused with the inverse permute when the
   partials are shard-major.
@@ -312,7 +314,7 @@ class ShardedCausalAttention:
         eb = self.eb
         st_ptr = _ptr(self.status)
 
-        def step(t, kv_ptrs, kv_view, home):
+        def step_items(t, kv_ptrs):
             items = []
             for g in range(self.G):
                 for r in range(P):
@@ -325,12 +327,28 @@ class ShardedCausalAttention:
                     it.q_pos = shard_segs(S, P, self.layout, r)
                     it.kv_pos = shard_segs(S, P, self.layout, ring_block(r, t, P))
                     items.append(it)
+            return items
+
+        def step(t, kv_ptrs, kv_view, home):
             dims = self._dims(kv_view, q_by_pos=self.pos, kv_by_pos=self.pos and home)
-            capi.attn_fwd_shard(items, dims, st_ptr, stream)
+            capi.attn_fwd_shard(step_items(t, kv_ptrs), dims, st_ptr, stream)
             self.launches += 1
             self.kernels += 1
 
-        self._ring(kh, vh, step)
+        if self.schedule == "direct":
+            # every block is read from its home rows (the all-gather reading),
+            # so the partials of all P steps are independent: they go out
+            # together, up to SCA_MAX_ITEMS items per launch
+            items = []
+            for t in range(P):
+                items += step_items(t, lambda g, r, t=t: self._kv_ptrs(kh, vh, t, g, r))
+            dims = self._dims(self._home_kv_view(), q_by_pos=self.pos, kv_by_pos=self.pos)
+            for i in range(0, len(items), capi.SCA_MAX_ITEMS):
+                capi.attn_fwd_shard(items[i:i + capi.SCA_MAX_ITEMS], dims, st_ptr, stream)
+                self.launches += 1
+                self.kernels += 1
+        else:
+            self._ring(kh, vh, step)
         rows = self.B * H * S
         capi.attn_merge_lse(_ptr(self.o_parts), _ptr(self.lse_parts), P, rows, D, rows * D, rows,
                             _ptr(self.o), _ptr(self.lse), _ptr(self.o_bf16) if self.o_bf16 is not None else 0,

@@ -68,7 +68,9 @@ def test_forward_sampled_rows_full_size(sca, name, kw):
     ("zigzag", 4, 1, {}), ("zigzag", 8, 1, {}), ("contiguous", 4, 1, {}), ("zigzag", 2, 4, {}),
     ("contiguous", 1, 1, {}), ("zigzag", 1, 2, {}), ("zigzag", 4, 1, {"addressing": "permuted"}),
     ("zigzag", 2, 4, {"addressing": "permuted", "schedule": "direct"}), ("zigzag", 4, 1, {"schedule": "fused"}),
-    ("zigzag", 2, 4, {"schedule": "fused"})])
+    ("zigzag", 2, 4, {"schedule": "fused"}), ("contiguous", 4, 1, {"schedule": "direct"}),
+    # 4 head groups x 4 shards x 4 blocks = 64 partials: two launches of 32
+    ("zigzag", 4, 4, {"schedule": "direct"})])
 def test_forward_small_full_oracle(sca, layout, P, G, kw):
     B, H, S, D = 2, 4, 1024, 128
     q, k, v = seeded_inputs.make_inputs(B, H, S, D, "bf16", seed=100 + P + G)
