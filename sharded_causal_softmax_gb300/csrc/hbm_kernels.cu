@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kPermThreads) zigzag_permute_kernel(const V* _
 // lanes of the group and reduced with shuffles.
 
 constexpr int kMergeThreads = 256;
+constexpr int kMergeFastN = 4;  // up to this many partials: all their loads issued at once
 
 __device__ __forceinline__ int64_t zz_natural_row(int64_t row, int64_t S, int P) {
   const int64_t o = row / S;
@@ -90,38 +91,68 @@ __global__ void __launch_bounds__(kMergeThreads) merge_lse_kernel(
   for (int64_t row0 = warp * RPW; row0 < rows; row0 += nwarps * RPW) {
     const int64_t row = row0 + sub;
     const bool active = row < rows;
-    // max lse over partials: lane li reads partials li, li+L, ...
     float M = -INFINITY;
-    if (active)
-      for (int p = li; p < n; p += L) M = fmaxf(M, lse_parts[p * lps + row]);
-#pragma unroll
-    for (int off = L / 2; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(gmask, M, off));
-    const float M0 = (M == -INFINITY) ? 0.f : M;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
-    if (active) {
-      int p = 0;
-      for (; p + 4 <= n; p += 4) {
-        float4 v[4];
-        float w[4];
+    if (n <= kMergeFastN) {
+      // every partial's o chunk and lse issued together (one round trip to
+      // memory per row, not two), then the same sums in the same order as
+      // the general path below
+      if (active) {
+        float4 v[kMergeFastN];
+        float w[kMergeFastN];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          v[u] = *reinterpret_cast<const float4*>(o_parts + (p + u) * ops + row * D + 4 * li);
-          w[u] = lse_parts[(p + u) * lps + row];
+        for (int u = 0; u < kMergeFastN; ++u)
+          if (u < n) {
+            v[u] = *reinterpret_cast<const float4*>(o_parts + u * ops + row * D + 4 * li);
+            w[u] = lse_parts[u * lps + row];
+          }
+#pragma unroll
+        for (int u = 0; u < kMergeFastN; ++u)
+          if (u < n) M = fmaxf(M, w[u]);
+        const float M0 = (M == -INFINITY) ? 0.f : M;
+#pragma unroll
+        for (int u = 0; u < kMergeFastN; ++u)
+          if (u < n) {
+            const float wu = expf(w[u] - M0);   // exp(-inf) = 0 for empty partials
+            wsum += wu;
+            acc.x += wu * v[u].x; acc.y += wu * v[u].y; acc.z += wu * v[u].z; acc.w += wu * v[u].w;
+          }
+      }
+    } else {
+      // max lse over partials: lane li reads partials li, li+L, ...
+      if (active)
+        for (int p = li; p < n; p += L) M = fmaxf(M, lse_parts[p * lps + row]);
+#pragma unroll
+      for (int off = L / 2; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(gmask, M, off));
+      const float M0 = (M == -INFINITY) ? 0.f : M;
+      if (active) {
+        int p = 0;
+        for (; p + 4 <= n; p += 4) {
+          float4 v[4];
+          float w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            v[u] = *reinterpret_cast<const float4*>(o_parts + (p + u) * ops + row * D + 4 * li);
+            w[u] = lse_parts[(p + u) * lps + row];
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float wu = expf(w[u] - M0);   // exp(-inf) = 0 for empty partials
+            wsum += wu;
+            acc.x += wu * v[u].x; acc.y += wu * v[u].y; acc.z += wu * v[u].z; acc.w += wu * v[u].w;
+          }
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float wu = expf(w[u] - M0);   // exp(-inf) = 0 for empty partials
+        for (; p < n; ++p) {
+          const float4 v = *reinterpret_cast<const float4*>(o_parts + p * ops + row * D + 4 * li);
+          const float wu = expf(lse_parts[p * lps + row] - M0);
           wsum += wu;
-          acc.x += wu * v[u].x; acc.y += wu * v[u].y; acc.z += wu * v[u].z; acc.w += wu * v[u].w;
+          acc.x += wu * v.x; acc.y += wu * v.y; acc.z += wu * v.z; acc.w += wu * v.w;
         }
       }
-      for (; p < n; ++p) {
-        const float4 v = *reinterpret_cast<const float4*>(o_parts + p * ops + row * D + 4 * li);
-        const float wu = expf(lse_parts[p * lps + row] - M0);
-        wsum += wu;
-        acc.x += wu * v.x; acc.y += wu * v.y; acc.z += wu * v.z; acc.w += wu * v.w;
-      }
+    }
+    if (active) {
+      const float M0 = (M == -INFINITY) ? 0.f : M;
       const bool empty = (M == -INFINITY);
       const float inv = empty ? 0.f : 1.f / wsum;
       acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
