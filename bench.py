@@ -1,11 +1,13 @@
 """Benchmark: one training step of sharded causal attention per timed step.
 
-A step is one pass of the whole hot path on device-resident inputs: zigzag
-permute of Q/K/V, P ring steps of per-block (o, lse) partials with
-double-buffered key/value staging, the exact lse merge (fused inverse
-permute), delta, the P ring steps of the backward and the inverse permutes
-of dQ/dK/dV.  Default workload: B=1, H=16, S=32768, D=128 bf16, P=4 zigzag
-shards (the training-step case); --workload picks another of seeded_inputs.
+A step is one pass of the whole hot path on device-resident inputs: P ring
+steps of per-block (o, lse) partials with double-buffered key/value staging,
+the exact lse merge, delta, the fp16 cast of the queries and the P ring
+steps of the backward.  Rows are addressed by their global positions, so the
+zigzag map needs no copy; with --addressing permuted the step also permutes
+Q/K/V and inverse-permutes the outputs.  Default workload: B=1, H=16,
+S=32768, D=128 bf16, P=4 zigzag shards (the training-step case);
+--workload picks another of seeded_inputs.
 
 FLOPs: forward 2*B*H*S^2*D, backward 5*B*H*S^2*D (causal; five matmuls in
 the backward including the recompute of S).
