@@ -9,23 +9,26 @@
 //                 S[n%2] = Q K_n^T           (A = Q from tensor memory)
 //                 O     += P_n V_n           (A = P from tensor memory)
 //               QK^T runs up to two tiles ahead of the softmax.  Keeping Q
-//               in tensor memory halves the shared-memory operand traffic of
-//               QK^T, which bounds the MMA rate at N = 128.
+//               in tensor memory halves QK^T's shared-memory operand
+//               traffic (reading Q from shared memory too measured 2%
+//               slower).
 //   warps 0-7   softmax, two warpgroups: warpgroup g owns columns
 //               [64g, 64g+64) of every S row, thread t of the warpgroup owns
 //               query row t (tensor-memory lane t).  The row maximum is
 //               combined across the two warpgroups through shared memory
 //               while the exponentials are already computed against the
 //               current reference maximum (redone only when it moves); each
-//               warpgroup keeps its part of the running sum and writes its
-//               half of P (bf16) over its own S columns.  O is rescaled when
+//               thread sums its exponentials as two interleaved partial sums
+//               (one serial add chain was on the tile's critical path), and
+//               each warpgroup writes its half of P (bf16) over its own S
+//               columns.  O is rescaled when
 //               the maximum grows by more than 2^8 (lazy rescale, exact
 //               after the final division).
 //               Epilogue: o = O / l, lse = m + ln l.
 //
 // Tensor memory: S0, S1 in columns [0,256), O in [256, 256+D), Q in
-// [256+D, 256+D+D/2); all 512 columns are allocated (one CTA per SM: shared memory use is above half
-// the SM).  Tiles with no visible (query, key) pair are skipped; tiles that
+// [256+D, 256+D+D/2); all 512 columns are allocated (one CTA per SM:
+// shared memory use is above half the SM).  Tiles with no visible (query, key) pair are skipped; tiles that
 // may hold masked pairs or ragged rows are masked elementwise.  Every
 // mbarrier wait is bounded (ptx.cuh); on expiry the CTA records
 // SCA_ERR_TIMEOUT, drains its in-flight copies and MMAs (bounded), frees
