@@ -40,7 +40,9 @@
 // bf16 dS alone would cost more than 1e-2.  dP^T and dV take bf16 V, dO, P^T,
 // except under grouped-query attention (F16PV), where dV sums P^T dO over
 // every query head of the group and bf16 P missed 1e-2: there V (once) and
-// each dO tile are converted too and P^T is rounded to fp16.
+// each dO tile are converted too and P^T is rounded to fp16.  Q (and, under
+// F16PV, dO) may arrive already in fp16, converted once per call by the
+// caller (launch flag f16_inputs): then their tiles are used as loaded.
 //
 // Every wait is bounded (ptx.cuh); on expiry the CTA records
 // SCA_ERR_TIMEOUT, drains in-flight copies/MMAs (bounded), frees tensor
