@@ -51,6 +51,22 @@ from . import capi
 _DT = {torch.bfloat16: capi.SCA_BF16, torch.float32: capi.SCA_F32}
 
 
+def f16_input_flags(stage: bool, dtype, algo: int, H: int, Hkv: int) -> int:
+    """sca_attn_dims.f16_inputs of a backward that stages its fp16 inputs:
+    the queries whenever the tensor-core kernel runs (bf16, not forced onto
+    the CUDA cores), and dO too under grouped key/value heads, where that
+    kernel also takes dO in fp16."""
+    if not stage or dtype != torch.bfloat16 or algo == capi.SCA_ALGO_SIMT:
+        return 0
+    return capi.SCA_F16_Q | (capi.SCA_F16_DOUT if Hkv < H else 0)
+
+
+def launch_groups(n_items: int, per_launch: int = capi.SCA_MAX_ITEMS):
+    """[lo, hi) ranges that send n_items independent items in as few
+    launches as the per-launch limit allows."""
+    return [(lo, min(lo + per_launch, n_items)) for lo in range(0, n_items, per_launch)]
+
+
 def ring_block(r: int, t: int, P: int) -> int:
     """Key/value block held by shard r at ring step t."""
     return (r - t) % P
@@ -149,9 +165,7 @@ class ShardedCausalAttention:
         # the tensor-core backward runs S, dK, dQ (and, grouped, dP, dV) as
         # fp16 products: its fp16 queries (and grouped dO) are cast once per
         # backward here rather than tile by tile in every key-tile CTA
-        self.f16_in = 0
-        if backward and f16_staging and dtype == torch.bfloat16 and algo != capi.SCA_ALGO_SIMT:
-            self.f16_in = capi.SCA_F16_Q | (capi.SCA_F16_DOUT if Hkv < H else 0)
+        self.f16_in = f16_input_flags(backward and f16_staging, dtype, algo, H, Hkv)
         self.q16 = z(B, H, S, D, dt=torch.float16) if self.f16_in else None
         self.do16 = z(B, H, S, D, dt=torch.float16) if self.f16_in & capi.SCA_F16_DOUT else None
         self.copy_stream = torch.cuda.Stream(device=dev) if ring else None
@@ -343,8 +357,8 @@ class ShardedCausalAttention:
             for t in range(P):
                 items += step_items(t, lambda g, r, t=t: self._kv_ptrs(kh, vh, t, g, r))
             dims = self._dims(self._home_kv_view(), q_by_pos=self.pos, kv_by_pos=self.pos)
-            for i in range(0, len(items), capi.SCA_MAX_ITEMS):
-                capi.attn_fwd_shard(items[i:i + capi.SCA_MAX_ITEMS], dims, st_ptr, stream)
+            for lo, hi in launch_groups(len(items)):
+                capi.attn_fwd_shard(items[lo:hi], dims, st_ptr, stream)
                 self.launches += 1
                 self.kernels += 1
         else:

@@ -45,3 +45,25 @@ def test_linear_attention_default_block():
     for args in [(1, 16, 32768, 128, 4), (2, 3, 2304, 128, 3), (1, 1, 128, 128, 1)]:
         b = default_block(*args, bf)
         assert b % 128 == 0 and args[2] % (b * args[4]) == 0
+
+
+def test_fp16_staging_flags():
+    import torch
+    from sharded_causal_softmax_gb300 import capi
+    from sharded_causal_softmax_gb300.sharded import f16_input_flags
+    auto, simt, tc = capi.SCA_ALGO_AUTO, capi.SCA_ALGO_SIMT, capi.SCA_ALGO_TC
+    assert f16_input_flags(True, torch.bfloat16, auto, 16, 16) == capi.SCA_F16_Q
+    assert f16_input_flags(True, torch.bfloat16, tc, 32, 8) == capi.SCA_F16_Q | capi.SCA_F16_DOUT
+    assert f16_input_flags(True, torch.bfloat16, simt, 32, 8) == 0     # CUDA-core kernels read bf16
+    assert f16_input_flags(True, torch.float32, auto, 16, 16) == 0     # fp32 inputs: no fp16 products
+    assert f16_input_flags(False, torch.bfloat16, auto, 32, 8) == 0    # staging switched off
+
+
+@pytest.mark.parametrize("n,per", [(0, 32), (1, 32), (16, 32), (32, 32), (33, 32), (64, 32), (100, 32), (7, 3)])
+def test_launch_groups_cover_every_item_once(n, per):
+    from sharded_causal_softmax_gb300.sharded import launch_groups
+    groups = launch_groups(n, per)
+    covered = [i for lo, hi in groups for i in range(lo, hi)]
+    assert covered == list(range(n))
+    assert all(0 < hi - lo <= per for lo, hi in groups)
+    assert len(groups) == -(-n // per)
