@@ -64,12 +64,15 @@ def flops(w, fwd=True, bwd=True):
     return f
 
 
-def workload_config(w, ws: int) -> dict:
+def workload_config(w, ws: int, visit: str = "ring", inner: int = 0) -> dict:
     """The `config` object both arms print for a workload."""
-    return {"workload": w.description, "name": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "P": w.P,
-            "method": w.method, "layout": w.layout, "schedule": w.schedule, "kv_heads": w.kv_heads or w.H,
-            "head_groups": w.head_groups, "step": "fwd+bwd" if w.backward else "fwd", "flops_per_step": flops(w),
-            "parallelism": f"{ws} independent replica(s), one per GPU"}
+    cfg = {"workload": w.description, "name": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "P": w.P,
+           "method": w.method, "layout": w.layout, "schedule": w.schedule, "kv_heads": w.kv_heads or w.H,
+           "head_groups": w.head_groups, "step": "fwd+bwd" if w.backward else "fwd", "flops_per_step": flops(w),
+           "parallelism": f"{ws} independent replica(s), one per GPU"}
+    if visit == "double_ring":
+        cfg["visit"] = f"double_ring (inner rings of {inner})"
+    return cfg
 
 
 def dist_env():
@@ -160,6 +163,42 @@ class ClockSampler:
                 "period_ms": self.period_ms}
 
 
+def choose_bf16_peak(peaks, region_ms, clocks):
+    """The measured bf16 peak that matches how the kernel was timed: the
+    burst figure (a short cuBLAS run at full clock) when the timed region is
+    short (< 1 s) and the SM clock held at its maximum, else the sustained
+    one (a seconds-long run under the power cap).  Returns (peak, name)."""
+    burst = peaks.get("bf16_tflops")
+    sustained = peaks.get("bf16_tflops_sustained", burst)
+    mhz, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    at_max = mhz is not None and mx is not None and mhz >= 0.97 * mx
+    if burst is not None and region_ms < 1000.0 and at_max:
+        return burst, "burst"
+    return sustained, "sustained"
+
+
+def pinned_copy_gbs(device, nbytes=256 << 20, reps=5):
+    """Host<->device copy bandwidth from pinned memory on this machine (best of
+    `reps` copies of `nbytes`, CUDA events), in GB/s per direction."""
+    host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dev = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    out = {}
+    for name, dst, src in (("h2d", dev, host), ("d2h", host, dev)):
+        dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            dst.copy_(src, non_blocking=True)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        out[name] = round(nbytes / (best * 1e-3) / 1e9, 1)
+    return out
+
+
 def load_peaks():
     try:
         with open(PEAKS_PATH) as f:
@@ -216,13 +255,16 @@ def run_gpu(args):
     dev_in = [x.to(device) for x in inputs]
     if args.schedule:
         w = dataclasses.replace(w, schedule=args.schedule)
-    def make_plan():
+    visit = {"visit": "double_ring", "inner": args.inner} if args.visit == "double_ring" else {}
+
+    def make_plan(**over):
         if w.method == "lasp":
             return sca.ShardedLinearAttention(w.B, w.H, w.S, w.D, w.P, dtype=dtype, backward=w.backward,
                                               block=args.lasp_block or None)
-        return sca.ShardedCausalAttention(w.B, w.H, w.S, w.D, w.P, layout=w.layout, dtype=dtype,
-                                          head_groups=w.head_groups, schedule=w.schedule, backward=w.backward,
-                                          addressing=args.addressing, kv_heads=w.kv_heads)
+        kw = dict(layout=w.layout, dtype=dtype, head_groups=w.head_groups, schedule=w.schedule,
+                  backward=w.backward, addressing=args.addressing, kv_heads=w.kv_heads, **visit)
+        kw.update(over)
+        return sca.ShardedCausalAttention(w.B, w.H, w.S, w.D, w.P, **kw)
 
     plan = make_plan()
     stream = torch.cuda.current_stream(device)
@@ -278,12 +320,17 @@ def run_gpu(args):
     sca.sharded.capi.attn_merge_lse = timed_hbm("merge_lse_kernel", sca.capi.attn_merge_lse, merge_bytes)
     sca.sharded.capi.attn_bwd_delta = timed_hbm("delta_kernel", sca.capi.attn_bwd_delta, delta_bytes)
 
-    def step():
-        plan.forward(*dev_in[:3])
-        kern = plan.kernels
+    staged = {"bytes": 0}
+
+    def step(p=None):
+        p = plan if p is None else p
+        p.forward(*dev_in[:3])
+        kern = p.kernels
+        staged["bytes"] += getattr(p, "staged_bytes", 0)
         if w.backward:
-            plan.backward(dev_in[3])
-            kern += plan.kernels
+            p.backward(dev_in[3])
+            kern += p.kernels
+            staged["bytes"] += getattr(p, "staged_bytes", 0)
         return kern
 
     clocks = ClockSampler(local).start()
@@ -297,6 +344,10 @@ def run_gpu(args):
     barrier(ws)
     torch.cuda.synchronize()
     timing_on[0] = True
+    ring_staged = getattr(plan, "stage_k", None) is not None
+    if ring_staged:
+        plan.stage_events = []
+    staged["bytes"] = 0
     launches = 0
     h0 = time.monotonic()
     t0 = torch.cuda.Event(enable_timing=True)
@@ -315,6 +366,34 @@ def run_gpu(args):
     ms_per_step = ms_max / args.steps
     step_flops = flops(w)
     value = step_flops * args.steps * ws / (ms_max * 1e-3) / 1e12
+    clock_summary = clocks.summary(h0, h1)
+
+    # What the ring's staging costs the step: its copy-engine time per step,
+    # and the step time of the same launches reading every block from its
+    # home rows (no staging copies), timed the same way right after.
+    staging = None
+    if ring_staged:
+        copy_ms = sum(a.elapsed_time(b) for a, b in plan.stage_events) / args.steps
+        plan.stage_events = None
+        home = make_plan(schedule="direct", group_steps=False)
+        for _ in range(max(1, args.warmup)):
+            step(home)
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.steps):
+            step(home)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        if home.read_status() != 0:
+            raise RuntimeError("device status word reports a failure")
+        home_ms = max_over_ranks(a0.elapsed_time(a1), ws, device) / args.steps
+        del home
+        staging = {"bytes_per_step": staged["bytes"] // args.steps, "copy_ms_per_step": round(copy_ms, 4),
+                   "ring_ms_per_step": round(ms_per_step, 4), "home_read_ms_per_step": round(home_ms, 4),
+                   "exposed_ms_per_step": round(ms_per_step - home_ms, 4),
+                   "exposed_frac_of_step": round((ms_per_step - home_ms) / ms_per_step, 4),
+                   "note": "home_read: the same per-step launches with every block read from its home rows"}
 
     # end to end through the public API with host buffers: every step copies
     # its inputs in from pinned host memory and all its results (O, lse and
@@ -377,6 +456,14 @@ def run_gpu(args):
     d2h = sum(x.numel() * x.element_size() for x in outs_host[0])
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, device)
     e2e_value = step_flops * e2e_steps * ws / (e2e_ms * 1e-3) / 1e12
+    # the copies' own limit on this machine: each direction on its own copy
+    # engine, so a step can go no faster than the slower direction's bytes
+    # at its measured pinned bandwidth, nor than the device-side step
+    del plans, dins
+    copy_gbs = pinned_copy_gbs(device)
+    copy_ms = max(h2d / (copy_gbs["h2d"] * 1e9), d2h / (copy_gbs["d2h"] * 1e9)) * 1e3
+    bound_ms = max(copy_ms, ms_per_step)
+    e2e_ms_step = e2e_ms / e2e_steps
 
     # dominant kernel and its roofline
     per = {}
@@ -385,6 +472,9 @@ def run_gpu(args):
             durs = [a.elapsed_time(b) for a, b in evs]
             per[kind] = (sum(durs), len(durs))
     peaks, peak_src = load_peaks()
+    bf16_peak, bf16_regime = choose_bf16_peak(peaks, ms_max, clock_summary)
+    other_regime = "sustained" if bf16_regime == "burst" else "burst"
+    other_peak = peaks.get("bf16_tflops_sustained" if other_regime == "sustained" else "bf16_tflops", bf16_peak)
     kind = max(per, key=lambda k: per[k][0])
     total_ms, n = per[kind]
     avg_s = total_ms / n * 1e-3
@@ -399,9 +489,10 @@ def run_gpu(args):
         bound, unit = "hbm", "GB/s"
         peak_note = f"{peak_src} copy bandwidth"
     elif tc:
-        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        peak = bf16_peak
         bound, unit = "tensor", "TFLOP/s"
-        peak_note = f"{peak_src} bf16 sustained (kernel timed inside a long step)"
+        peak_note = (f"{peak_src} bf16 {bf16_regime} (timed region {ms_max:.0f} ms at median SM "
+                     f"{clock_summary.get('sm_mhz')} of {clock_summary.get('sm_max_mhz')} MHz)")
     else:
         # fp32 FMA issue: 152 SMs x 128 FMA/clk x 2 flop x measured max SM clock
         mhz = peaks.get("sm_max_mhz", 2070.0)
@@ -422,6 +513,11 @@ def run_gpu(args):
     if bound == "hbm":
         roofline["bytes_per_launch"] = launch_bytes
         roofline["tflops"] = round(launch_flops / avg_s / 1e12, 2)
+    if bound == "tensor":
+        roofline["peak_regime"] = bf16_regime
+        roofline[f"frac_{other_regime}"] = round(achieved / other_peak, 4)
+        roofline[f"peak_{other_regime}"] = other_peak
+        roofline["sm_mhz_median"] = clock_summary.get("sm_mhz")
     permute_alone = not hbm["zigzag_permute_kernel"] and w.layout == "zigzag"
     if permute_alone:
         # the step addresses rows by position and runs no permute: time the
@@ -448,9 +544,14 @@ def run_gpu(args):
                                "bytes_per_launch": nb // len(evs)}
     if permute_alone and "zigzag_permute_kernel" in hbm_stats:
         hbm_stats["zigzag_permute_kernel"]["note"] = "timed alone: the step addresses rows by position"
-    other = {k: {"avg_launch_ms": round(v[0] / v[1], 4), "launches": v[1],
-                 "tflops": round(flops(w, fwd=(k == "fwd"), bwd=(k == "bwd")) * args.steps / v[0] * 1e-9, 2)}
-             for k, v in per.items()}
+    other = {}
+    for k, v in per.items():
+        tf = flops(w, fwd=(k == "fwd"), bwd=(k == "bwd")) * args.steps / v[0] * 1e-9
+        other[k] = {"kernel": plan.kernel_name(k), "avg_launch_ms": round(v[0] / v[1], 4), "launches": v[1],
+                    "tflops": round(tf, 2)}
+        if plan.uses_tensor_cores(k) and not (bound_of is not None and bound_of(k) == "hbm"):
+            other[k][f"frac_{bf16_regime}"] = round(tf / bf16_peak, 4)
+            other[k][f"frac_{other_regime}"] = round(tf / other_peak, 4)
 
     line = {
         "metric": METRIC,
@@ -465,18 +566,23 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded N(0,1))",
-        "config": dict(workload_config(w, ws), addressing=plan.addressing,
+        "config": dict(workload_config(w, ws, args.visit, args.inner), addressing=plan.addressing,
                        l2="inputs larger than L2 (no flush)"
                        if sum(x.numel() * x.element_size() for x in inputs) > L2_BYTES else "inputs fit in L2"),
-        "clocks": clocks.summary(h0, h1),
+        "clocks": clock_summary,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "pipeline": "two plans; each step's H2D and D2H run on copy streams beside the compute"},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": round(e2e_ms_step, 4),
+                "copy_gbs": copy_gbs, "copy_bound_ms_per_step": round(copy_ms, 4),
+                "bound_ms_per_step": round(bound_ms, 4), "frac_of_bound": round(bound_ms / e2e_ms_step, 4),
+                "pipeline": "two plans; each step's H2D and D2H run on copy streams beside the compute",
+                "bound": "max(device step, the slower copy direction's bytes at its measured pinned bandwidth)"},
         "gpu_launches": launches,
         "roofline": roofline,
         "kernels": other,
         "hbm_kernels": {"peak_gbs": hbm_peak, "peak_source": f"{peak_src} copy bandwidth", **hbm_stats},
     }
+    if staging is not None:
+        line["staging"] = staging
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     if rank == 0:
@@ -555,7 +661,7 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
             "impl": "reference",
-            "config": workload_config(w, ws),
+            "config": workload_config(w, ws, args.visit, args.inner),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -574,6 +680,9 @@ def main():
     ap.add_argument("--schedule", choices=["ring", "direct", "fused"], default=None,
                     help="override the workload's schedule")
     ap.add_argument("--addressing", choices=["auto", "position", "permuted"], default="auto")
+    ap.add_argument("--visit", choices=["ring", "double_ring"], default="ring",
+                    help="order in which each shard visits the key/value blocks")
+    ap.add_argument("--inner", type=int, default=2, help="double ring: shards per inner ring")
     ap.add_argument("--lasp-block", type=int, default=0,
                     help="linear attention: rows per stored state (64: CUDA cores; a multiple of 128: tensor cores)")
     ap.add_argument("--heads", type=int, default=0,

@@ -47,7 +47,9 @@ typedef enum {
   SCA_ERR_UNSUPPORTED = -2,  /* valid but not implemented (e.g. D not 64/128)  */
   SCA_ERR_CUDA = -3,         /* a CUDA runtime/driver call failed              */
   SCA_ERR_TIMEOUT = -4,      /* device-side bounded wait gave up (dev_status)  */
-  SCA_ERR_ALIGN = -5         /* pointer or stride misaligned                   */
+  SCA_ERR_ALIGN = -5,        /* pointer or stride misaligned                   */
+  SCA_ERR_RANGE = -6         /* an fp16 conversion met a finite value beyond
+                                the fp16 range, |x| >= 65536 (dev_status)    */
 } sca_status;
 
 typedef enum { SCA_BF16 = 0, SCA_F32 = 1 } sca_dtype;
@@ -148,17 +150,28 @@ int attn_fwd_shard(const sca_fwd_item* items, int n_items, const sca_attn_dims* 
 /* attn_merge_lse - exact merge of n (o, lse) partials of the same rows:
  *   M = max_i lse_i, w_i = exp(lse_i - M),
  *   lse = M + ln sum_i w_i,  o = sum_i w_i o_i / sum_i w_i.
+ * Defined by: the pages print no merge.  They keep one partial per key
+ * block so that a shard's output can be assembled as blocks arrive ("Avances
+ * en la capacitacion de LLMs de secuencia larga", section "Limitaciones de
+ * los Enfoques Existentes"); with each partial normalised and carrying its
+ * natural-log lse (attn_fwd_shard), the formula above is the exact way to
+ * combine them (the textbook log-sum-exp rescaling), so the merged row is
+ * the softmax over the union of the blocks' keys.
  * Rows whose partials are all -inf give o = 0, lse = -inf.
  * Layout: o_parts[p * o_part_stride + row * D + d] (fp32),
  * lse_parts[p * lse_part_stride + row] (fp32), rows contiguous.
- * Outputs: o_out fp32 [rows, D] (may alias partial 0), lse_out fp32 [rows]
- * (may alias partial 0), o_bf16_out optional bf16 copy (NULL to skip).
+ * Outputs: o_out fp32 [rows, D], lse_out fp32 [rows], o_bf16_out optional
+ * bf16 copy (NULL to skip).  Without unpermuting, o_out may be exactly one
+ * partial's o rows (o_parts + p * o_part_stride) and lse_out exactly one
+ * partial's lse rows; every other overlap of an output with an input or
+ * with another output is rejected (SCA_ERR_ARG).
  * If `unpermute_P` > 0 the rows are taken as `rows / S` sequences of S
  * rows in zigzag shard-major order over unpermute_P shards, and each output
  * row is written at its natural position (fused inverse zigzag permute; the
- * outputs must then not alias the inputs).
+ * outputs must then not overlap the inputs at all).
  * Errors: SCA_ERR_ARG for n < 1 or n > 64, rows < 0, D not a positive
- * multiple of 4, S not divisible by 2*unpermute_P; SCA_ERR_ALIGN. */
+ * multiple of 4, S not divisible by 2*unpermute_P, overlaps as above;
+ * SCA_ERR_ALIGN. */
 int attn_merge_lse(const float* o_parts, const float* lse_parts, int n, int64_t rows, int D,
                    int64_t o_part_stride, int64_t lse_part_stride,
                    float* o_out, float* lse_out, void* o_bf16_out,
@@ -233,7 +246,10 @@ typedef struct {
  * products (q and k are converted to fp16 inside the kernel, dS is rounded
  * to fp16), and with grouped-query heads dP and dV too (v and dout
  * converted, P rounded to fp16): |q|, |k| (and |v|, |dout|) must stay below
- * 65504.  dims->f16_inputs lets the caller pass q (and, grouped, dout)
+ * 65536.  A finite input at or above that would become +-inf in fp16; the
+ * kernel records SCA_ERR_RANGE in dev_status when it converts one (as does
+ * cast_bf16_to_f16 for the inputs the caller converted), so such a call
+ * cannot pass for a good one.  dims->f16_inputs lets the caller pass q (and, grouped, dout)
  * already converted by cast_bf16_to_f16: the same values, converted once
  * per call instead of once per key tile that reads them.  dq is summed over key tiles
  * by fp32 reduce-adds in no fixed order, so it is reproducible only up to
@@ -245,14 +261,18 @@ int attn_bwd_shard(const sca_bwd_item* items, int n_items, const sca_attn_dims* 
                    int* dev_status, void* stream);
 
 /* cast_bf16_to_f16 - dst[i] = src[i] rounded from bf16 to fp16 (round to
- * nearest even), for i < n: exact for |x| in [2^-14, 65504], fp16
- * subnormals below, +-inf above.  No counterpart on the pages: the staging
- * step that gives attn_bwd_shard (dims->f16_inputs) its fp16 queries once
- * per call.  src and dst may not overlap; n a multiple of 8 and both
- * pointers 16-byte aligned (whole 16-byte vectors).
+ * nearest even), for i < n: exact for |x| in [2^-14, 65280] (every bf16
+ * value up to the largest below 65536), fp16 subnormals below 2^-14 (an
+ * absolute error under 2^-25), +-inf for finite |x| >= 65536.  Meeting such
+ * a value records SCA_ERR_RANGE in *dev_status (may be NULL); the
+ * conversion still completes.  +-inf and NaN inputs stay +-inf and NaN.
+ * No counterpart on the pages: the staging step that gives attn_bwd_shard
+ * (dims->f16_inputs) its fp16 queries once per call.  src and dst may not
+ * overlap; n a multiple of 8 and both pointers 16-byte aligned (whole
+ * 16-byte vectors).
  * Errors: SCA_ERR_ARG for NULL pointers, n < 0, n % 8 != 0, overlap;
  * SCA_ERR_ALIGN for misaligned pointers. */
-int cast_bf16_to_f16(const void* src, void* dst, int64_t n, void* stream);
+int cast_bf16_to_f16(const void* src, void* dst, int64_t n, int* dev_status, void* stream);
 
 /* attn_bwd_delta - delta_i = sum_d dO_id * O_id for `rows` contiguous rows:
  * o fp32 [rows, D], dout [rows, D] of dtype `dout_dtype`, delta fp32 [rows].
@@ -338,8 +358,10 @@ int lasp_bwd(const void* q, const void* k, const void* v, const void* dout, int 
  * must not allocate).  Limit: BH * (S / 64) * D^2 + 2 * BH * P * D^2
  * floats of state must fit the 8M-float (32 MB) array, else
  * SCA_ERR_UNSUPPORTED before anything runs.  The array's device address is
- * looked up once per device, on the first call: make that first call
- * outside any stream capture.  All calls share the array: two calls in
+ * looked up on the first call on each device and kept once the lookup
+ * succeeds (a failed lookup returns SCA_ERR_CUDA and is retried by the next
+ * call); make that first call outside any stream capture.  Devices with an
+ * ordinal above 63 get SCA_ERR_CUDA.  All calls share the array: two calls in
  * flight at once (other streams or threads, same device) race and must be
  * serialised by the caller.  Nothing in the array must start at zero (every
  * state is written before it is read).  o: fp32 [BH, S, D], overwritten. */

@@ -20,8 +20,9 @@ SCA_ERR_UNSUPPORTED = -2
 SCA_ERR_CUDA = -3
 SCA_ERR_TIMEOUT = -4
 SCA_ERR_ALIGN = -5
+SCA_ERR_RANGE = -6
 STATUS_NAMES = {0: "SCA_OK", -1: "SCA_ERR_ARG", -2: "SCA_ERR_UNSUPPORTED", -3: "SCA_ERR_CUDA",
-                -4: "SCA_ERR_TIMEOUT", -5: "SCA_ERR_ALIGN"}
+                -4: "SCA_ERR_TIMEOUT", -5: "SCA_ERR_ALIGN", -6: "SCA_ERR_RANGE"}
 
 SCA_BF16 = 0
 SCA_F32 = 1
@@ -88,7 +89,7 @@ def _load():
         "ring_stage_segments": (c_int, [c_void_p, c_void_p, c_int64, c_int64, POINTER(sca_segs), c_int64, c_void_p]),
         "attn_bwd_shard": (c_int, [POINTER(sca_bwd_item), c_int, POINTER(sca_attn_dims), c_void_p, c_void_p]),
         "attn_bwd_delta": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int64, c_int, c_void_p]),
-        "cast_bf16_to_f16": (c_int, [c_void_p, c_void_p, c_int64, c_void_p]),
+        "cast_bf16_to_f16": (c_int, [c_void_p, c_void_p, c_int64, c_void_p, c_void_p]),
         "lasp_block_states": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int64, c_int64, c_int, c_int, c_void_p,
                                       c_void_p]),
         "lasp_scan": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int, c_int, c_int, c_int, c_void_p]),
@@ -210,8 +211,8 @@ def attn_bwd_delta(o: int, dout: int, dout_dtype: int, delta: int, rows: int, D:
     return check(lib().attn_bwd_delta(o, dout, dout_dtype, delta, rows, D, stream))
 
 
-def cast_bf16_to_f16(src: int, dst: int, n: int, stream: int) -> int:
-    return check(lib().cast_bf16_to_f16(src, dst, n, stream))
+def cast_bf16_to_f16(src: int, dst: int, n: int, dev_status: int, stream: int) -> int:
+    return check(lib().cast_bf16_to_f16(src, dst, n, dev_status, stream))
 
 
 def sca_read_status(dev_status: int, stream: int) -> int:

@@ -34,8 +34,9 @@
 //
 // Precision: S^T, dK and dQ run as fp16 MMAs.  The elementwise warps convert
 // the K tile (once) and each Q tile in shared memory from bf16 to fp16
-// (exact for |x| in [2^-14, 65504], so inputs must stay inside the fp16
-// range), and round dS to fp16 (2^-11 relative) instead of bf16 (2^-8):
+// (exact for |x| in [2^-14, 65280]; a finite |x| >= 65536 would become
+// +-inf and is recorded as SCA_ERR_RANGE in the status word), and round dS
+// to fp16 (2^-11 relative) instead of bf16 (2^-8):
 // with few visible keys a query's dQ is a short sum of large dS terms and
 // bf16 dS alone would cost more than 1e-2.  dP^T and dV take bf16 V, dO, P^T,
 // except under grouped-query attention (F16PV), where dV sums P^T dO over
@@ -443,8 +444,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     uint8_t* sds = smem + L::DS_OFF + wg * PANEL + (row >> 3) * 1024 + (row & 7) * 128;
     int n = 0;
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_full, 0, abort, status));
+    // a finite input beyond the fp16 range would become +-inf: recorded as
+    // SCA_ERR_RANGE (the kernel still runs to completion)
+    bool range_bad = false;
     if (ok) {   // K (and V) to fp16; the two tiles are contiguous
-      smem_bf16_to_f16<(F16PV ? 2 : 1) * L::TILE, 256>(smem + L::K_OFF, threadIdx.x);
+      range_bad |= smem_bf16_to_f16<(F16PV ? 2 : 1) * L::TILE, 256>(smem + L::K_OFF, threadIdx.x);
       fence_async_smem();
     }
     mbar_arrive(&bars->k_conv);
@@ -454,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     auto convert_q = [&](int j) -> bool {
       const bool w = __all_sync(0xffffffffu, mbar_wait(&bars->q_full[j & 1], (j >> 1) & 1, abort, status));
       if (w && !q_is_f16) {
-        smem_bf16_to_f16<L::TILE, 256>(smem + L::Q_OFF + (j & 1) * L::TILE, threadIdx.x);
+        range_bad |= smem_bf16_to_f16<L::TILE, 256>(smem + L::Q_OFF + (j & 1) * L::TILE, threadIdx.x);
         fence_async_smem();
       }
       mbar_arrive(&bars->q_conv);
@@ -464,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     auto convert_do = [&](int j) -> bool {
       const bool w = __all_sync(0xffffffffu, mbar_wait(&bars->do_full[j & 1], (j >> 1) & 1, abort, status));
       if (w && !do_is_f16) {
-        smem_bf16_to_f16<L::TILE, 256>(smem + L::DO_OFF + (j & 1) * L::TILE, threadIdx.x);
+        range_bad |= smem_bf16_to_f16<L::TILE, 256>(smem + L::DO_OFF + (j & 1) * L::TILE, threadIdx.x);
         fence_async_smem();
       }
       mbar_arrive(&bars->do_conv);
@@ -616,6 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         ++n;
       }
     }
+    if (range_bad) report(status, SCA_ERR_RANGE);
     // dK (warpgroup 0, times scale) and dV (warpgroup 1): thread = key row,
     // staged fp32 in 32-column 128B-swizzled boxes over the K/V tiles (dK)
     // and the Q stages (dV), free since the last MMA completed; one thread

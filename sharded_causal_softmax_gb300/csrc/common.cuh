@@ -152,6 +152,15 @@ SCA_INLINE void report(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// Does either bf16 half of w hold a finite value beyond the fp16 range?
+// bf16 magnitudes from 0x4780 (65536) up to 0x7f7f (the largest finite)
+// round to +-inf in fp16; 0x477f (65280) and below convert exactly or to
+// fp16 subnormals; +-inf and NaN stay what they are.
+SCA_INLINE bool bf16x2_beyond_f16(uint32_t w) {
+  const uint32_t lo = w & 0x7fffu, hi = (w >> 16) & 0x7fffu;
+  return (lo - 0x4780u < 0x7f80u - 0x4780u) | (hi - 0x4780u < 0x7f80u - 0x4780u);
+}
+
 SCA_INLINE float to_f32(float x) { return x; }
 SCA_INLINE float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 

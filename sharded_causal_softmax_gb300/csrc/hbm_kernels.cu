@@ -16,11 +16,17 @@ namespace sca {
 // sequence o is a contiguous copy of one source chunk.  Forward (natural ->
 // shard-major): destination chunk 2r holds natural chunk r and 2r+1 holds
 // natural chunk 2P-1-r.  Inverse: natural chunk n comes from shard-major
-// chunk 2n (n < P) or 2(2P-1-n)+1.  Each CTA copies a contiguous span of one
-// chunk, so loads and stores are fully coalesced.
+// chunk 2n (n < P) or 2(2P-1-n)+1.
+//
+// Work is cut into tiles of kPermThreads * kPermUnroll vectors inside one
+// chunk (a chunk's last tile may be short).  The grid is one wave of
+// resident blocks, and block b copies tiles b, b + grid, ...: every block
+// gets the same number of tiles to within one, so no partial second wave
+// idles most of the GPU.  Each thread has kPermUnroll 16-byte loads in
+// flight before its first store; loads and stores are fully coalesced.
 
 constexpr int kPermThreads = 256;
-constexpr int kPermUnroll = 4;
+constexpr int kPermUnroll = 8;
 
 __host__ __device__ __forceinline__ int zz_src_chunk(int ch, int P, int inverse) {
   if (!inverse) {
@@ -33,27 +39,29 @@ __host__ __device__ __forceinline__ int zz_src_chunk(int ch, int P, int inverse)
 template <typename V>
 __global__ void __launch_bounds__(kPermThreads) zigzag_permute_kernel(const V* __restrict__ src,
                                                                       V* __restrict__ dst, int64_t nseg,
-                                                                      int64_t chunk_vecs, int P,
-                                                                      int inverse) {
+                                                                      int64_t chunk_vecs, int64_t tiles_per_chunk,
+                                                                      int P, int inverse) {
+  constexpr int64_t kTile = static_cast<int64_t>(kPermThreads) * kPermUnroll;
   const int two_p = 2 * P;
-  for (int64_t g = blockIdx.y; g < nseg; g += gridDim.y) {
+  const int64_t n_tiles = nseg * tiles_per_chunk;
+  for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const int64_t g = t / tiles_per_chunk;             // destination chunk (o, ch)
+    const int64_t base = (t - g * tiles_per_chunk) * kTile;
     const int64_t o = g / two_p;
     const int ch = static_cast<int>(g - o * two_p);
-    const V* s = src + (o * two_p + zz_src_chunk(ch, P, inverse)) * chunk_vecs;
-    V* d = dst + (o * two_p + ch) * chunk_vecs;
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * kPermThreads * kPermUnroll; base < chunk_vecs;
-         base += static_cast<int64_t>(gridDim.x) * kPermThreads * kPermUnroll) {
-      V tmp[kPermUnroll];
+    const V* s = src + (o * two_p + zz_src_chunk(ch, P, inverse)) * chunk_vecs + base;
+    V* d = dst + g * chunk_vecs + base;
+    const int64_t n = chunk_vecs - base < kTile ? chunk_vecs - base : kTile;
+    V tmp[kPermUnroll];
 #pragma unroll
-      for (int u = 0; u < kPermUnroll; ++u) {
-        const int64_t i = base + u * kPermThreads + threadIdx.x;
-        if (i < chunk_vecs) tmp[u] = s[i];
-      }
+    for (int u = 0; u < kPermUnroll; ++u) {
+      const int i = u * kPermThreads + threadIdx.x;
+      if (i < n) tmp[u] = s[i];
+    }
 #pragma unroll
-      for (int u = 0; u < kPermUnroll; ++u) {
-        const int64_t i = base + u * kPermThreads + threadIdx.x;
-        if (i < chunk_vecs) d[i] = tmp[u];
-      }
+    for (int u = 0; u < kPermUnroll; ++u) {
+      const int i = u * kPermThreads + threadIdx.x;
+      if (i < n) d[i] = tmp[u];
     }
   }
 }
@@ -77,9 +85,14 @@ __device__ __forceinline__ int64_t zz_natural_row(int64_t row, int64_t S, int P)
   return o * S + nat;
 }
 
+// o_out / lse_out may be partial p's own rows (the host allows that exact
+// alias and no other overlap), so the inputs are not declared __restrict__,
+// and every lane of a row's group has finished reading before any lane of
+// the group stores (the lse of a row is read by all L lanes and written by
+// lane 0).
 template <int L>
 __global__ void __launch_bounds__(kMergeThreads) merge_lse_kernel(
-    const float* __restrict__ o_parts, const float* __restrict__ lse_parts, int n, int64_t rows,
+    const float* o_parts, const float* lse_parts, int n, int64_t rows,
     int64_t ops, int64_t lps, float* o_out, float* lse_out, __nv_bfloat16* ob_out, int uP, int64_t S) {
   constexpr int RPW = 32 / L;  // rows per warp
   const int lane = threadIdx.x & 31;
@@ -151,6 +164,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_lse_kernel(
         }
       }
     }
+    __syncwarp(gmask);   // a row's group is uniform in `active`; all its loads are done
     if (active) {
       const float M0 = (M == -INFINITY) ? 0.f : M;
       const bool empty = (M == -INFINITY);
@@ -202,12 +216,17 @@ __global__ void __launch_bounds__(kMergeThreads) delta_kernel(const float* __res
 //
 // Eight values per 16-byte vector; grid-stride over the vectors.  Each bf16
 // is widened exactly to fp32 (its bits in the high half) and rounded to fp16
-// by the hardware conversion.
+// by the hardware conversion.  A finite bf16 value above the fp16 range
+// (|x| >= 65536; the largest bf16 below that, 65280, converts exactly)
+// becomes +-inf in fp16: the kernel records SCA_ERR_RANGE in the status word
+// when it meets one, and still writes the converted value.
 
 constexpr int kCastThreads = 256;
 
 __global__ void __launch_bounds__(kCastThreads) cast_bf16_f16_kernel(const uint4* __restrict__ src,
-                                                                     uint4* __restrict__ dst, int64_t nvec) {
+                                                                     uint4* __restrict__ dst, int64_t nvec,
+                                                                     int* status) {
+  bool bad = false;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(kCastThreads) + threadIdx.x; i < nvec;
        i += static_cast<int64_t>(gridDim.x) * kCastThreads) {
     const uint4 v = src[i];
@@ -215,19 +234,25 @@ __global__ void __launch_bounds__(kCastThreads) cast_bf16_f16_kernel(const uint4
     uint32_t o[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
+      bad |= bf16x2_beyond_f16(w[k]);
       const __half2 h = __floats2half2_rn(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u));
       o[k] = *reinterpret_cast<const uint32_t*>(&h);
     }
     dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
+  if (bad) report(status, SCA_ERR_RANGE);
 }
 
-static int grid_for(int64_t work_items, int per_block) {
+static int sm_count() {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
+static int grid_for(int64_t work_items, int per_block) {
   int64_t blocks = (work_items + per_block - 1) / per_block;
-  const int64_t cap = static_cast<int64_t>(sms) * 16;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
   if (blocks > cap) blocks = cap;
   return static_cast<int>(blocks < 1 ? 1 : blocks);
 }
@@ -238,11 +263,23 @@ static bool overlap(const void* a, int64_t a_bytes, const void* b, int64_t b_byt
   return x < y + static_cast<uintptr_t>(b_bytes) && y < x + static_cast<uintptr_t>(a_bytes);
 }
 
+// Does [out, out + bytes) overlap one of the n regions base + p * stride of
+// `bytes` each, other than (when exact_ok) by coinciding with it exactly?
+static bool bad_overlap(const void* out, int64_t bytes, const void* base, int64_t stride_bytes, int n,
+                        int64_t part_bytes, bool exact_ok) {
+  for (int p = 0; p < n; ++p) {
+    const void* part = static_cast<const char*>(base) + p * stride_bytes;
+    if (!overlap(out, bytes, part, part_bytes)) continue;
+    if (!(exact_ok && out == part && bytes == part_bytes)) return true;
+  }
+  return false;
+}
+
 }  // namespace sca
 
 using namespace sca;
 
-extern "C" int cast_bf16_to_f16(const void* src, void* dst, int64_t n, void* stream) {
+extern "C" int cast_bf16_to_f16(const void* src, void* dst, int64_t n, int* dev_status, void* stream) {
   SCA_REQUIRE(src && dst, SCA_ERR_ARG, "cast_bf16_to_f16: NULL pointer");
   SCA_REQUIRE(n >= 0 && n % 8 == 0, SCA_ERR_ARG, "cast_bf16_to_f16: n=%lld must be a non-negative multiple of 8",
               static_cast<long long>(n));
@@ -251,7 +288,7 @@ extern "C" int cast_bf16_to_f16(const void* src, void* dst, int64_t n, void* str
   if (n == 0) return SCA_OK;
   const int64_t nvec = n / 8;
   cast_bf16_f16_kernel<<<grid_for(nvec, kCastThreads * 4), kCastThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(src), static_cast<uint4*>(dst), nvec);
+      static_cast<const uint4*>(src), static_cast<uint4*>(dst), nvec, dev_status);
   return cuda_status(cudaGetLastError(), "cast_bf16_to_f16 launch");
 }
 
@@ -274,21 +311,21 @@ extern "C" int zigzag_permute(const void* src, void* dst, int64_t outer, int64_t
   const bool vec16 = chunk_bytes % 16 == 0 && aligned(src, 16) && aligned(dst, 16);
   const int64_t vsz = vec16 ? 16 : 4;
   const int64_t chunk_vecs = chunk_bytes / vsz;
-  const int per_block = kPermThreads * kPermUnroll;
-  int64_t gx = (chunk_vecs + per_block - 1) / per_block;
-  const int gy = static_cast<int>(nseg < 65535 ? nseg : 65535);
-  const int64_t cap = grid_for(1LL << 40, 1) / gy + 1;
-  if (gx > cap) gx = cap;
-  dim3 grid(static_cast<unsigned>(gx < 1 ? 1 : gx), gy);
+  const int64_t tile = static_cast<int64_t>(kPermThreads) * kPermUnroll;
+  const int64_t tiles_per_chunk = (chunk_vecs + tile - 1) / tile;
+  // one wave: 2048 resident threads per SM at 256 per block
+  const int64_t resident = static_cast<int64_t>(sm_count()) * (2048 / kPermThreads);
+  const int64_t n_tiles = nseg * tiles_per_chunk;
+  const unsigned grid = static_cast<unsigned>(n_tiles < resident ? n_tiles : resident);
   cudaStream_t st = as_stream(stream);
   if (vec16)
     zigzag_permute_kernel<uint4><<<grid, kPermThreads, 0, st>>>(static_cast<const uint4*>(src),
                                                                 static_cast<uint4*>(dst), nseg, chunk_vecs,
-                                                                P, inverse);
+                                                                tiles_per_chunk, P, inverse);
   else
     zigzag_permute_kernel<uint32_t><<<grid, kPermThreads, 0, st>>>(static_cast<const uint32_t*>(src),
                                                                    static_cast<uint32_t*>(dst), nseg,
-                                                                   chunk_vecs, P, inverse);
+                                                                   chunk_vecs, tiles_per_chunk, P, inverse);
   return cuda_status(cudaGetLastError(), "zigzag_permute launch");
 }
 
@@ -346,12 +383,29 @@ extern "C" int attn_merge_lse(const float* o_parts, const float* lse_parts, int 
   SCA_REQUIRE(o_part_stride % 4 == 0, SCA_ERR_ALIGN, "attn_merge_lse: o_part_stride not a multiple of 4");
   SCA_REQUIRE(aligned(o_parts, 16) && aligned(o_out, 16) && aligned(o_bf16_out, 8), SCA_ERR_ALIGN,
               "attn_merge_lse: o pointers must be 16-byte aligned (bf16 copy 8-byte)");
-  if (unpermute_P > 0) {
+  if (unpermute_P > 0)
     SCA_REQUIRE(S > 0 && S % (2 * unpermute_P) == 0 && rows % S == 0, SCA_ERR_ARG,
                 "attn_merge_lse: unpermute needs S %% 2P == 0 and rows %% S == 0");
-    SCA_REQUIRE(!overlap(o_parts, (n - 1) * o_part_stride * 4 + rows * D * 4, o_out, rows * D * 4) &&
-                    !overlap(lse_parts, (n - 1) * lse_part_stride * 4 + rows * 4, lse_out, rows * 4),
-                SCA_ERR_ARG, "attn_merge_lse: outputs may not alias inputs when unpermuting");
+  {
+    // An output may be exactly one partial's rows when rows keep their
+    // places (no unpermute): every element is then read by the lanes that
+    // write it.  Any other overlap with an input, or between outputs, races.
+    const bool exact_ok = unpermute_P == 0;
+    const int64_t ob = rows * D * 4, lb = rows * 4;
+    SCA_REQUIRE(!bad_overlap(o_out, ob, o_parts, o_part_stride * 4, n, ob, exact_ok) &&
+                    !bad_overlap(o_out, ob, lse_parts, lse_part_stride * 4, n, lb, false) &&
+                    !bad_overlap(lse_out, lb, lse_parts, lse_part_stride * 4, n, lb, exact_ok) &&
+                    !bad_overlap(lse_out, lb, o_parts, o_part_stride * 4, n, ob, false) && !overlap(o_out, ob, lse_out, lb),
+                SCA_ERR_ARG,
+                exact_ok ? "attn_merge_lse: an output overlaps an input other than by being one partial's rows exactly"
+                         : "attn_merge_lse: outputs may not overlap inputs when unpermuting");
+    if (o_bf16_out) {
+      const int64_t bb = rows * D * 2;
+      SCA_REQUIRE(!bad_overlap(o_bf16_out, bb, o_parts, o_part_stride * 4, n, ob, false) &&
+                      !bad_overlap(o_bf16_out, bb, lse_parts, lse_part_stride * 4, n, lb, false) &&
+                      !overlap(o_bf16_out, bb, o_out, ob) && !overlap(o_bf16_out, bb, lse_out, lb),
+                  SCA_ERR_ARG, "attn_merge_lse: o_bf16_out overlaps another buffer");
+    }
   }
   if (rows == 0) return SCA_OK;
   const int L = D / 4;

@@ -290,22 +290,32 @@ static cudaError_t allow_smem(K kernel, int bytes) {
 constexpr int64_t kScratchFloats = int64_t(8) << 20;
 __device__ __align__(256) float g_scratch[kScratchFloats];
 
-// Device address of g_scratch on the current device, looked up once per
-// device (the first call must not be inside a stream capture).
+// Device address of g_scratch on the current device.  A successful lookup
+// is kept per device (at most kMaxDevices); a failed one (for instance made
+// inside a stream capture) is not, so a later call retries it.  The first
+// call on a device should come before any stream capture.
+constexpr int kMaxDevices = 64;
 static float* scratch_ptr(cudaError_t* err) {
-  static std::once_flag once[64];
-  static float* ptr[64];
-  static cudaError_t res[64];
+  static std::mutex mu;
+  static float* ptr[kMaxDevices] = {};
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess) return nullptr;
-  std::call_once(once[dev & 63], [&] {
+  if (dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> g(mu);
+  if (!ptr[dev]) {
     void* p = nullptr;
-    res[dev & 63] = cudaGetSymbolAddress(&p, g_scratch);
-    ptr[dev & 63] = static_cast<float*>(p);
-  });
-  *err = res[dev & 63];
-  return *err == cudaSuccess ? ptr[dev & 63] : nullptr;
+    *err = cudaGetSymbolAddress(&p, g_scratch);
+    if (*err != cudaSuccess) {
+      cudaGetLastError();   // not sticky: leave no error behind for the next launch check
+      return nullptr;
+    }
+    ptr[dev] = static_cast<float*>(p);
+  }
+  return ptr[dev];
 }
 
 }  // namespace lasp

@@ -307,22 +307,27 @@ SCA_INLINE uint32_t pack_f16x2(float lo, float hi) {
 // magnitude in [2^-14, 65504] converts exactly (fp16 has more mantissa bits);
 // smaller ones become fp16 subnormals, larger ones overflow.  The element
 // positions, and so any swizzled layout, are unchanged.  All of a thread's
-// loads are issued before its first store.
+// loads are issued before its first store.  Returns whether this thread met
+// a finite value beyond the fp16 range (bf16x2_beyond_f16).
 template <int BYTES, int NT>
-SCA_INLINE void smem_bf16_to_f16(uint8_t* base, int tid) {
+SCA_INLINE bool smem_bf16_to_f16(uint8_t* base, int tid) {
   static_assert(BYTES % (16 * NT) == 0, "whole 16-byte chunks per thread");
   constexpr int kIter = BYTES / (16 * NT);
   uint4 v[kIter];
+  bool bad = false;
 #pragma unroll
   for (int k = 0; k < kIter; ++k) v[k] = *reinterpret_cast<const uint4*>(base + (k * NT + tid) * 16);
 #pragma unroll
   for (int k = 0; k < kIter; ++k) {
     uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 4; ++i) {
+      bad |= bf16x2_beyond_f16(w[i]);
       w[i] = pack_f16x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+    }
     *reinterpret_cast<uint4*>(base + (k * NT + tid) * 16) = make_uint4(w[0], w[1], w[2], w[3]);
   }
+  return bad;
 }
 
 }  // namespace sca

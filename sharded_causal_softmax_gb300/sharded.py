@@ -26,6 +26,17 @@ The schedule (host logic only; every byte is moved or computed by libsca):
   home rows (the K/V all-gather reading of the TSP page); its forward
   partials of all P steps are independent and go out together, up to
   SCA_MAX_ITEMS (query shard, block) items per launch.
+* Double ring (same page, section "Mejorando la Eficiencia de Comunicacion
+  con la Atencion de Doble Anillo"; the page gives no layout): with
+  visit="double_ring" the P shards form P / inner groups of `inner`
+  consecutive shards.  Shard r = g * inner + i first passes blocks around
+  the inner ring of its group (inner steps: blocks of group g, places
+  i, i-1, ...), then the outer ring moves every group on to the blocks of
+  the group before it, and the inner ring runs again.  At step
+  t = u * inner + v shard r holds block ((g - u) mod outer) * inner +
+  (i - v) mod inner.  Each staging copy takes a rank's next block from the
+  rank that held it at the step before: a neighbour in the group on an
+  inner hop, a rank of the previous group on an outer hop.
 * Merge: the P partials of every row are combined exactly by log-sum-exp
   rescaling (``attn_merge_lse``), fused with the inverse permute when the
   partials are shard-major.
@@ -72,6 +83,34 @@ def ring_block(r: int, t: int, P: int) -> int:
     return (r - t) % P
 
 
+def double_ring_block(r: int, t: int, P: int, inner: int) -> int:
+    """Key/value block held by shard r at step t of the double ring over
+    P / inner groups of `inner` shards (see the module docstring)."""
+    outer = P // inner
+    g, i = divmod(r, inner)
+    u, v = divmod(t, inner)
+    return ((g - u) % outer) * inner + (i - v) % inner
+
+
+def hop_senders(block_of, t_next: int, P: int):
+    """senders[r]: the shard whose block at step t_next - 1 shard r holds at
+    step t_next (every step's map from shards to blocks is one-to-one)."""
+    held = {block_of(r, t_next - 1): r for r in range(P)}
+    return [held[block_of(r, t_next)] for r in range(P)]
+
+
+def copy_runs(senders):
+    """(dst0, src0, n) runs of consecutive destinations whose senders are
+    consecutive too: each run is one contiguous copy of staged slabs."""
+    runs = []
+    for r, s in enumerate(senders):
+        if runs and runs[-1][0] + runs[-1][2] == r and runs[-1][1] + runs[-1][2] == s:
+            runs[-1] = (runs[-1][0], runs[-1][1], runs[-1][2] + 1)
+        else:
+            runs.append((r, s, 1))
+    return runs
+
+
 def shard_segs(S: int, P: int, layout: str, r: int) -> capi.sca_segs:
     """Global positions of shard r's rows, in the shard's row order."""
     if layout == "zigzag":
@@ -100,11 +139,19 @@ class ShardedCausalAttention:
 
     def __init__(self, B, H, S, D, P, layout="zigzag", dtype=torch.bfloat16, head_groups=1,
                  schedule="ring", scale=None, causal=True, algo=capi.SCA_ALGO_AUTO, backward=False,
-                 bf16_out=False, device=None, addressing="auto", kv_heads=None, f16_staging=True):
+                 bf16_out=False, device=None, addressing="auto", kv_heads=None, f16_staging=True,
+                 visit="ring", inner=None, group_steps=True):
         if layout not in ("zigzag", "contiguous"):
             raise ValueError(f"layout {layout!r}")
         if schedule not in ("ring", "direct", "fused"):
             raise ValueError(f"schedule {schedule!r}")
+        if visit == "ring":
+            inner = P
+        elif visit == "double_ring":
+            if inner is None or inner < 1 or P % inner:
+                raise ValueError(f"double_ring needs an inner ring size dividing P={P} (got {inner})")
+        else:
+            raise ValueError(f"visit {visit!r}")
         if addressing not in ("auto", "position", "permuted"):
             raise ValueError(f"addressing {addressing!r}")
         if dtype not in _DT:
@@ -128,6 +175,11 @@ class ShardedCausalAttention:
         self.G, self.Hg = head_groups, H // head_groups
         self.Hkv, self.Hkvg = Hkv, Hkv // head_groups   # key/value heads: all, per head group
         self.layout, self.schedule, self.dtype = layout, schedule, dtype
+        self.visit, self.inner = visit, inner
+        # direct schedule: the forward's partials of all steps in as few
+        # launches as possible, or (False) one launch per step as the ring
+        # sends them, only without staging copies
+        self.group_steps = group_steps
         self.addressing = addressing
         self.pos = addressing == "position"
         fused = schedule == "fused"
@@ -175,6 +227,10 @@ class ShardedCausalAttention:
         self._inputs = None
         self.launches = 0   # kernels + copies issued by the last forward/backward
         self.kernels = 0    # kernels alone
+        self.staged_bytes = 0   # bytes copied into staging buffers by the last forward/backward
+        # when set to a list, each staging pass of a ring step appends its
+        # (start, end) events, recorded on the copy stream
+        self.stage_events = None
 
     # ------------------------------------------------------------ helpers
 
@@ -242,26 +298,34 @@ class ShardedCausalAttention:
     def _stage_kv_view(self):
         return capi.view(self.Hkvg * self.n_r * self.D, self.n_r * self.D, self.D)
 
+    def block(self, r: int, t: int) -> int:
+        """Key/value block shard r holds (visits) at step t."""
+        if self.visit == "double_ring":
+            return double_ring_block(r, t, self.P, self.inner)
+        return ring_block(r, t, self.P)
+
     def _kv_ptrs(self, k_home, v_home, t, g, r):
         """(k, v) base pointers of the block rank (g, r) holds at step t."""
-        P = self.P
         if self.stage_k is None or t == 0:
-            off = self._kv_rows(g, ring_block(r, t, P)) * self.D * self.eb
+            off = self._kv_rows(g, self.block(r, t)) * self.D * self.eb
             return _ptr(k_home) + off, _ptr(v_home) + off
         buf = t % 2
         return _ptr(self.stage_k[buf][g, r]), _ptr(self.stage_v[buf][g, r])
 
     def _stage(self, k_home, v_home, t_next):
-        """Ring pass into the spare buffer: rank (g, r) receives what rank
-        (g, r-1) holds at step t_next - 1."""
+        """Hand-off into the spare buffer: rank (g, r) receives the block it
+        visits at step t_next from the rank that holds it at step t_next - 1
+        (its left neighbour on the ring; on the double ring a neighbour in
+        its group, or a rank of the previous group on an outer hop)."""
         P, B, Hg, n_r, D, eb = self.P, self.B, self.Hkvg, self.n_r, self.D, self.eb
         cs = self.copy_stream.cuda_stream
         dst_k, dst_v = self.stage_k[t_next % 2], self.stage_v[t_next % 2]
         row = D * eb
+        blk = B * Hg * n_r
         for g in range(self.G):
-            if t_next == 1:   # neighbours' home blocks
+            if t_next == 1:   # the senders' blocks are still at home
                 for r in range(P):
-                    src_r = (r - 1) % P
+                    src_r = self.block(r, 1)
                     for b in range(B):
                         off = ((b * self.Hkv + g * Hg) * self.S) * row
                         for home, dst in ((k_home, dst_k), (v_home, dst_v)):
@@ -272,14 +336,14 @@ class ShardedCausalAttention:
                                 capi.ring_stage_block(_ptr(home) + off, _ptr(dst[g, r, b]), Hg, self.S,
                                                       src_r * n_r, n_r, row, cs)
                             self.launches += 1
-            else:             # neighbours' staged blocks: a rotation by one rank
+                            self.staged_bytes += Hg * n_r * row
+            else:             # the senders' staged blocks: one copy per run of consecutive ranks
                 src_k, src_v = self.stage_k[(t_next - 1) % 2], self.stage_v[(t_next - 1) % 2]
-                blk = B * Hg * n_r
-                for src, dst in ((src_k, dst_k), (src_v, dst_v)):
-                    capi.ring_stage_block(_ptr(src[g, 0]), _ptr(dst[g, 1]), 1, (P - 1) * blk, 0, (P - 1) * blk,
-                                          row, cs)
-                    capi.ring_stage_block(_ptr(src[g, P - 1]), _ptr(dst[g, 0]), 1, blk, 0, blk, row, cs)
-                    self.launches += 2
+                for r0, s0, n in copy_runs(hop_senders(self.block, t_next, P)):
+                    for src, dst in ((src_k, dst_k), (src_v, dst_v)):
+                        capi.ring_stage_block(_ptr(src[g, s0]), _ptr(dst[g, r0]), 1, n * blk, 0, n * blk, row, cs)
+                        self.launches += 1
+                        self.staged_bytes += n * blk * row
 
     def _ring(self, k_home, v_home, launch_step):
         """Run launch_step(t, kv_ptrs(g, r), kv_view, home) for t = 0..P-1
@@ -295,7 +359,13 @@ class ShardedCausalAttention:
                 with torch.cuda.stream(self.copy_stream):
                     if t >= 1:
                         self.copy_stream.wait_event(self.ev_done[t - 1])
+                    if self.stage_events is not None:
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        e0.record(self.copy_stream)
                     self._stage(k_home, v_home, t + 1)
+                    if self.stage_events is not None:
+                        e1.record(self.copy_stream)
+                        self.stage_events.append((e0, e1))
                     self.ev_staged[t + 1].record(self.copy_stream)
             if ring and t >= 1:
                 cur.wait_event(self.ev_staged[t])
@@ -311,7 +381,7 @@ class ShardedCausalAttention:
     def forward(self, q, k, v):
         self._check_inputs(q)
         self._check_inputs(k, v, heads=self.Hkv)
-        self.launches = self.kernels = 0
+        self.launches = self.kernels = self.staged_bytes = 0
         self._inputs = (q, k, v)
         stream = torch.cuda.current_stream(self.device).cuda_stream
         if self.schedule == "fused":
@@ -339,7 +409,7 @@ class ShardedCausalAttention:
                     it.o = _ptr(self.o_parts[t]) + rows * D * 4
                     it.lse = _ptr(self.lse_parts[t]) + rows * 4
                     it.q_pos = shard_segs(S, P, self.layout, r)
-                    it.kv_pos = shard_segs(S, P, self.layout, ring_block(r, t, P))
+                    it.kv_pos = shard_segs(S, P, self.layout, self.block(r, t))
                     items.append(it)
             return items
 
@@ -349,7 +419,7 @@ class ShardedCausalAttention:
             self.launches += 1
             self.kernels += 1
 
-        if self.schedule == "direct":
+        if self.schedule == "direct" and self.group_steps:
             # every block is read from its home rows (the all-gather reading),
             # so the partials of all P steps are independent: they go out
             # together, up to SCA_MAX_ITEMS items per launch
@@ -410,7 +480,7 @@ class ShardedCausalAttention:
             q, k, v = self._inputs
         self._check_inputs(do, q)
         self._check_inputs(k, v, heads=self.Hkv)
-        self.launches = self.kernels = 0
+        self.launches = self.kernels = self.staged_bytes = 0
         stream = torch.cuda.current_stream(self.device).cuda_stream
         S, D, H, P, B = self.S, self.D, self.H, self.P, self.B
         eb = self.eb
@@ -439,7 +509,7 @@ class ShardedCausalAttention:
             items = []
             for g in range(self.G):
                 for r in range(P):
-                    j = ring_block(r, t, P)
+                    j = self.block(r, t)
                     qo, ko = self._rows(g, r), self._kv_rows(g, j)
                     it = capi.sca_bwd_item()
                     it.q = _ptr(qh) + qo * D * eb
@@ -470,12 +540,12 @@ class ShardedCausalAttention:
         """The backward's query (and grouped dO) tensors: fp16 copies when the
         plan stages them, else the inputs themselves."""
         if self.f16_in & capi.SCA_F16_Q:
-            capi.cast_bf16_to_f16(_ptr(q), _ptr(self.q16), q.numel(), stream)
+            capi.cast_bf16_to_f16(_ptr(q), _ptr(self.q16), q.numel(), _ptr(self.status), stream)
             q = self.q16
             self.launches += 1
             self.kernels += 1
         if self.f16_in & capi.SCA_F16_DOUT:
-            capi.cast_bf16_to_f16(_ptr(do), _ptr(self.do16), do.numel(), stream)
+            capi.cast_bf16_to_f16(_ptr(do), _ptr(self.do16), do.numel(), _ptr(self.status), stream)
             do = self.do16
             self.launches += 1
             self.kernels += 1

@@ -221,12 +221,12 @@ def test_f16_inputs_flag_rejected_outside_the_tensor_core_backward(lib, case):
 
 def test_cast_rejects_bad_arguments(lib):
     f = lib.cast_bf16_to_f16
-    assert f(None, A, 8, None) == capi.SCA_ERR_ARG
-    assert f(A, 2 * A, 12, None) == capi.SCA_ERR_ARG          # not whole 16-byte vectors
-    assert f(A, 2 * A, -8, None) == capi.SCA_ERR_ARG
-    assert f(A + 8, 2 * A, 8, None) == capi.SCA_ERR_ALIGN
-    assert f(A, A + 16, 64, None) == capi.SCA_ERR_ARG         # overlapping ranges
-    assert f(A, 2 * A, 0, None) == capi.SCA_OK                # nothing to do, no launch
+    assert f(None, A, 8, None, None) == capi.SCA_ERR_ARG
+    assert f(A, 2 * A, 12, None, None) == capi.SCA_ERR_ARG          # not whole 16-byte vectors
+    assert f(A, 2 * A, -8, None, None) == capi.SCA_ERR_ARG
+    assert f(A + 8, 2 * A, 8, None, None) == capi.SCA_ERR_ALIGN
+    assert f(A, A + 16, 64, None, None) == capi.SCA_ERR_ARG         # overlapping ranges
+    assert f(A, 2 * A, 0, 3 * A, None) == capi.SCA_OK               # nothing to do, no launch
     arr = (capi.sca_bwd_item * 1)(_bwd_item(dk=A + 4))
     assert lib.attn_bwd_shard(arr, 1, ctypes.byref(_dims()), None, None) == capi.SCA_ERR_ALIGN
     assert lib.attn_bwd_shard(arr, 0, ctypes.byref(_dims()), None, None) == capi.SCA_ERR_ARG
@@ -251,6 +251,28 @@ def test_merge_rejects_bad_arguments(lib):
     assert f(A + 4, 2 * A, 2, 10, 128, 1280, 10, 3 * A, 4 * A, None, 0, 0, None) == capi.SCA_ERR_ALIGN
     assert f(A, 2 * A, 2, 10, 128, 1280, 10, 3 * A, 4 * A, None, 4, 12, None) == capi.SCA_ERR_ARG  # S % 2P
     assert f(A, 2 * A, 2, 0, 128, 0, 0, 3 * A, 4 * A, None, 0, 0, None) == capi.SCA_OK
+
+
+def test_merge_rejects_overlaps_other_than_one_partials_rows(lib):
+    """An output may be exactly one partial's rows (each element is then read
+    and written by the same lanes); any other overlap races and is refused
+    before a launch.  (The exact alias itself runs on the GPU tests.)"""
+    f = lib.attn_merge_lse
+    rows, D, n = 10, 128, 2
+    ob, lb = rows * D * 4, rows * 4
+    op, lp = A, 2 * A          # partials: o at A (stride rows*D), lse at 2A (stride rows)
+    def call(o_out, lse_out, bf=None, uP=0, S=0):
+        return f(op, lp, n, rows, D, rows * D, rows, o_out, lse_out, bf, uP, S, None)
+    assert call(op + 16, 4 * A) == capi.SCA_ERR_ARG               # o_out shifted by 4 columns into partial 0
+    assert call(op + ob + 512, 4 * A) == capi.SCA_ERR_ARG         # o_out straddles partial 1 at a row offset
+    assert call(3 * A, lp + 4) == capi.SCA_ERR_ARG                # lse_out one row into partial 0's lse
+    assert call(3 * A, op + 64) == capi.SCA_ERR_ARG               # lse_out inside the o partials
+    assert call(lp, 4 * A) == capi.SCA_ERR_ARG                    # o_out over the lse partials
+    assert call(3 * A, 3 * A + 256) == capi.SCA_ERR_ARG           # lse_out inside o_out
+    assert call(3 * A, 4 * A, bf=3 * A + 1024) == capi.SCA_ERR_ARG   # bf16 copy over o_out
+    assert call(3 * A, 4 * A, bf=op) == capi.SCA_ERR_ARG             # bf16 copy over partial 0
+    assert call(op, lp, uP=1, S=rows) == capi.SCA_ERR_ARG         # unpermuting: no alias at all
+    assert call(op + ob, lp + lb, uP=1, S=rows) == capi.SCA_ERR_ARG
 
 
 def test_stage_and_delta_reject_bad_arguments(lib):

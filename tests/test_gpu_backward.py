@@ -29,15 +29,19 @@ def sca():
     ("f32", "contiguous", 2, 1, "ring", 256, "auto"), ("f32", "zigzag", 4, 1, "ring", 200 * 8 // 8, "auto"),
     ("bf16", "zigzag", 4, 1, "ring", 1024, "permuted"), ("bf16", "zigzag", 2, 2, "direct", 1024, "permuted"),
     ("bf16", "zigzag", 4, 1, "fused", 1024, "auto"), ("bf16", "zigzag", 2, 2, "fused", 896, "auto"),
-    ("f32", "contiguous", 2, 1, "fused", 256, "auto"), ("f32", "zigzag", 4, 1, "ring", 1024, "position")])
+    ("f32", "contiguous", 2, 1, "fused", 256, "auto"), ("f32", "zigzag", 4, 1, "ring", 1024, "position"),
+    ("bf16", "zigzag", 4, 1, "double_ring", 1024, "auto"), ("bf16", "zigzag", 8, 2, "double_ring", 2048, "auto"),
+    ("bf16", "zigzag", 4, 1, "double_ring", 1024, "permuted")])
 def test_backward_small_full_oracle(sca, dtype, layout, P, G, schedule, S, addressing):
     B, H, D = 1, 2, 128 if dtype == "bf16" else 64
     if layout == "zigzag" and S % (2 * P):
         S = 2 * P * (S // (2 * P))
     q, k, v, do = seeded_inputs.make_inputs(B, H, S, D, dtype, seed=200 + P, with_do=True)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
-    plan = sca.ShardedCausalAttention(B, H, S, D, P, layout=layout, dtype=tdt, head_groups=G, schedule=schedule,
-                                      backward=True, addressing=addressing)
+    visit = {"visit": "double_ring", "inner": 2} if schedule == "double_ring" else {}
+    plan = sca.ShardedCausalAttention(B, H, S, D, P, layout=layout, dtype=tdt, head_groups=G,
+                                      schedule="ring" if visit else schedule, backward=True, addressing=addressing,
+                                      **visit)
     qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
     o, lse = plan.forward(qd, kd, vd)
     dq, dk, dv = plan.backward(dod, qd, kd, vd)
@@ -67,11 +71,13 @@ def test_backward_repeat_overwrites(sca, schedule):
     assert torch.allclose(a[0], b[0], rtol=0, atol=1e-5)
 
 
-@pytest.mark.parametrize("schedule", ["ring", "fused"])
+@pytest.mark.parametrize("schedule", ["ring", "fused", "double_ring"])
 def test_training_step_full_size_sampled(sca, schedule):
     w = WORKLOADS["train_s32k"]
     q, k, v, do = seeded_inputs.workload_inputs(w)
-    plan = sca.ShardedCausalAttention(w.B, w.H, w.S, w.D, w.P, layout=w.layout, schedule=schedule, backward=True)
+    visit = {"visit": "double_ring", "inner": 2} if schedule == "double_ring" else {}
+    plan = sca.ShardedCausalAttention(w.B, w.H, w.S, w.D, w.P, layout=w.layout,
+                                      schedule="ring" if visit else schedule, backward=True, **visit)
     o, lse = plan.forward(q.cuda(), k.cuda(), v.cuda())
     dq, dk, dv = plan.backward(do.cuda())
     torch.cuda.synchronize()

@@ -31,8 +31,30 @@ def test_cast_matches_torch_bit_for_bit(sca, n):
     x[: min(n, special.numel())] = special[: min(n, special.numel())]
     src = x.cuda()
     dst = torch.full((n,), float("nan"), dtype=torch.float16, device="cuda")
-    sca.capi.cast_bf16_to_f16(src.data_ptr(), dst.data_ptr(), n, torch.cuda.current_stream().cuda_stream)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    sca.capi.cast_bf16_to_f16(src.data_ptr(), dst.data_ptr(), n, status.data_ptr(), stream)
     torch.cuda.synchronize()
+    want = x.to(torch.float16)
+    assert torch.equal(dst.cpu().view(torch.int16), want.view(torch.int16))
+    # the specials include finite values beyond the fp16 range (65520 rounds
+    # to bf16 65536; 7e4, -1e6): the conversion reports them
+    beyond = (x.float().abs() >= 65536) & torch.isfinite(x.float())
+    assert bool(beyond.any())
+    assert sca.capi.sca_read_status(status.data_ptr(), stream) == sca.capi.SCA_ERR_RANGE
+
+
+def test_cast_in_range_reports_nothing(sca):
+    """The largest bf16 below 65536 (65280), infinities and NaN convert
+    without a range report; the status word stays 0."""
+    x = torch.tensor([65280.0, -65280.0, float("inf"), -float("inf"), float("nan"), 1e-9, 0.0, 3.5] * 4,
+                     dtype=torch.bfloat16)
+    src = x.cuda()
+    dst = torch.empty(x.numel(), dtype=torch.float16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    sca.capi.cast_bf16_to_f16(src.data_ptr(), dst.data_ptr(), x.numel(), status.data_ptr(), stream)
+    assert sca.capi.sca_read_status(status.data_ptr(), stream) == sca.capi.SCA_OK
     want = x.to(torch.float16)
     assert torch.equal(dst.cpu().view(torch.int16), want.view(torch.int16))
 
@@ -54,3 +76,31 @@ def test_staged_backward_matches_in_kernel_conversion(sca, schedule, kv_heads, H
     (dq1, dk1, dv1), (dq0, dk0, dv0) = grads
     assert torch.equal(dk1, dk0) and torch.equal(dv1, dv0)
     torch.testing.assert_close(dq1, dq0, rtol=1e-5, atol=1e-6)
+
+
+@pytest.mark.parametrize("where,staging", [("q", True), ("q", False), ("k", True), ("v_grouped", True)])
+def test_backward_reports_values_beyond_fp16(sca, where, staging):
+    """A finite bf16 input that fp16 cannot hold (7e4 rounds to bf16 70144)
+    would turn into +-inf inside the fp16 products of the backward: the call
+    records SCA_ERR_RANGE in its status word instead of passing for a good
+    one.  Q goes through the once-per-call cast (staging) or the kernel's own
+    conversion; K always through the kernel's; V (grouped heads, where dP and
+    dV are fp16 products) through the kernel's.  Nothing faults, and a clean
+    call on the same plan afterwards reports nothing."""
+    B, S, D, P = 1, 512, 128, 2
+    kvh = 1 if where == "v_grouped" else None
+    H = 2
+    q, k, v, do = (x.cuda() for x in seeded_inputs.make_inputs(B, H, S, D, "bf16", seed=73, with_do=True,
+                                                              kv_heads=kvh))
+    bad = {"q": q, "k": k, "v_grouped": v}[where].clone()
+    bad[0, 0, 300, 5] = 7e4
+    ins = {"q": q, "k": k, "v": v}
+    ins["v" if where == "v_grouped" else where] = bad
+    plan = sca.ShardedCausalAttention(B, H, S, D, P, backward=True, kv_heads=kvh, f16_staging=staging)
+    plan.forward(ins["q"], ins["k"], ins["v"])
+    plan.backward(do)
+    assert plan.read_status() == sca.capi.SCA_ERR_RANGE
+    plan.status.zero_()
+    plan.forward(q, k, v)
+    plan.backward(do)
+    assert plan.read_status() == sca.capi.SCA_OK

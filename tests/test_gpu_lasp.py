@@ -5,7 +5,9 @@ fp32 operands split into two bf16 parts): small cases in full (outputs,
 gradients and the states each shard receives), the 32K training workload at
 full size on sampled rows.  Both keep about fp32 accuracy, and without
 normalisation the outputs grow like sqrt(t): the fp32 bounds (2e-4 max-abs,
-2e-5 mean-abs) apply relative to the largest reference magnitude."""
+2e-5 mean-abs) apply row by row, relative to the largest reference
+magnitude of that row (at least 1), so an early row of magnitude O(1) is held
+to the absolute fp32 bounds however large the late rows grow."""
 import numpy as np
 import pytest
 import torch
@@ -13,7 +15,7 @@ import torch
 import oracle
 import seeded_inputs
 from seeded_inputs import WORKLOADS
-from tests.gpu_util import errors, scale_for
+from tests.gpu_util import scale_for
 
 pytestmark = pytest.mark.gpu
 REL = (2e-4, 2e-5)
@@ -28,11 +30,20 @@ def sca():
 
 
 def assert_close_rel(name, got, ref, rel=REL):
+    """Per row (the last axis is the row's D values): the row's max-abs
+    error <= rel[0] * m_t and its mean-abs error <= rel[1] * m_t, with
+    m_t = max(1, max |ref_t|)."""
     ref = np.asarray(ref, dtype=np.float64)
-    mag = max(1.0, float(np.abs(ref).max()))
-    mx, mn = errors(got, ref)
-    assert mx <= rel[0] * mag and mn <= rel[1] * mag, \
-        f"{name}: max-abs {mx:.3e}, mean-abs {mn:.3e} against magnitude {mag:.3e}"
+    g = got.double().cpu().numpy() if hasattr(got, "cpu") else np.asarray(got, dtype=np.float64)
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    assert np.all(np.isfinite(g)), f"{name}: non-finite values"
+    err = np.abs(g - ref).reshape(-1, ref.shape[-1])
+    mag = np.maximum(1.0, np.abs(ref).reshape(-1, ref.shape[-1]).max(axis=1))
+    rmax, rmean = err.max(axis=1) / mag, err.mean(axis=1) / mag
+    worst = int(np.argmax(np.maximum(rmax / rel[0], rmean / rel[1])))
+    assert rmax[worst] <= rel[0] and rmean[worst] <= rel[1], \
+        (f"{name}: row {worst}: max-abs {err[worst].max():.3e}, mean-abs {err[worst].mean():.3e} against its "
+         f"magnitude {mag[worst]:.3e} (relative {rmax[worst]:.2e} / {rmean[worst]:.2e}, bounds {rel})")
 
 
 @pytest.mark.parametrize("dtype,B,H,S,D,P,block", [

@@ -49,7 +49,8 @@ def test_forward_full_oracle(sca, name, kw):
     assert_close("lse", lse, rl, tol_for(w.dtype))
 
 
-@pytest.mark.parametrize("name,kw", [("ring_s128k", {}), ("2d_s32k", {}), ("ring_s128k", {"schedule": "fused"})])
+@pytest.mark.parametrize("name,kw", [("ring_s128k", {}), ("2d_s32k", {}), ("ring_s128k", {"schedule": "fused"}),
+                                     ("ring_s128k", {"visit": "double_ring", "inner": 4})])
 def test_forward_sampled_rows_full_size(sca, name, kw):
     w = WORKLOADS[name]
     q, k, v = seeded_inputs.workload_inputs(w)[:3]
@@ -70,7 +71,13 @@ def test_forward_sampled_rows_full_size(sca, name, kw):
     ("zigzag", 2, 4, {"addressing": "permuted", "schedule": "direct"}), ("zigzag", 4, 1, {"schedule": "fused"}),
     ("zigzag", 2, 4, {"schedule": "fused"}), ("contiguous", 4, 1, {"schedule": "direct"}),
     # 4 head groups x 4 shards x 4 blocks = 64 partials: two launches of 32
-    ("zigzag", 4, 4, {"schedule": "direct"})])
+    ("zigzag", 4, 4, {"schedule": "direct"}),
+    # double ring: 2 groups of 2 shards / 4 of 2; staged hand-offs inside and between groups
+    ("zigzag", 4, 1, {"visit": "double_ring", "inner": 2}), ("zigzag", 8, 1, {"visit": "double_ring", "inner": 2}),
+    ("zigzag", 4, 2, {"visit": "double_ring", "inner": 2, "addressing": "permuted"}),
+    ("contiguous", 4, 1, {"visit": "double_ring", "inner": 2}),
+    # the direct schedule, one launch per step (the ring's launches without its staging copies)
+    ("zigzag", 4, 1, {"schedule": "direct", "group_steps": False})])
 def test_forward_small_full_oracle(sca, layout, P, G, kw):
     B, H, S, D = 2, 4, 1024, 128
     q, k, v = seeded_inputs.make_inputs(B, H, S, D, "bf16", seed=100 + P + G)
@@ -93,14 +100,41 @@ def test_ring_staging_equals_direct_reads(sca):
     q, k, v = seeded_inputs.make_inputs(w.B, H, S, w.D, "bf16", seed=w.seed)
     outs = []
     for kw in ({"schedule": "ring"}, {"schedule": "direct"}, {"schedule": "ring", "addressing": "permuted"},
-               {"schedule": "direct", "addressing": "permuted"}, {"schedule": "fused"}):
+               {"schedule": "direct", "addressing": "permuted"}, {"schedule": "direct", "group_steps": False},
+               {"schedule": "fused"}):
         plan = sca.ShardedCausalAttention(w.B, H, S, w.D, w.P, **kw)
         o, lse = plan.forward(q.cuda(), k.cuda(), v.cuda())
         outs.append((o.clone(), lse.clone()))
-    for o, lse in outs[1:4]:
+    for o, lse in outs[1:5]:
         assert torch.equal(outs[0][0], o) and torch.equal(outs[0][1], lse)
-    assert torch.allclose(outs[0][0], outs[4][0], rtol=0, atol=2e-3)
-    assert torch.allclose(outs[0][1], outs[4][1], rtol=0, atol=1e-4)
+    assert torch.allclose(outs[0][0], outs[5][0], rtol=0, atol=2e-3)
+    assert torch.allclose(outs[0][1], outs[5][1], rtol=0, atol=1e-4)
+
+
+def test_double_ring_partials_are_the_ring_partials(sca):
+    """The double ring visits the same (shard, block) pairs in another order:
+    each pair's partial is computed by the same kernel from the same rows, so
+    the partial stored for block j of shard r is bit for bit the ring's;
+    only the merge order (step slots) differs, so O and lse agree up to fp32
+    rounding.  Staged copies carry the blocks unchanged through inner and
+    outer hops."""
+    w = WORKLOADS["ring_s128k"]
+    S, H, P, inner = 16384, 2, w.P, 4
+    q, k, v = (x.cuda() for x in seeded_inputs.make_inputs(w.B, H, S, w.D, "bf16", seed=w.seed + 1))
+    ring = sca.ShardedCausalAttention(w.B, H, S, w.D, P)
+    dbl = sca.ShardedCausalAttention(w.B, H, S, w.D, P, visit="double_ring", inner=inner)
+    o1, l1 = ring.forward(q, k, v)
+    o2, l2 = dbl.forward(q, k, v)
+    assert ring.read_status() == 0 and dbl.read_status() == 0
+    segs = [oracle.shard_positions(S, P, "zigzag")[r] for r in range(P)]
+    for r in range(P):
+        rows = torch.as_tensor(segs[r], device="cuda")
+        for t in range(P):
+            j = dbl.block(r, t)
+            t_ring = (r - j) % P
+            assert torch.equal(dbl.o_parts[t][:, :, rows], ring.o_parts[t_ring][:, :, rows])
+            assert torch.equal(dbl.lse_parts[t][:, :, rows], ring.lse_parts[t_ring][:, :, rows])
+    assert torch.allclose(o1, o2, rtol=0, atol=1e-5) and torch.allclose(l1, l2, rtol=0, atol=1e-5)
 
 
 def test_repeated_calls_are_deterministic(sca):

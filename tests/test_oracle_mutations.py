@@ -75,6 +75,20 @@ def _backward_no_delta(q, k, v, do, scale, causal=True, o=None, lse=None):
 _orig_backward = oatt.attention_backward
 
 
+def _double_ring_outer_first(P, r, inner):
+    # slip: the loops swapped, the outer ring turning fastest
+    outer = P // inner
+    g, i = divmod(r, inner)
+    return [((g - u) % outer) * inner + ((i - v) % inner) for v in range(inner) for u in range(outer)]
+
+
+def _double_ring_inner_up(P, r, inner):
+    # slip: the inner ring turning the other way (place i + v)
+    outer = P // inner
+    g, i = divmod(r, inner)
+    return [((g - u) % outer) * inner + ((i + v) % inner) for u in range(outer) for v in range(inner)]
+
+
 def _kv_head_interleaved(h, n_heads, n_kv_heads):
     # wrong grouping: query heads dealt round-robin over the key/value heads
     return h % n_kv_heads
@@ -100,6 +114,8 @@ MERGE_PINS = [pins.test_merge_two_halves_closed_form,
               lambda: pins.test_sharded_equals_unsharded("zigzag", 4)]
 ZIGZAG_PINS = [pins.test_zigzag_matches_golden_chunk_map,
                lambda: pins.test_zigzag_balances_causal_work(4, 5)]
+DOUBLE_RING_PINS = [lambda: pins.test_double_ring_matches_hand_derived_orders(8, 4),
+                    lambda: pins.test_double_ring_structure(8, 2)]
 BACKWARD_PINS = [pins.test_backward_finite_differences, pins.test_backward_invariants]
 GQA_PINS = [lambda: pins.test_gqa_forward_matches_torch_sdpa_on_repeated_kv(4, 2),
             lambda: pins.test_gqa_backward_matches_torch_autograd(4, 2), pins.test_gqa_backward_finite_differences]
@@ -147,6 +163,13 @@ def test_planted_gqa_backward_mistake_is_caught(monkeypatch):
     assert _some_pin_fails(GQA_PINS[1:]), "no pin caught the unsummed key/value gradient"
 
 
+@pytest.mark.parametrize("bad", [_double_ring_outer_first, _double_ring_inner_up])
+def test_planted_double_ring_mistake_is_caught(monkeypatch, bad):
+    monkeypatch.setattr(oshd, "double_ring_visit_order", bad)
+    monkeypatch.setattr(oracle, "double_ring_visit_order", bad)
+    assert _some_pin_fails(DOUBLE_RING_PINS), f"no pin caught mutation {bad.__name__}"
+
+
 def test_unmutated_oracle_passes_every_listed_pin():
-    for lst in (FORWARD_PINS, MERGE_PINS, ZIGZAG_PINS, BACKWARD_PINS, GQA_PINS):
+    for lst in (FORWARD_PINS, MERGE_PINS, ZIGZAG_PINS, BACKWARD_PINS, GQA_PINS, DOUBLE_RING_PINS):
         assert not _some_pin_fails(lst)

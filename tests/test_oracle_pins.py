@@ -157,6 +157,57 @@ def test_merge_any_visiting_order_and_double_ring():
         np.testing.assert_allclose(ls_, lse, atol=1e-12)
 
 
+# Double ring, P = outer x inner shards, shard r = (group g, place i) with
+# r = g*inner + i.  Written out by hand from the reading of the 2D page's
+# double ring ("Mejorando la Eficiencia de Comunicacion con la Atencion de
+# Doble Anillo"): for `inner` steps the blocks go round the inner ring of
+# the group whose blocks are being visited (place i, then i-1, ...); then
+# the outer ring moves every shard on to the blocks of the group before it.
+DOUBLE_RING_ORDERS = {
+    (4, 2): [[0, 1, 2, 3], [1, 0, 3, 2], [2, 3, 0, 1], [3, 2, 1, 0]],
+    (8, 4): [[0, 3, 2, 1, 4, 7, 6, 5], [1, 0, 3, 2, 5, 4, 7, 6], [2, 1, 0, 3, 6, 5, 4, 7],
+             [3, 2, 1, 0, 7, 6, 5, 4], [4, 7, 6, 5, 0, 3, 2, 1], [5, 4, 7, 6, 1, 0, 3, 2],
+             [6, 5, 4, 7, 2, 1, 0, 3], [7, 6, 5, 4, 3, 2, 1, 0]],
+    (6, 2): [[0, 1, 4, 5, 2, 3], [1, 0, 5, 4, 3, 2], [2, 3, 0, 1, 4, 5], [3, 2, 1, 0, 5, 4],
+             [4, 5, 2, 3, 0, 1], [5, 4, 3, 2, 1, 0]],
+}
+
+
+@pytest.mark.parametrize("P,inner", sorted(DOUBLE_RING_ORDERS))
+def test_double_ring_matches_hand_derived_orders(P, inner):
+    for r in range(P):
+        assert oracle.double_ring_visit_order(P, r, inner) == DOUBLE_RING_ORDERS[(P, inner)][r], r
+
+
+@pytest.mark.parametrize("P,inner", [(4, 2), (8, 4), (8, 2), (6, 3), (6, 2), (12, 4), (4, 1), (4, 4)])
+def test_double_ring_structure(P, inner):
+    """The two levels of the order, independently of the literal tables:
+    every shard visits every block once, starting with its own; step block
+    u*inner + v lies in group (g - u) mod outer; inside that segment the
+    place steps down by one each step (the inner ring); at every step the
+    blocks held form a one-to-one map, so each hand-off is a permutation in
+    which an inner hop moves a block to the next shard of the same group."""
+    outer = P // inner
+    orders = [oracle.double_ring_visit_order(P, r, inner) for r in range(P)]
+    for r, order in enumerate(orders):
+        g, i = divmod(r, inner)
+        assert sorted(order) == list(range(P)) and order[0] == r
+        for u in range(outer):
+            seg = order[u * inner:(u + 1) * inner]
+            assert all(b // inner == (g - u) % outer for b in seg), (r, u, seg)
+            assert [b % inner for b in seg] == [(i - v) % inner for v in range(inner)], (r, u, seg)
+    for t in range(P):
+        held = [orders[r][t] for r in range(P)]
+        assert sorted(held) == list(range(P))
+        if t + 1 < P and (t + 1) % inner:                 # inner hop: from the previous place in the group
+            for r in range(P):
+                sender = held.index(orders[r][t + 1])
+                assert sender // inner == r // inner and sender % inner == (r % inner - 1) % inner
+    # inner = P is the single ring, inner = 1 the ring over groups of one
+    if inner in (1, P):
+        assert orders == [oracle.ring_visit_order(P, r) for r in range(P)]
+
+
 def test_merge_identity_and_permutation():
     n, R, D = 4, 30, 7
     o = RNG.standard_normal((n, R, D))

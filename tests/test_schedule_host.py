@@ -2,7 +2,9 @@
 device memory is touched, so no GPU is needed)."""
 import pytest
 
-from sharded_causal_softmax_gb300.sharded import ShardedCausalAttention, ring_block, shard_segs
+import oracle
+from sharded_causal_softmax_gb300.sharded import (ShardedCausalAttention, copy_runs, double_ring_block, hop_senders,
+                                                  ring_block, shard_segs)
 
 
 @pytest.mark.parametrize("kw,msg", [
@@ -12,6 +14,9 @@ from sharded_causal_softmax_gb300.sharded import ShardedCausalAttention, ring_bl
     (dict(addressing="sideways"), "addressing"),
     (dict(addressing="position", S=768), "128"),             # zigzag chunks of 96 rows
     (dict(layout="diagonal"), "layout"),
+    (dict(visit="double_ring"), "inner"),                    # no inner ring size
+    (dict(visit="double_ring", inner=3), "inner"),           # 3 does not divide P = 4
+    (dict(visit="spiral"), "visit"),
 ])
 def test_schedule_rejects_bad_arguments(kw, msg):
     args = dict(B=1, H=8, S=1024, D=128, P=4)
@@ -67,3 +72,42 @@ def test_launch_groups_cover_every_item_once(n, per):
     assert covered == list(range(n))
     assert all(0 < hi - lo <= per for lo, hi in groups)
     assert len(groups) == -(-n // per)
+
+
+@pytest.mark.parametrize("P,inner", [(4, 2), (8, 4), (8, 2), (6, 3), (4, 4), (4, 1), (16, 4)])
+def test_double_ring_schedule_follows_the_oracle_order(P, inner):
+    for r in range(P):
+        assert [double_ring_block(r, t, P, inner) for t in range(P)] == oracle.double_ring_visit_order(P, r, inner)
+
+
+def test_ring_hand_off_is_two_copies():
+    """Every ring hand-off is a rotation by one shard: two contiguous copies
+    (shards 1..P-1 from 0..P-2, shard 0 from P-1)."""
+    P = 8
+    for t in range(1, P):
+        runs = copy_runs(hop_senders(lambda r, s: ring_block(r, s, P), t, P))
+        assert sorted(runs) == [(0, P - 1, 1), (1, 0, P - 1)]
+
+
+@pytest.mark.parametrize("P,inner", [(8, 4), (8, 2), (6, 3)])
+def test_double_ring_hand_offs(P, inner):
+    """Inner hops rotate inside each group (two copies per group); outer hops
+    take every block from a shard of the previous group.  Every run of a
+    hand-off copies real staged slabs: each destination receives exactly the
+    block it visits next."""
+    blk = lambda r, t: double_ring_block(r, t, P, inner)
+    for t in range(1, P):
+        senders = hop_senders(blk, t, P)
+        assert sorted(senders) == list(range(P))
+        for r, s in enumerate(senders):
+            assert blk(s, t - 1) == blk(r, t)
+            if t % inner:   # inner hop
+                assert s // inner == r // inner
+            else:           # outer hop
+                assert s // inner == (r // inner - 1) % (P // inner)
+        covered = []
+        for r0, s0, n in copy_runs(senders):
+            covered += [(r0 + k, s0 + k) for k in range(n)]
+        assert sorted(covered) == sorted(enumerate(senders))
+        if t % inner:
+            assert len(copy_runs(senders)) == 2 * (P // inner) - (P // inner if inner == 1 else 0)
