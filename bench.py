@@ -389,10 +389,25 @@ def run_gpu(args):
             raise RuntimeError("device status word reports a failure")
         home_ms = max_over_ranks(a0.elapsed_time(a1), ws, device) / args.steps
         del home
+        # one hand-off alone (the rotation of staged blocks between two ring
+        # steps, nothing else running): the copy engine's own rate
+        cs = plan.copy_stream
+        plan.staged_bytes = 0
+        h0e, h1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(cs):
+            h0e.record(cs)
+            plan._stage(dev_in[1], dev_in[2], 2 if w.P > 2 else 1)
+            h1e.record(cs)
+        torch.cuda.synchronize()
+        handoff_ms = h0e.elapsed_time(h1e)
+        handoff_bytes = plan.staged_bytes
         staging = {"bytes_per_step": staged["bytes"] // args.steps, "copy_ms_per_step": round(copy_ms, 4),
                    "ring_ms_per_step": round(ms_per_step, 4), "home_read_ms_per_step": round(home_ms, 4),
                    "exposed_ms_per_step": round(ms_per_step - home_ms, 4),
                    "exposed_frac_of_step": round((ms_per_step - home_ms) / ms_per_step, 4),
+                   "handoff_alone_ms": round(handoff_ms, 4), "handoff_bytes": handoff_bytes,
+                   "handoff_alone_gbs": round(handoff_bytes / (handoff_ms * 1e-3) / 1e9, 1),
                    "note": "home_read: the same per-step launches with every block read from its home rows"}
 
     # end to end through the public API with host buffers: every step copies

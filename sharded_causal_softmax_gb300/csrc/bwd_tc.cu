@@ -12,7 +12,11 @@
 //   dV += P^T dO_i                                 (A = P^T in tmem)
 //   dS^T = P^T (dP^T - delta_i)                    (warps 0-7, phase 2)
 //   dK += dS^T Q_i         dQ_i = dS K             (A = dS^T in tmem / dS in smem)
-//   dq[rows of tile i] += scale * dQ_i             (TMA reduce-add, fp32)
+//   dq[rows of tile i] += dQ_i                     (TMA reduce-add, fp32)
+//
+// dS carries the score scale: phase 2 forms P^T (scale dP^T - scale delta)
+// with one fused multiply-add against -scale*delta staged by the producer,
+// so dK and dQ come out of the products already scaled.
 //
 // The MMAs run in that order, so phase 1 overlaps dP^T, phase 2 overlaps
 // dV, and the next tile's S^T overlaps the read-back of dQ_i.  Both phases
@@ -299,10 +303,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
         for (int k = 0; k < BM / 32; ++k) {
           // -lse*log2(e), or -inf where P must be 0 (row past the slab, or a
-          // row that sees no key at all), so exp2(s*scale*log2e + it) is P
+          // row that sees no key at all), so exp2(s*scale*log2e + it) is P;
+          // -scale*delta, so scale*(dP - delta) is one FMA
           const int i = lane + 32 * k;
           l2s[i] = lse_r[k] == -INFINITY ? -INFINITY : -lse_r[k] * kLog2e;
-          l2s[BM + i] = dl_r[k];
+          l2s[BM + i] = -a.scale * dl_r[k];
         }
         mbar_arrive(&bars->q_full[st]);
         // dO stage st still holds half of tile n-2's dQ until its reduce has
@@ -482,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       TileCursor cur;
       for (int t; ok && (t = cur.next(nqt, lane, qvis)) >= 0;) {
         const QTile qt = q_tile(gm, t, causal, nk, kmin, kmax);
-        // -lse*log2e and delta of this warpgroup's 64 query columns (staged by warp 8)
+        // -lse*log2e and -scale*delta of this warpgroup's 64 query columns (staged by warp 8)
         const float* nl2 = lse_sm + (n & 1) * 2 * BM + 64 * wg;
         const float* dls = nl2 + BM;
         // phase 1: P^T = exp2(s * scale * log2(e) - lse * log2(e)), kept in fp32
@@ -542,14 +547,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           exps(std::false_type{});
         else
           exps(std::true_type{});
-        // phase 2: dS^T = P^T (dP^T - delta), fp16, to tensor memory (A of the
-        // dK MMAs) and to this warpgroup's dS panel (A of the dQ MMAs)
+        // phase 2: dS^T = scale P^T (dP^T - delta), fp16, to tensor memory (A of
+        // the dK MMAs) and to this warpgroup's dS panel (A of the dQ MMAs)
         // the dS panels hold half of the previous tile's dQ until its reduce
         // has read them
         w = mbar_wait(&bars->dp_full, n & 1, abort, status);
         if (w && n > 0) w = mbar_wait(&bars->ds_free, (n - 1) & 1, abort, status);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         tc_fence_after();
+        const float2 sc2 = make_float2(a.scale, a.scale);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t dr[32];
@@ -564,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             for (int u = 0; u < 2; ++u) {
               const int j = i + 2 * u;
               const float2 pp = make_float2(__uint_as_float(pr[32 * c + j]), __uint_as_float(pr[32 * c + j + 1]));
-              const float2 d = fmul2(pp, fsub2(make_float2(__uint_as_float(dr[j]), __uint_as_float(dr[j + 1])), dp[u]));
+              const float2 d = fmul2(pp, ffma2(make_float2(__uint_as_float(dr[j]), __uint_as_float(dr[j + 1])), sc2, dp[u]));
               dk[j >> 1] = pack_f16x2(d.x, d.y);
             }
           }
@@ -597,19 +603,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         for (int c = 0; c < D / 2; c += 32) tmem_wait_ld32(r + c);
         tc_fence_before();
         mbar_arrive(&bars->tmem_free);
-        // scale * dQ staged for the producer's TMA reduce-add over the dS panels
-        // (warpgroup 0) or this tile's dO (warpgroup 1), both free since the
-        // dQ MMA ran: 32-column boxes of 128 rows, 128B-swizzled like the
-        // reduce's map
+        // dQ (already scaled through dS) staged for the producer's TMA
+        // reduce-add over the dS panels (warpgroup 0) or this tile's dO
+        // (warpgroup 1), both free since the dQ MMA ran: 32-column boxes of
+        // 128 rows, 128B-swizzled like the reduce's map
         uint8_t* stg = smem + (wg == 0 ? L::DS_OFF : L::DO_OFF + (n & 1) * L::TILE) + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
         for (int sub = 0; sub < D / 64; ++sub) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint32_t* x = r + 32 * sub + 4 * j;
-            const float4 v = make_float4(a.scale * __uint_as_float(x[0]), a.scale * __uint_as_float(x[1]),
-                                         a.scale * __uint_as_float(x[2]), a.scale * __uint_as_float(x[3]));
-            *reinterpret_cast<float4*>(stg + sub * PANEL + ((j ^ (row & 7)) << 4)) = v;
+            *reinterpret_cast<uint4*>(stg + sub * PANEL + ((j ^ (row & 7)) << 4)) = make_uint4(x[0], x[1], x[2], x[3]);
           }
         }
         fence_async_smem();
@@ -621,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       }
     }
     if (range_bad) report(status, SCA_ERR_RANGE);
-    // dK (warpgroup 0, times scale) and dV (warpgroup 1): thread = key row,
+    // dK (warpgroup 0, already scaled through dS) and dV (warpgroup 1): thread = key row,
     // staged fp32 in 32-column 128B-swizzled boxes over the K/V tiles (dK)
     // and the Q stages (dV), free since the last MMA completed; one thread
     // per warpgroup then has the TMA unit add them into (accumulate) or
@@ -632,18 +636,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       tc_fence_after();
       const uint32_t src = (wg == 0 ? tdK : tdV) + lane_off;
       uint8_t* stg = smem + (wg == 0 ? L::K_OFF : L::Q_OFF) + (row >> 3) * 1024 + (row & 7) * 128;
-      const float mul = wg == 0 ? a.scale : 1.f;
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
         uint32_t r[32];
         tmem_ld32(src + c, r);
         tmem_wait_ld32(r);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 v = make_float4(mul * __uint_as_float(r[4 * j]), mul * __uint_as_float(r[4 * j + 1]),
-                                       mul * __uint_as_float(r[4 * j + 2]), mul * __uint_as_float(r[4 * j + 3]));
-          *reinterpret_cast<float4*>(stg + (c / 32) * PANEL + ((j ^ (row & 7)) << 4)) = v;
-        }
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(stg + (c / 32) * PANEL + ((j ^ (row & 7)) << 4)) =
+              make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
       }
       fence_async_smem();
       mbar_arrive(&bars->epi_staged[wg]);

@@ -348,13 +348,24 @@ class ShardedCausalAttention:
     def _ring(self, k_home, v_home, launch_step):
         """Run launch_step(t, kv_ptrs(g, r), kv_view, home) for t = 0..P-1
         with the staging copies of step t+1 overlapped on the copy stream;
-        `home` says whether the blocks are read from their home rows."""
+        `home` says whether the blocks are read from their home rows.
+
+        Step t's kernel is enqueued before the copies of step t+1: those
+        copies wait only for step t-1 (the buffer they overwrite), so the
+        host's time spent issuing them overlaps step t on the GPU instead of
+        delaying its launch."""
         cur = torch.cuda.current_stream(self.device)
         ring = self.stage_k is not None
         if ring:
             self.ev_ready.record(cur)
             self.copy_stream.wait_event(self.ev_ready)
         for t in range(self.P):
+            if ring and t >= 1:
+                cur.wait_event(self.ev_staged[t])
+            home = not ring or t == 0
+            view = self._home_kv_view() if home else self._stage_kv_view()
+            launch_step(t, lambda g, r: self._kv_ptrs(k_home, v_home, t, g, r), view, home)
+            self.ev_done[t].record(cur)
             if ring and t + 1 < self.P:
                 with torch.cuda.stream(self.copy_stream):
                     if t >= 1:
@@ -367,12 +378,6 @@ class ShardedCausalAttention:
                         e1.record(self.copy_stream)
                         self.stage_events.append((e0, e1))
                     self.ev_staged[t + 1].record(self.copy_stream)
-            if ring and t >= 1:
-                cur.wait_event(self.ev_staged[t])
-            home = not ring or t == 0
-            view = self._home_kv_view() if home else self._stage_kv_view()
-            launch_step(t, lambda g, r: self._kv_ptrs(k_home, v_home, t, g, r), view, home)
-            self.ev_done[t].record(cur)
         if ring:  # the staging buffers are reused by the next call
             cur.wait_stream(self.copy_stream)
 
