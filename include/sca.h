@@ -192,12 +192,16 @@ int zigzag_permute(const void* src, void* dst, int64_t outer, int64_t S, int64_t
 
 /* ring_stage_block - one ring step's key/value hand-off emulated on one GPU:
  * copy rows [row0, row0 + rows) of every (b, h) of a [outer, S_src, row]
- * tensor into a contiguous [outer, rows, row] staging buffer with the copy
- * engine (one strided 2-D copy), so the next ring step's block is staged
- * while the current one is computed (double buffering of the METP
- * abstract; point-to-point passing of key/value blocks, "Avances en la
- * capacitacion de LLMs de secuencia larga", section "Limitaciones de los
- * Enfoques Existentes").  Errors: SCA_ERR_ARG for out-of-range rows. */
+ * tensor into a contiguous [outer, rows, row] staging buffer, so the next
+ * ring step's block is staged while the current one is computed (double
+ * buffering of the METP abstract; point-to-point passing of key/value
+ * blocks, "Avances en la capacitacion de LLMs de secuencia larga", section
+ * "Limitaciones de los Enfoques Existentes").  When addresses and row sizes
+ * are multiples of 16 bytes the copy is a small kernel (one 64-thread block
+ * per SM, few registers) that runs beside the attention kernels; otherwise
+ * it is one strided 2-D runtime copy.  Issue it on a stream of its own (of
+ * high priority, so its blocks are dispatched first) to overlap it with
+ * compute.  Errors: SCA_ERR_ARG for out-of-range rows. */
 int ring_stage_block(const void* src, void* dst, int64_t outer, int64_t S_src, int64_t row0,
                      int64_t rows, int64_t row_bytes, void* stream);
 
@@ -205,10 +209,11 @@ int ring_stage_block(const void* src, void* dst, int64_t outer, int64_t S_src, i
  * its rows are the `seg->n` segments of `seg->len` rows starting at rows
  * seg->start[i] of every (b, h) of a [outer, S_src, row] tensor (a zigzag
  * shard: chunks r and 2P-1-r), gathered in segment order into a contiguous
- * [outer, seg->n * seg->len, row] staging slab, one strided 2-D copy-engine
- * copy per segment (double buffering of the METP abstract; block passing of
- * "Avances en la capacitacion de LLMs de secuencia larga", section
- * "Limitaciones de los Enfoques Existentes").  The caller owns both buffers;
+ * [outer, seg->n * seg->len, row] staging slab, one strided 2-D copy per
+ * segment (the copy kernel of ring_stage_block, under the same conditions;
+ * double buffering of the METP abstract; block passing of "Avances en la
+ * capacitacion de LLMs de secuencia larga", section "Limitaciones de los
+ * Enfoques Existentes").  The caller owns both buffers;
  * they must not overlap.  Errors: SCA_ERR_ARG for NULL pointers, segment
  * counts outside {1, 2}, rows outside [0, S_src). */
 int ring_stage_segments(const void* src, void* dst, int64_t outer, int64_t S_src, const sca_segs* seg,

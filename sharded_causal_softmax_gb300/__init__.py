@@ -6,7 +6,7 @@ exactly by log-sum-exp rescaling - runs in the CUDA kernels of libsca.so
 behind the C ABI of ``include/sca.h``.  ``capi`` is the ctypes binding of
 that ABI (same function names); ``ShardedCausalAttention`` is the host-side
 schedule of P virtual shards (zigzag or contiguous, ring visiting order with
-double-buffered staging, head groups) on one GPU; ``ShardedLinearAttention``
+multi-buffered staging, head groups; or the double ring) on one GPU; ``ShardedLinearAttention``
 the schedule of causal linear attention over P contiguous shards that pass
 their states point to point (LASP).
 """

@@ -66,6 +66,41 @@ __global__ void __launch_bounds__(kPermThreads) zigzag_permute_kernel(const V* _
   }
 }
 
+// ------------------------------------------------------------ ring hand-off
+//
+// A 2-D copy (height rows of width_vecs 16-byte vectors, source and
+// destination row pitches in vectors) that runs beside the attention
+// kernels: one block of kCopyThreads per SM and few registers, so a block
+// fits next to an attention CTA (which leaves most of an SM's threads and a
+// few thousand registers unused) and the hand-off proceeds while the SMs
+// compute.  Each thread keeps kCopyUnroll loads in flight.
+
+constexpr int kCopyThreads = 64;
+constexpr int kCopyUnroll = 8;
+
+__global__ void __launch_bounds__(kCopyThreads) ring_copy_kernel(const uint4* __restrict__ src,
+                                                                 uint4* __restrict__ dst, int64_t height,
+                                                                 int64_t width_vecs, int64_t spitch,
+                                                                 int64_t dpitch) {
+  // a hand-off's rows are few and wide (one per batch x head): every block
+  // walks every row and strides over its columns
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kCopyThreads * kCopyUnroll;
+  for (int64_t r = 0; r < height; ++r) {
+    const uint4* s = src + r * spitch;
+    uint4* d = dst + r * dpitch;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * kCopyThreads * kCopyUnroll + threadIdx.x; base < width_vecs;
+         base += step) {
+      uint4 v[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u)
+        if (base + u * kCopyThreads < width_vecs) v[u] = s[base + u * kCopyThreads];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u)
+        if (base + u * kCopyThreads < width_vecs) d[base + u * kCopyThreads] = v[u];
+    }
+  }
+}
+
 // ---------------------------------------------------------------- lse merge
 //
 // One group of L = D/4 lanes per row; each lane owns 4 consecutive columns
@@ -329,6 +364,26 @@ extern "C" int zigzag_permute(const void* src, void* dst, int64_t outer, int64_t
   return cuda_status(cudaGetLastError(), "zigzag_permute launch");
 }
 
+// height rows of `width` bytes, pitches in bytes: the hand-off copy kernel
+// when every address and size is a whole number of 16-byte vectors, else
+// the runtime's 2-D copy.
+static int stage_copy(void* dst, int64_t dpitch, const void* src, int64_t spitch, int64_t width, int64_t height,
+                      cudaStream_t st, const char* what) {
+  if (width == 0 || height == 0) return SCA_OK;
+  if (aligned(src, 16) && aligned(dst, 16) && width % 16 == 0 && spitch % 16 == 0 && dpitch % 16 == 0) {
+    const int64_t per = static_cast<int64_t>(kCopyThreads) * kCopyUnroll;
+    const int64_t blocks = (width / 16 + per - 1) / per;
+    const int grid = static_cast<int>(blocks < sm_count() ? blocks : sm_count());
+    ring_copy_kernel<<<grid, kCopyThreads, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), height,
+                                                    width / 16, spitch / 16, dpitch / 16);
+    return cuda_status(cudaGetLastError(), what);
+  }
+  return cuda_status(cudaMemcpy2DAsync(dst, static_cast<size_t>(dpitch), src, static_cast<size_t>(spitch),
+                                       static_cast<size_t>(width), static_cast<size_t>(height),
+                                       cudaMemcpyDeviceToDevice, st),
+                     what);
+}
+
 extern "C" int ring_stage_block(const void* src, void* dst, int64_t outer, int64_t S_src, int64_t row0,
                                 int64_t rows, int64_t row_bytes, void* stream) {
   SCA_REQUIRE(src && dst, SCA_ERR_ARG, "ring_stage_block: NULL pointer");
@@ -337,11 +392,8 @@ extern "C" int ring_stage_block(const void* src, void* dst, int64_t outer, int64
               static_cast<long long>(row0 + rows), static_cast<long long>(S_src));
   if (outer == 0 || rows == 0) return SCA_OK;
   const char* s = static_cast<const char*>(src) + row0 * row_bytes;
-  const cudaError_t e =
-      cudaMemcpy2DAsync(dst, static_cast<size_t>(rows * row_bytes), s, static_cast<size_t>(S_src * row_bytes),
-                        static_cast<size_t>(rows * row_bytes), static_cast<size_t>(outer),
-                        cudaMemcpyDeviceToDevice, as_stream(stream));
-  return cuda_status(e, "ring_stage_block copy");
+  return stage_copy(dst, rows * row_bytes, s, S_src * row_bytes, rows * row_bytes, outer, as_stream(stream),
+                    "ring_stage_block copy");
 }
 
 extern "C" int ring_stage_segments(const void* src, void* dst, int64_t outer, int64_t S_src, const sca_segs* seg,
@@ -362,10 +414,10 @@ extern "C" int ring_stage_segments(const void* src, void* dst, int64_t outer, in
               SCA_ERR_ARG, "ring_stage_segments: src and dst overlap");
   for (int i = 0; i < seg->n; ++i) {
     const char* s = static_cast<const char*>(src) + seg->start[i] * row_bytes;
-    const cudaError_t e = cudaMemcpy2DAsync(static_cast<char*>(dst) + i * width, dpitch, s,
-                                            static_cast<size_t>(S_src * row_bytes), width,
-                                            static_cast<size_t>(outer), cudaMemcpyDeviceToDevice, as_stream(stream));
-    if (e != cudaSuccess) return cuda_status(e, "ring_stage_segments copy");
+    const int rc = stage_copy(static_cast<char*>(dst) + i * width, static_cast<int64_t>(dpitch), s,
+                              S_src * row_bytes, static_cast<int64_t>(width), outer, as_stream(stream),
+                              "ring_stage_segments copy");
+    if (rc != SCA_OK) return rc;
   }
   return SCA_OK;
 }

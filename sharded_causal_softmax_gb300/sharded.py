@@ -19,10 +19,11 @@ The schedule (host logic only; every byte is moved or computed by libsca):
   step t rank (g, r) holds key/value block (r - t) mod P and computes the
   (o, lse) partial of its queries against it.  With the "ring" schedule the
   blocks move like a ring pass: before step t+1, each rank's staging buffer
-  receives the block its left neighbour holds at step t, copied by the copy
-  engine on a side stream into the spare one of two staging buffers while
-  step t computes (the double buffer of the METP abstract, FITEE
-  10.1631/FITEE.2400602).  The "direct" schedule reads every block from its
+  receives the block its left neighbour holds at step t, copied by a small
+  copy kernel on a high-priority side stream into a spare staging buffer
+  while the steps before it compute (the double buffer of the METP
+  abstract, FITEE 10.1631/FITEE.2400602; three buffers from P = 4 on, so
+  each copy overlaps two steps).  The "direct" schedule reads every block from its
   home rows (the K/V all-gather reading of the TSP page); its forward
   partials of all P steps are independent and go out together, up to
   SCA_MAX_ITEMS (query shard, block) items per launch.
@@ -200,8 +201,12 @@ class ShardedCausalAttention:
         self.lse = z(B, H, S)
         self.o_bf16 = z(B, H, S, D, dt=torch.bfloat16) if bf16_out else None
         ring = schedule == "ring" and P > 1
-        self.stage_k = [z(self.G, P, B, self.Hkvg, self.n_r, D, dt=dtype) for _ in range(2)] if ring else None
-        self.stage_v = [z(self.G, P, B, self.Hkvg, self.n_r, D, dt=dtype) for _ in range(2)] if ring else None
+        # staging buffers: step t reads buffer t % n_stage, and the copy that
+        # fills it for step t+1 may start once step t+1-n_stage is done.  With
+        # three, each hand-off has two steps of compute to hide behind.
+        self.n_stage = 3 if P > 3 else 2
+        self.stage_k = [z(self.G, P, B, self.Hkvg, self.n_r, D, dt=dtype) for _ in range(self.n_stage)] if ring else None
+        self.stage_v = [z(self.G, P, B, self.Hkvg, self.n_r, D, dt=dtype) for _ in range(self.n_stage)] if ring else None
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         if backward:
             self.delta = z(B, H, S)
@@ -220,7 +225,10 @@ class ShardedCausalAttention:
         self.f16_in = f16_input_flags(backward and f16_staging, dtype, algo, H, Hkv)
         self.q16 = z(B, H, S, D, dt=torch.float16) if self.f16_in else None
         self.do16 = z(B, H, S, D, dt=torch.float16) if self.f16_in & capi.SCA_F16_DOUT else None
-        self.copy_stream = torch.cuda.Stream(device=dev) if ring else None
+        # the hand-offs run on a stream of their own, at high priority: their
+        # small copy blocks are dispatched ahead of attention CTAs and fit
+        # beside them on the SMs
+        self.copy_stream = torch.cuda.Stream(device=dev, priority=-1) if ring else None
         self.ev_ready = torch.cuda.Event()
         self.ev_staged = [torch.cuda.Event() for _ in range(P)]
         self.ev_done = [torch.cuda.Event() for _ in range(P)]
@@ -309,7 +317,7 @@ class ShardedCausalAttention:
         if self.stage_k is None or t == 0:
             off = self._kv_rows(g, self.block(r, t)) * self.D * self.eb
             return _ptr(k_home) + off, _ptr(v_home) + off
-        buf = t % 2
+        buf = t % self.n_stage
         return _ptr(self.stage_k[buf][g, r]), _ptr(self.stage_v[buf][g, r])
 
     def _stage(self, k_home, v_home, t_next):
@@ -319,7 +327,8 @@ class ShardedCausalAttention:
         its group, or a rank of the previous group on an outer hop)."""
         P, B, Hg, n_r, D, eb = self.P, self.B, self.Hkvg, self.n_r, self.D, self.eb
         cs = self.copy_stream.cuda_stream
-        dst_k, dst_v = self.stage_k[t_next % 2], self.stage_v[t_next % 2]
+        ns = self.n_stage
+        dst_k, dst_v = self.stage_k[t_next % ns], self.stage_v[t_next % ns]
         row = D * eb
         blk = B * Hg * n_r
         for g in range(self.G):
@@ -338,7 +347,7 @@ class ShardedCausalAttention:
                             self.launches += 1
                             self.staged_bytes += Hg * n_r * row
             else:             # the senders' staged blocks: one copy per run of consecutive ranks
-                src_k, src_v = self.stage_k[(t_next - 1) % 2], self.stage_v[(t_next - 1) % 2]
+                src_k, src_v = self.stage_k[(t_next - 1) % ns], self.stage_v[(t_next - 1) % ns]
                 for r0, s0, n in copy_runs(hop_senders(self.block, t_next, P)):
                     for src, dst in ((src_k, dst_k), (src_v, dst_v)):
                         capi.ring_stage_block(_ptr(src[g, s0]), _ptr(dst[g, r0]), 1, n * blk, 0, n * blk, row, cs)
@@ -351,9 +360,9 @@ class ShardedCausalAttention:
         `home` says whether the blocks are read from their home rows.
 
         Step t's kernel is enqueued before the copies of step t+1: those
-        copies wait only for step t-1 (the buffer they overwrite), so the
-        host's time spent issuing them overlaps step t on the GPU instead of
-        delaying its launch."""
+        copies wait only for the step that last read the buffer they
+        overwrite (t+1-n_stage), so the host's time spent issuing them
+        overlaps step t on the GPU instead of delaying its launch."""
         cur = torch.cuda.current_stream(self.device)
         ring = self.stage_k is not None
         if ring:
@@ -368,8 +377,10 @@ class ShardedCausalAttention:
             self.ev_done[t].record(cur)
             if ring and t + 1 < self.P:
                 with torch.cuda.stream(self.copy_stream):
-                    if t >= 1:
-                        self.copy_stream.wait_event(self.ev_done[t - 1])
+                    # the buffer this copy fills was last read by step
+                    # t+1-n_stage (step 0 reads home rows, no buffer)
+                    if t + 1 - self.n_stage >= 1:
+                        self.copy_stream.wait_event(self.ev_done[t + 1 - self.n_stage])
                     if self.stage_events is not None:
                         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                         e0.record(self.copy_stream)
