@@ -183,12 +183,16 @@ int attn_merge_lse(const float* o_parts, const float* lse_parts, int n, int64_t 
  * 2P-1-r (TSP page, "Zyphra presenta el paralelismo de secuencia y tensor
  * (TSP)", section "Lo que realmente significa plegar": K/V are reordered in
  * zigzag before FlashAttention to balance causal work).  inverse = 1 undoes
- * it.  A pure copy (bit exact).  src and dst must not overlap.
+ * it.  A pure copy (bit exact).  src and dst must not overlap.  When both
+ * pointers and the chunk size (S/(2P) * row_bytes) are multiples of 16
+ * bytes, the chunks move by bulk copies through shared memory (the TMA
+ * unit); a bounded wait that gives up records SCA_ERR_TIMEOUT in
+ * *dev_status (may be NULL).  Otherwise a vectorised copy kernel moves them.
  * Errors: SCA_ERR_ARG for S % (2P) != 0, P < 1, row_bytes not a positive
  * multiple of 4, overlapping buffers; SCA_ERR_ALIGN if pointers are not
  * 4-byte aligned. */
 int zigzag_permute(const void* src, void* dst, int64_t outer, int64_t S, int64_t row_bytes,
-                   int P, int inverse, void* stream);
+                   int P, int inverse, int* dev_status, void* stream);
 
 /* ring_stage_block - one ring step's key/value hand-off emulated on one GPU:
  * copy rows [row0, row0 + rows) of every (b, h) of a [outer, S_src, row]

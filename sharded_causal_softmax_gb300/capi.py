@@ -84,7 +84,7 @@ def _load():
         "attn_fwd_shard": (c_int, [POINTER(sca_fwd_item), c_int, POINTER(sca_attn_dims), c_void_p, c_void_p]),
         "attn_merge_lse": (c_int, [c_void_p, c_void_p, c_int, c_int64, c_int, c_int64, c_int64, c_void_p,
                                    c_void_p, c_void_p, c_int, c_int64, c_void_p]),
-        "zigzag_permute": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int, c_int, c_void_p]),
+        "zigzag_permute": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int, c_int, c_void_p, c_void_p]),
         "ring_stage_block": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_int64, c_void_p]),
         "ring_stage_segments": (c_int, [c_void_p, c_void_p, c_int64, c_int64, POINTER(sca_segs), c_int64, c_void_p]),
         "attn_bwd_shard": (c_int, [POINTER(sca_bwd_item), c_int, POINTER(sca_attn_dims), c_void_p, c_void_p]),
@@ -158,8 +158,8 @@ def attn_merge_lse(o_parts: int, lse_parts: int, n: int, rows: int, D: int, o_pa
 
 
 def zigzag_permute(src: int, dst: int, outer: int, S: int, row_bytes: int, P: int, inverse: int,
-                   stream: int) -> int:
-    return check(lib().zigzag_permute(src, dst, outer, S, row_bytes, P, inverse, stream))
+                   dev_status: int, stream: int) -> int:
+    return check(lib().zigzag_permute(src, dst, outer, S, row_bytes, P, inverse, dev_status, stream))
 
 
 def ring_stage_block(src: int, dst: int, outer: int, S_src: int, row0: int, rows: int, row_bytes: int,

@@ -5,8 +5,11 @@
 
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "host_common.h"
+#include "ptx.cuh"
 
 namespace sca {
 
@@ -66,6 +69,75 @@ __global__ void __launch_bounds__(kPermThreads) zigzag_permute_kernel(const V* _
   }
 }
 
+// The same permute by bulk copies.  Every chunk is contiguous in both
+// tensors, so it is cut into pieces of up to kBulkPiece bytes, each moved
+// global -> shared -> global by the TMA unit.  One thread drives a block:
+// loads run kBulkStages-1 pieces ahead of the stores, and a stage is
+// reloaded once the store that used it has read it.  Two blocks per SM keep
+// ~128 KB of loads and as many stores in flight per SM.  Waits are bounded:
+// one that gives up records SCA_ERR_TIMEOUT and ends the block.
+
+constexpr int kBulkStages = 3;
+constexpr int kBulkPiece = 32 * 1024;
+constexpr int kBulkSmem = kBulkStages * kBulkPiece + 64;
+
+__global__ void __launch_bounds__(32) zigzag_permute_bulk_kernel(const uint8_t* __restrict__ src,
+                                                                 uint8_t* __restrict__ dst, int64_t nseg,
+                                                                 int64_t chunk_bytes, int64_t pieces_per_chunk,
+                                                                 int P, int inverse, int* status) {
+  extern __shared__ __align__(128) uint8_t bsm[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(bsm + kBulkStages * kBulkPiece);
+  int* abort = reinterpret_cast<int*>(full + kBulkStages);
+  if (threadIdx.x != 0) return;   // one thread drives the copies
+  for (int s = 0; s < kBulkStages; ++s) mbar_init(&full[s], 1);
+  *abort = 0;
+  fence_mbar_init();
+  const int two_p = 2 * P;
+  const int64_t n_pieces = nseg * pieces_per_chunk;
+  const int64_t mine = n_pieces > blockIdx.x ? (n_pieces - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  auto locate = [&](int64_t i, const uint8_t*& s, uint8_t*& d, uint32_t& bytes) {
+    const int64_t p = blockIdx.x + i * gridDim.x;
+    const int64_t g = p / pieces_per_chunk;                 // destination chunk (o, ch)
+    const int64_t off = (p - g * pieces_per_chunk) * kBulkPiece;
+    const int64_t o = g / two_p;
+    const int ch = static_cast<int>(g - o * two_p);
+    s = src + (o * two_p + zz_src_chunk(ch, P, inverse)) * chunk_bytes + off;
+    d = dst + g * chunk_bytes + off;
+    bytes = static_cast<uint32_t>(min64(kBulkPiece, chunk_bytes - off));
+  };
+  constexpr int kAhead = kBulkStages - 1;
+  for (int64_t i = 0; i < mine + kAhead; ++i) {
+    const int64_t j = i - kAhead;   // the piece stored this iteration
+    if (j >= 0 && j < mine) {
+      const int st = static_cast<int>(j % kBulkStages);
+      if (!mbar_wait(&full[st], static_cast<uint32_t>((j / kBulkStages) & 1), abort, status)) break;
+      const uint8_t* s;
+      uint8_t* d;
+      uint32_t bytes;
+      locate(j, s, d, bytes);
+      bulk_store(d, bsm + st * kBulkPiece, bytes);
+      bulk_commit();
+    }
+    if (i < mine) {
+      const int st = static_cast<int>(i % kBulkStages);
+      // the stage's previous piece (i - kBulkStages) was stored last
+      // iteration: let that store read it (the one just issued may pend)
+      if (i >= kBulkStages) bulk_wait_read<1>();
+      const uint8_t* s;
+      uint8_t* d;
+      uint32_t bytes;
+      locate(i, s, d, bytes);
+      mbar_arrive_expect_tx(&full[st], bytes);
+      bulk_load(bsm + st * kBulkPiece, s, bytes, &full[st]);
+    }
+  }
+  if (*abort) {   // let loads still in flight land before the block's shared memory goes away
+    for (int64_t i = (mine > kBulkStages ? mine - kBulkStages : 0); i < mine; ++i)
+      mbar_wait_drain(&full[i % kBulkStages], static_cast<uint32_t>((i / kBulkStages) & 1));
+  }
+  bulk_wait_read<0>();   // every store has read shared memory before the block exits
+}
+
 // ------------------------------------------------------------ ring hand-off
 //
 // A 2-D copy (height rows of width_vecs 16-byte vectors, source and
@@ -108,7 +180,9 @@ __global__ void __launch_bounds__(kCopyThreads) ring_copy_kernel(const uint4* __
 // lanes of the group and reduced with shuffles.
 
 constexpr int kMergeThreads = 256;
-constexpr int kMergeFastN = 4;  // up to this many partials: all their loads issued at once
+// up to NF partials (a template parameter, 4 or 8) every load of a row is
+// issued at once; more go through the two-pass path
+constexpr int kMergeMaxFast = 8;
 
 __device__ __forceinline__ int64_t zz_natural_row(int64_t row, int64_t S, int P) {
   const int64_t o = row / S;
@@ -125,7 +199,7 @@ __device__ __forceinline__ int64_t zz_natural_row(int64_t row, int64_t S, int P)
 // and every lane of a row's group has finished reading before any lane of
 // the group stores (the lse of a row is read by all L lanes and written by
 // lane 0).
-template <int L>
+template <int L, int NF>
 __global__ void __launch_bounds__(kMergeThreads) merge_lse_kernel(
     const float* o_parts, const float* lse_parts, int n, int64_t rows,
     int64_t ops, int64_t lps, float* o_out, float* lse_out, __nv_bfloat16* ob_out, int uP, int64_t S) {
@@ -142,25 +216,25 @@ __global__ void __launch_bounds__(kMergeThreads) merge_lse_kernel(
     float M = -INFINITY;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
-    if (n <= kMergeFastN) {
+    if (n <= NF) {
       // every partial's o chunk and lse issued together (one round trip to
       // memory per row, not two), then the same sums in the same order as
       // the general path below
       if (active) {
-        float4 v[kMergeFastN];
-        float w[kMergeFastN];
+        float4 v[NF];
+        float w[NF];
 #pragma unroll
-        for (int u = 0; u < kMergeFastN; ++u)
+        for (int u = 0; u < NF; ++u)
           if (u < n) {
             v[u] = *reinterpret_cast<const float4*>(o_parts + u * ops + row * D + 4 * li);
             w[u] = lse_parts[u * lps + row];
           }
 #pragma unroll
-        for (int u = 0; u < kMergeFastN; ++u)
+        for (int u = 0; u < NF; ++u)
           if (u < n) M = fmaxf(M, w[u]);
         const float M0 = (M == -INFINITY) ? 0.f : M;
 #pragma unroll
-        for (int u = 0; u < kMergeFastN; ++u)
+        for (int u = 0; u < NF; ++u)
           if (u < n) {
             const float wu = expf(w[u] - M0);   // exp(-inf) = 0 for empty partials
             wsum += wu;
@@ -328,7 +402,7 @@ extern "C" int cast_bf16_to_f16(const void* src, void* dst, int64_t n, int* dev_
 }
 
 extern "C" int zigzag_permute(const void* src, void* dst, int64_t outer, int64_t S, int64_t row_bytes, int P,
-                              int inverse, void* stream) {
+                              int inverse, int* dev_status, void* stream) {
   SCA_REQUIRE(src && dst, SCA_ERR_ARG, "zigzag_permute: NULL pointer");
   SCA_REQUIRE(P >= 1, SCA_ERR_ARG, "zigzag_permute: P=%d must be >= 1", P);
   SCA_REQUIRE(outer >= 0 && S >= 0, SCA_ERR_ARG, "zigzag_permute: negative size");
@@ -344,6 +418,30 @@ extern "C" int zigzag_permute(const void* src, void* dst, int64_t outer, int64_t
   const int64_t chunk_bytes = (S / (2 * P)) * row_bytes;
   const int64_t nseg = outer * 2 * P;
   const bool vec16 = chunk_bytes % 16 == 0 && aligned(src, 16) && aligned(dst, 16);
+  cudaStream_t st = as_stream(stream);
+  if (vec16) {   // bulk copies through shared memory
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64) {
+      std::lock_guard<std::mutex> g(mu);
+      if (!attr_set[dev]) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(zigzag_permute_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmem);
+        if (e != cudaSuccess) return cuda_status(e, "zigzag_permute attribute");
+        attr_set[dev] = true;
+      }
+      const int64_t ppc = (chunk_bytes + kBulkPiece - 1) / kBulkPiece;
+      const int64_t n_pieces = nseg * ppc;
+      const int64_t blocks = static_cast<int64_t>(sm_count()) * 2;
+      const unsigned grid = static_cast<unsigned>(n_pieces < blocks ? n_pieces : blocks);
+      zigzag_permute_bulk_kernel<<<grid, 32, kBulkSmem, st>>>(static_cast<const uint8_t*>(src),
+                                                              static_cast<uint8_t*>(dst), nseg, chunk_bytes, ppc, P,
+                                                              inverse, dev_status);
+      return cuda_status(cudaGetLastError(), "zigzag_permute launch");
+    }
+  }
   const int64_t vsz = vec16 ? 16 : 4;
   const int64_t chunk_vecs = chunk_bytes / vsz;
   const int64_t tile = static_cast<int64_t>(kPermThreads) * kPermUnroll;
@@ -352,7 +450,6 @@ extern "C" int zigzag_permute(const void* src, void* dst, int64_t outer, int64_t
   const int64_t resident = static_cast<int64_t>(sm_count()) * (2048 / kPermThreads);
   const int64_t n_tiles = nseg * tiles_per_chunk;
   const unsigned grid = static_cast<unsigned>(n_tiles < resident ? n_tiles : resident);
-  cudaStream_t st = as_stream(stream);
   if (vec16)
     zigzag_permute_kernel<uint4><<<grid, kPermThreads, 0, st>>>(static_cast<const uint4*>(src),
                                                                 static_cast<uint4*>(dst), nseg, chunk_vecs,
@@ -465,11 +562,15 @@ extern "C" int attn_merge_lse(const float* o_parts, const float* lse_parts, int 
   const int grid = grid_for(warps * 32, kMergeThreads);
   cudaStream_t st = as_stream(stream);
   auto* ob = static_cast<__nv_bfloat16*>(o_bf16_out);
-#define SCA_MERGE_CASE(LL)                                                                             \
-  case LL:                                                                                             \
-    merge_lse_kernel<LL><<<grid, kMergeThreads, 0, st>>>(o_parts, lse_parts, n, rows, o_part_stride,   \
-                                                         lse_part_stride, o_out, lse_out, ob,         \
-                                                         unpermute_P, S);                              \
+#define SCA_MERGE_CASE(LL)                                                                               \
+  case LL:                                                                                               \
+    if (n <= 4)                                                                                          \
+      merge_lse_kernel<LL, 4><<<grid, kMergeThreads, 0, st>>>(o_parts, lse_parts, n, rows, o_part_stride,  \
+                                                              lse_part_stride, o_out, lse_out, ob,        \
+                                                              unpermute_P, S);                             \
+    else                                                                                                 \
+      merge_lse_kernel<LL, kMergeMaxFast><<<grid, kMergeThreads, 0, st>>>(                                \
+          o_parts, lse_parts, n, rows, o_part_stride, lse_part_stride, o_out, lse_out, ob, unpermute_P, S); \
     break;
   switch (L) {
     SCA_MERGE_CASE(1)

@@ -244,7 +244,7 @@ class ShardedCausalAttention:
 
     def _permute(self, src, dst, row_bytes, inverse, stream):
         capi.zigzag_permute(_ptr(src), _ptr(dst), src.numel() // (self.S * (row_bytes // src.element_size())),
-                            self.S, row_bytes, self.P, inverse, stream)
+                            self.S, row_bytes, self.P, inverse, _ptr(self.status), stream)
         self.launches += 1
         self.kernels += 1
 

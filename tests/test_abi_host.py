@@ -234,13 +234,13 @@ def test_cast_rejects_bad_arguments(lib):
 
 def test_permute_rejects_bad_arguments(lib):
     f = lib.zigzag_permute
-    assert f(A, 2 * A, 4, 100, 256, 4, 0, None) == capi.SCA_ERR_ARG           # 100 % 8 != 0
-    assert f(A, 2 * A, 4, 64, 256, 0, 0, None) == capi.SCA_ERR_ARG             # P = 0
-    assert f(A, 2 * A, 4, 64, 6, 4, 0, None) == capi.SCA_ERR_ARG               # row bytes not x4
-    assert f(None, 2 * A, 4, 64, 256, 4, 0, None) == capi.SCA_ERR_ARG
-    assert f(A, A + 256, 4, 64, 256, 4, 0, None) == capi.SCA_ERR_ARG           # overlap
-    assert f(A + 2, 2 * A, 4, 64, 256, 4, 0, None) == capi.SCA_ERR_ALIGN
-    assert f(A, 2 * A, 0, 64, 256, 4, 0, None) == capi.SCA_OK                  # empty: nothing to do
+    assert f(A, 2 * A, 4, 100, 256, 4, 0, None, None) == capi.SCA_ERR_ARG           # 100 % 8 != 0
+    assert f(A, 2 * A, 4, 64, 256, 0, 0, None, None) == capi.SCA_ERR_ARG             # P = 0
+    assert f(A, 2 * A, 4, 64, 6, 4, 0, None, None) == capi.SCA_ERR_ARG               # row bytes not x4
+    assert f(None, 2 * A, 4, 64, 256, 4, 0, None, None) == capi.SCA_ERR_ARG
+    assert f(A, A + 256, 4, 64, 256, 4, 0, None, None) == capi.SCA_ERR_ARG           # overlap
+    assert f(A + 2, 2 * A, 4, 64, 256, 4, 0, None, None) == capi.SCA_ERR_ALIGN
+    assert f(A, 2 * A, 0, 64, 256, 4, 0, None, None) == capi.SCA_OK                  # empty: nothing to do
 
 
 def test_merge_rejects_bad_arguments(lib):
@@ -284,7 +284,7 @@ def test_stage_and_delta_reject_bad_arguments(lib):
 
 def test_binding_raises_with_message(lib):
     with pytest.raises(capi.ScaError) as e:
-        capi.zigzag_permute(A, 2 * A, 4, 100, 256, 4, 0, 0)
+        capi.zigzag_permute(A, 2 * A, 4, 100, 256, 4, 0, 0, 0)
     assert "SCA_ERR_ARG" in str(e.value) and "divisible" in str(e.value)
 
 

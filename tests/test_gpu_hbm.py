@@ -24,21 +24,25 @@ def _stream():
 
 @pytest.mark.parametrize("dtype,D,P,S", [
     (torch.bfloat16, 128, 4, 8192), (torch.bfloat16, 128, 8, 1024), (torch.float32, 128, 4, 512),
-    (torch.bfloat16, 64, 2, 12), (torch.float32, 1, 4, 8 * 33), (torch.bfloat16, 128, 1, 256)])
+    (torch.bfloat16, 64, 2, 12), (torch.float32, 1, 4, 8 * 33), (torch.bfloat16, 128, 1, 256),
+    # chunks of 200 rows x 256 B = 51200 B: bulk pieces of 32 KB and a ragged 18 KB one
+    (torch.bfloat16, 128, 3, 1200)])
 def test_zigzag_permute_bit_exact(sca, dtype, D, P, S):
     g = torch.Generator().manual_seed(5)
     x = torch.randn(2, 3, S, D, generator=g).to(dtype)
     xd = x.cuda()
     y = torch.empty_like(xd)
     row = D * x.element_size()
-    sca.zigzag_permute(xd.data_ptr(), y.data_ptr(), 6, S, row, P, 0, _stream())
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sca.zigzag_permute(xd.data_ptr(), y.data_ptr(), 6, S, row, P, 0, status.data_ptr(), _stream())
     order = oracle.zigzag_order(S, P)
     ref = x[..., torch.as_tensor(order), :]
     assert torch.equal(y.cpu().view(torch.int16 if dtype == torch.bfloat16 else torch.int32),
                        ref.view(torch.int16 if dtype == torch.bfloat16 else torch.int32))
     back = torch.empty_like(xd)
-    sca.zigzag_permute(y.data_ptr(), back.data_ptr(), 6, S, row, P, 1, _stream())
+    sca.zigzag_permute(y.data_ptr(), back.data_ptr(), 6, S, row, P, 1, status.data_ptr(), _stream())
     assert torch.equal(back.cpu(), x)
+    assert sca.sca_read_status(status.data_ptr(), _stream()) == 0
 
 
 def test_zigzag_permute_full_size_bit_exact(sca):
@@ -46,7 +50,7 @@ def test_zigzag_permute_full_size_bit_exact(sca):
     g = torch.Generator().manual_seed(9)
     x = torch.randn(1, 16, 32768, 128, generator=g).to(torch.bfloat16).cuda()
     y = torch.empty_like(x)
-    sca.zigzag_permute(x.data_ptr(), y.data_ptr(), 16, 32768, 256, 4, 0, _stream())
+    sca.zigzag_permute(x.data_ptr(), y.data_ptr(), 16, 32768, 256, 4, 0, 0, _stream())
     order = torch.as_tensor(oracle.zigzag_order(32768, 4), device="cuda")
     assert torch.equal(y, x[..., order, :])
 
