@@ -223,6 +223,29 @@ int ring_stage_block(const void* src, void* dst, int64_t outer, int64_t S_src, i
 int ring_stage_segments(const void* src, void* dst, int64_t outer, int64_t S_src, const sca_segs* seg,
                         int64_t row_bytes, void* stream);
 
+/* One strided 2-D copy of a ring hand-off: `height` rows of `width` bytes,
+ * row r from src + r * src_pitch to dst + r * dst_pitch (pitches in bytes). */
+typedef struct {
+  const void* src;
+  void* dst;
+  int64_t height, width, src_pitch, dst_pitch;
+} sca_copy;
+
+#define SCA_MAX_COPIES 128
+
+/* ring_stage_copies - every copy of one ring hand-off (the blocks all ranks
+ * receive for the next step, gathered from home rows or passed on from a
+ * neighbour's staging buffer) in one launch of the hand-off copy kernel (one
+ * 64-thread block per SM, few registers: it runs beside the attention
+ * kernels; double buffering of the METP abstract).  Up to SCA_MAX_COPIES
+ * copies; pointers 16-byte aligned, widths and pitches multiples of 16
+ * bytes, pitches at least the width; no copy's source may overlap its own
+ * destination, and no copy may write what another copy of the call reads or
+ * writes (they run concurrently).  Issue it on a stream of its own, of high
+ * priority, to overlap it with compute.  Errors: SCA_ERR_ARG (count, NULL,
+ * sizes, overlap), SCA_ERR_ALIGN. */
+int ring_stage_copies(const sca_copy* copies, int n, void* stream);
+
 /* One (query shard, key/value block) work item of the backward.  dq, dk, dv
  * are fp32: with dims->accumulate = 1 the item ADDS its contribution, with 0
  * it overwrites them (every row of dq and of dk/dv is written, also rows

@@ -32,8 +32,10 @@ SCA_ALGO_TC = 2
 SCA_MAX_ITEMS = 32
 SCA_F16_Q = 1
 SCA_F16_DOUT = 2
+SCA_MAX_COPIES = 128
 
 EXPORTED = ("attn_fwd_shard", "attn_merge_lse", "zigzag_permute", "ring_stage_block", "ring_stage_segments",
+            "ring_stage_copies",
             "attn_bwd_shard", "attn_bwd_delta", "cast_bf16_to_f16", "lasp_block_states", "lasp_scan",
             "lasp_exchange", "lasp_fwd", "lasp_bwd", "lasp_fwd_noalloc", "sca_selftest_wait_timeout",
             "sca_last_error", "sca_read_status", "sca_version")
@@ -63,6 +65,11 @@ class sca_attn_dims(ctypes.Structure):
                 ("f16_inputs", c_int32)]
 
 
+class sca_copy(ctypes.Structure):
+    _fields_ = [("src", c_void_p), ("dst", c_void_p), ("height", c_int64), ("width", c_int64),
+                ("src_pitch", c_int64), ("dst_pitch", c_int64)]
+
+
 class sca_fwd_item(ctypes.Structure):
     _fields_ = [("q", c_void_p), ("k", c_void_p), ("v", c_void_p), ("o", c_void_p), ("lse", c_void_p),
                 ("q_pos", sca_segs), ("kv_pos", sca_segs)]
@@ -87,6 +94,7 @@ def _load():
         "zigzag_permute": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int, c_int, c_void_p, c_void_p]),
         "ring_stage_block": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_int64, c_void_p]),
         "ring_stage_segments": (c_int, [c_void_p, c_void_p, c_int64, c_int64, POINTER(sca_segs), c_int64, c_void_p]),
+        "ring_stage_copies": (c_int, [POINTER(sca_copy), c_int, c_void_p]),
         "attn_bwd_shard": (c_int, [POINTER(sca_bwd_item), c_int, POINTER(sca_attn_dims), c_void_p, c_void_p]),
         "attn_bwd_delta": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int64, c_int, c_void_p]),
         "cast_bf16_to_f16": (c_int, [c_void_p, c_void_p, c_int64, c_void_p, c_void_p]),
@@ -170,6 +178,17 @@ def ring_stage_block(src: int, dst: int, outer: int, S_src: int, row0: int, rows
 def ring_stage_segments(src: int, dst: int, outer: int, S_src: int, seg: sca_segs, row_bytes: int,
                         stream: int) -> int:
     return check(lib().ring_stage_segments(src, dst, outer, S_src, ctypes.byref(seg), row_bytes, stream))
+
+
+def ring_stage_copies(copies, stream: int) -> int:
+    arr = (sca_copy * max(1, len(copies)))(*copies)
+    return check(lib().ring_stage_copies(arr, len(copies), stream))
+
+
+def copy2d(src: int, dst: int, height: int, width: int, src_pitch: int, dst_pitch: int) -> sca_copy:
+    c = sca_copy()
+    c.src, c.dst, c.height, c.width, c.src_pitch, c.dst_pitch = src, dst, height, width, src_pitch, dst_pitch
+    return c
 
 
 def lasp_block_states(a: int, b: int, dtype: int, st: int, BH: int, S: int, D: int, block: int, dev_status: int,

@@ -140,35 +140,54 @@ __global__ void __launch_bounds__(32) zigzag_permute_bulk_kernel(const uint8_t* 
 
 // ------------------------------------------------------------ ring hand-off
 //
-// A 2-D copy (height rows of width_vecs 16-byte vectors, source and
-// destination row pitches in vectors) that runs beside the attention
-// kernels: one block of kCopyThreads per SM and few registers, so a block
-// fits next to an attention CTA (which leaves most of an SM's threads and a
-// few thousand registers unused) and the hand-off proceeds while the SMs
-// compute.  Each thread keeps kCopyUnroll loads in flight.
+// Every copy of one hand-off (strided 2-D copies of 16-byte vectors) in one
+// launch of one block of kCopyThreads per SM at few registers: a block
+// fits next to an attention CTA (which leaves a few thousand registers and
+// most of an SM's threads unused), so the hand-off proceeds while the SMs
+// compute.  The copies are cut into units of one row by kCopySlice vectors
+// (16 KB); block b takes units b, b + grid, ...  Each thread keeps
+// kCopyUnroll 16-byte loads in flight.
 
 constexpr int kCopyThreads = 64;
-constexpr int kCopyUnroll = 8;
+constexpr int kCopyUnroll = 12;
+constexpr int kCopySlice = kCopyThreads * kCopyUnroll;   // vectors per unit
 
-__global__ void __launch_bounds__(kCopyThreads) ring_copy_kernel(const uint4* __restrict__ src,
-                                                                 uint4* __restrict__ dst, int64_t height,
-                                                                 int64_t width_vecs, int64_t spitch,
-                                                                 int64_t dpitch) {
-  // a hand-off's rows are few and wide (one per batch x head): every block
-  // walks every row and strides over its columns
-  const int64_t step = static_cast<int64_t>(gridDim.x) * kCopyThreads * kCopyUnroll;
-  for (int64_t r = 0; r < height; ++r) {
-    const uint4* s = src + r * spitch;
-    uint4* d = dst + r * dpitch;
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * kCopyThreads * kCopyUnroll + threadIdx.x; base < width_vecs;
-         base += step) {
-      uint4 v[kCopyUnroll];
+struct CopyJob {
+  const uint4* src;
+  uint4* dst;
+  int64_t spitch, dpitch;     // row pitches, vectors
+  int32_t height, width;      // rows, vectors per row
+  int32_t slices;             // units per row
+  int32_t units_before;       // units of the jobs before this one
+};
+
+struct CopyBatch {
+  CopyJob job[SCA_MAX_COPIES];
+  int32_t n, units;
+};
+static_assert(sizeof(CopyBatch) <= 32764, "kernel parameters");
+
+__global__ void __launch_bounds__(kCopyThreads) ring_copy_kernel(const __grid_constant__ CopyBatch cb) {
+  for (int32_t u = blockIdx.x; u < cb.units; u += gridDim.x) {
+    int j = 0;
+    while (j + 1 < cb.n && cb.job[j + 1].units_before <= u) ++j;
+    const CopyJob& c = cb.job[j];
+    const int32_t local = u - c.units_before;
+    const int32_t r = local / c.slices;
+    const int32_t c0 = (local - r * c.slices) * kCopySlice;
+    const int32_t nv = c.width - c0 < kCopySlice ? c.width - c0 : kCopySlice;
+    const uint4* s = c.src + r * c.spitch + c0;
+    uint4* d = c.dst + r * c.dpitch + c0;
+    uint4 v[kCopyUnroll];
 #pragma unroll
-      for (int u = 0; u < kCopyUnroll; ++u)
-        if (base + u * kCopyThreads < width_vecs) v[u] = s[base + u * kCopyThreads];
+    for (int k = 0; k < kCopyUnroll; ++k) {
+      const int32_t i = k * kCopyThreads + threadIdx.x;
+      if (i < nv) v[k] = s[i];
+    }
 #pragma unroll
-      for (int u = 0; u < kCopyUnroll; ++u)
-        if (base + u * kCopyThreads < width_vecs) d[base + u * kCopyThreads] = v[u];
+    for (int k = 0; k < kCopyUnroll; ++k) {
+      const int32_t i = k * kCopyThreads + threadIdx.x;
+      if (i < nv) d[i] = v[k];
     }
   }
 }
@@ -461,20 +480,53 @@ extern "C" int zigzag_permute(const void* src, void* dst, int64_t outer, int64_t
   return cuda_status(cudaGetLastError(), "zigzag_permute launch");
 }
 
+// Launches the copy kernel over copies [0, n) (n <= SCA_MAX_COPIES, every
+// address, width and pitch a multiple of 16 bytes, checked by the caller).
+static int launch_copies(const sca_copy* copies, int n, cudaStream_t st, const char* what) {
+  CopyBatch cb;
+  int64_t units = 0;
+  cb.n = 0;
+  for (int i = 0; i < n; ++i) {
+    if (copies[i].height == 0 || copies[i].width == 0) continue;
+    CopyJob& j = cb.job[cb.n++];
+    j.src = static_cast<const uint4*>(copies[i].src);
+    j.dst = static_cast<uint4*>(copies[i].dst);
+    j.spitch = copies[i].src_pitch / 16;
+    j.dpitch = copies[i].dst_pitch / 16;
+    j.height = static_cast<int32_t>(copies[i].height);
+    j.width = static_cast<int32_t>(copies[i].width / 16);
+    j.slices = (j.width + kCopySlice - 1) / kCopySlice;
+    j.units_before = static_cast<int32_t>(units);
+    units += static_cast<int64_t>(j.height) * j.slices;
+  }
+  if (cb.n == 0) return SCA_OK;
+  SCA_REQUIRE(units < (int64_t(1) << 31), SCA_ERR_UNSUPPORTED, "%s: copy too large for one launch", what);
+  cb.units = static_cast<int32_t>(units);
+  const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
+  ring_copy_kernel<<<grid, kCopyThreads, 0, st>>>(cb);
+  return cuda_status(cudaGetLastError(), what);
+}
+
+static bool copy_ok(const sca_copy& c) {
+  return c.height >= 0 && c.width >= 0 && c.width % 16 == 0 && c.src_pitch % 16 == 0 && c.dst_pitch % 16 == 0 &&
+         c.width / 16 < (int64_t(1) << 31) && c.height < (int64_t(1) << 31) &&
+         (c.height <= 1 || (c.src_pitch >= c.width && c.dst_pitch >= c.width));
+}
+
 // height rows of `width` bytes, pitches in bytes: the hand-off copy kernel
 // when every address and size is a whole number of 16-byte vectors, else
 // the runtime's 2-D copy.
 static int stage_copy(void* dst, int64_t dpitch, const void* src, int64_t spitch, int64_t width, int64_t height,
                       cudaStream_t st, const char* what) {
   if (width == 0 || height == 0) return SCA_OK;
-  if (aligned(src, 16) && aligned(dst, 16) && width % 16 == 0 && spitch % 16 == 0 && dpitch % 16 == 0) {
-    const int64_t per = static_cast<int64_t>(kCopyThreads) * kCopyUnroll;
-    const int64_t blocks = (width / 16 + per - 1) / per;
-    const int grid = static_cast<int>(blocks < sm_count() ? blocks : sm_count());
-    ring_copy_kernel<<<grid, kCopyThreads, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), height,
-                                                    width / 16, spitch / 16, dpitch / 16);
-    return cuda_status(cudaGetLastError(), what);
-  }
+  sca_copy c;
+  c.src = src;
+  c.dst = dst;
+  c.height = height;
+  c.width = width;
+  c.src_pitch = spitch;
+  c.dst_pitch = dpitch;
+  if (aligned(src, 16) && aligned(dst, 16) && copy_ok(c)) return launch_copies(&c, 1, st, what);
   return cuda_status(cudaMemcpy2DAsync(dst, static_cast<size_t>(dpitch), src, static_cast<size_t>(spitch),
                                        static_cast<size_t>(width), static_cast<size_t>(height),
                                        cudaMemcpyDeviceToDevice, st),
@@ -517,6 +569,26 @@ extern "C" int ring_stage_segments(const void* src, void* dst, int64_t outer, in
     if (rc != SCA_OK) return rc;
   }
   return SCA_OK;
+}
+
+extern "C" int ring_stage_copies(const sca_copy* copies, int n, void* stream) {
+  SCA_REQUIRE(n >= 0 && n <= SCA_MAX_COPIES, SCA_ERR_ARG, "ring_stage_copies: n=%d outside [0, %d]", n,
+              SCA_MAX_COPIES);
+  SCA_REQUIRE(n == 0 || copies, SCA_ERR_ARG, "ring_stage_copies: NULL copies");
+  for (int i = 0; i < n; ++i) {
+    const sca_copy& c = copies[i];
+    SCA_REQUIRE(c.src && c.dst, SCA_ERR_ARG, "ring_stage_copies: copy %d has a NULL pointer", i);
+    SCA_REQUIRE(copy_ok(c), SCA_ERR_ARG,
+                "ring_stage_copies: copy %d: sizes must be non-negative, width and pitches multiples of 16 bytes, "
+                "pitches at least the width",
+                i);
+    SCA_REQUIRE(aligned(c.src, 16) && aligned(c.dst, 16), SCA_ERR_ALIGN,
+                "ring_stage_copies: copy %d: pointers not 16-byte aligned", i);
+    const int64_t sb = c.height == 0 ? 0 : (c.height - 1) * c.src_pitch + c.width;
+    const int64_t db = c.height == 0 ? 0 : (c.height - 1) * c.dst_pitch + c.width;
+    SCA_REQUIRE(!overlap(c.src, sb, c.dst, db), SCA_ERR_ARG, "ring_stage_copies: copy %d: src and dst overlap", i);
+  }
+  return launch_copies(copies, n, as_stream(stream), "ring_stage_copies launch");
 }
 
 extern "C" int attn_merge_lse(const float* o_parts, const float* lse_parts, int n, int64_t rows, int D,

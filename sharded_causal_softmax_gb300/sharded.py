@@ -324,35 +324,42 @@ class ShardedCausalAttention:
         """Hand-off into the spare buffer: rank (g, r) receives the block it
         visits at step t_next from the rank that holds it at step t_next - 1
         (its left neighbour on the ring; on the double ring a neighbour in
-        its group, or a rank of the previous group on an outer hop)."""
+        its group, or a rank of the previous group on an outer hop).  Every
+        copy of the hand-off goes out in one ring_stage_copies launch."""
         P, B, Hg, n_r, D, eb = self.P, self.B, self.Hkvg, self.n_r, self.D, self.eb
         cs = self.copy_stream.cuda_stream
         ns = self.n_stage
         dst_k, dst_v = self.stage_k[t_next % ns], self.stage_v[t_next % ns]
         row = D * eb
         blk = B * Hg * n_r
+        copies = []
         for g in range(self.G):
             if t_next == 1:   # the senders' blocks are still at home
                 for r in range(P):
-                    src_r = self.block(r, 1)
+                    segs = shard_segs(self.S, P, self.layout, self.block(r, 1))
                     for b in range(B):
                         off = ((b * self.Hkv + g * Hg) * self.S) * row
                         for home, dst in ((k_home, dst_k), (v_home, dst_v)):
                             if self.pos:   # gather the block's chunks from natural order
-                                capi.ring_stage_segments(_ptr(home) + off, _ptr(dst[g, r, b]), Hg, self.S,
-                                                         shard_segs(self.S, P, self.layout, src_r), row, cs)
+                                w = segs.len * row
+                                for i in range(segs.n):
+                                    copies.append(capi.copy2d(_ptr(home) + off + segs.start[i] * row,
+                                                              _ptr(dst[g, r, b]) + i * w, Hg, w, self.S * row,
+                                                              segs.n * w))
                             else:
-                                capi.ring_stage_block(_ptr(home) + off, _ptr(dst[g, r, b]), Hg, self.S,
-                                                      src_r * n_r, n_r, row, cs)
-                            self.launches += 1
-                            self.staged_bytes += Hg * n_r * row
+                                w = n_r * row
+                                copies.append(capi.copy2d(_ptr(home) + off + self.block(r, 1) * w,
+                                                          _ptr(dst[g, r, b]), Hg, w, self.S * row, w))
             else:             # the senders' staged blocks: one copy per run of consecutive ranks
                 src_k, src_v = self.stage_k[(t_next - 1) % ns], self.stage_v[(t_next - 1) % ns]
                 for r0, s0, n in copy_runs(hop_senders(self.block, t_next, P)):
                     for src, dst in ((src_k, dst_k), (src_v, dst_v)):
-                        capi.ring_stage_block(_ptr(src[g, s0]), _ptr(dst[g, r0]), 1, n * blk, 0, n * blk, row, cs)
-                        self.launches += 1
-                        self.staged_bytes += n * blk * row
+                        w = n * blk * row
+                        copies.append(capi.copy2d(_ptr(src[g, s0]), _ptr(dst[g, r0]), 1, w, w, w))
+        for lo in range(0, len(copies), capi.SCA_MAX_COPIES):
+            capi.ring_stage_copies(copies[lo:lo + capi.SCA_MAX_COPIES], cs)
+            self.launches += 1
+        self.staged_bytes += sum(c.height * c.width for c in copies)
 
     def _ring(self, k_home, v_home, launch_step):
         """Run launch_step(t, kv_ptrs(g, r), kv_view, home) for t = 0..P-1

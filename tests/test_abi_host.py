@@ -275,6 +275,21 @@ def test_merge_rejects_overlaps_other_than_one_partials_rows(lib):
     assert call(op + ob, lp + lb, uP=1, S=rows) == capi.SCA_ERR_ARG
 
 
+def test_stage_copies_reject_bad_arguments(lib):
+    f = lib.ring_stage_copies
+    ok = capi.copy2d(A, 2 * A, 4, 256, 512, 256)
+    arr = lambda *cs: (capi.sca_copy * len(cs))(*cs)
+    assert f(arr(ok), capi.SCA_MAX_COPIES + 1, None) == capi.SCA_ERR_ARG                       # too many copies
+    assert f(None, 1, None) == capi.SCA_ERR_ARG
+    assert f(arr(capi.copy2d(0, 2 * A, 4, 256, 512, 256)), 1, None) == capi.SCA_ERR_ARG        # NULL source
+    assert f(arr(capi.copy2d(A, 2 * A, 4, 250, 512, 256)), 1, None) == capi.SCA_ERR_ARG        # width not x16
+    assert f(arr(capi.copy2d(A, 2 * A, 4, 256, 128, 256)), 1, None) == capi.SCA_ERR_ARG        # pitch < width
+    assert f(arr(capi.copy2d(A + 8, 2 * A, 4, 256, 512, 256)), 1, None) == capi.SCA_ERR_ALIGN
+    assert f(arr(capi.copy2d(A, A + 512, 4, 256, 512, 256)), 1, None) == capi.SCA_ERR_ARG      # overlapping
+    assert f(arr(ok), 0, None) == capi.SCA_OK                                                   # nothing to do
+    assert f(arr(capi.copy2d(A, 2 * A, 0, 256, 512, 256)), 1, None) == capi.SCA_OK             # empty copy
+
+
 def test_stage_and_delta_reject_bad_arguments(lib):
     assert lib.ring_stage_block(A, 2 * A, 4, 64, 60, 8, 256, None) == capi.SCA_ERR_ARG   # rows past S
     assert lib.attn_bwd_delta(A, 2 * A, capi.SCA_BF16, 3 * A, 10, 96, None) == capi.SCA_ERR_UNSUPPORTED

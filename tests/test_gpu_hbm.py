@@ -119,3 +119,27 @@ def test_delta_matches_definition(sca, dtype, D):
     torch.cuda.synchronize()
     ref = (o.double().numpy() * do.double().numpy()).sum(axis=1)
     assert_close("delta", out, ref, (1e-4, 1e-5))
+
+
+def test_ring_stage_copies_bit_exact(sca):
+    """One hand-off of mixed copies in one launch: strided gathers of a
+    block's rows out of a [heads, S, D] tensor (narrow and wide rows), a
+    flat copy larger than one unit of the kernel, and a one-row copy that is
+    not a whole number of units; each lands exactly where torch puts it."""
+    from sharded_causal_softmax_gb300 import capi
+    g = torch.Generator().manual_seed(11)
+    H, S, D = 3, 4096, 128
+    x = torch.randn(H, S, D, generator=g).to(torch.bfloat16).cuda()
+    row = D * 2
+    a = torch.empty(H, 1000, D, dtype=torch.bfloat16, device="cuda")   # rows [700, 1700) of every head
+    b = torch.empty(H, 32, D, dtype=torch.bfloat16, device="cuda")     # rows [8, 40): narrow
+    flat = torch.empty(S * D, dtype=torch.bfloat16, device="cuda")     # head 1 whole (1 MB)
+    odd = torch.empty(37 * D, dtype=torch.bfloat16, device="cuda")     # 37 rows of head 2 as one row
+    cps = [capi.copy2d(x.data_ptr() + 700 * row, a.data_ptr(), H, 1000 * row, S * row, 1000 * row),
+           capi.copy2d(x.data_ptr() + 8 * row, b.data_ptr(), H, 32 * row, S * row, 32 * row),
+           capi.copy2d(x[1].data_ptr(), flat.data_ptr(), 1, S * row, S * row, S * row),
+           capi.copy2d(x[2].data_ptr() + 100 * row, odd.data_ptr(), 1, 37 * row, 37 * row, 37 * row)]
+    capi.ring_stage_copies(cps, _stream())
+    torch.cuda.synchronize()
+    assert torch.equal(a, x[:, 700:1700]) and torch.equal(b, x[:, 8:40])
+    assert torch.equal(flat, x[1].reshape(-1)) and torch.equal(odd, x[2, 100:137].reshape(-1))
