@@ -24,7 +24,12 @@
 //               columns.  O is rescaled when
 //               the maximum grows by more than 2^8 (lazy rescale, exact
 //               after the final division).
-//               Epilogue: o = O / l, lse = m + ln l.
+//               Epilogue: o = O / l, lse = m + ln l.  o goes through the
+//               spent K stages: each thread writes its row (16-byte chunks,
+//               chunk index XOR (row & 7), so no bank conflicts), then each
+//               warp store instruction writes whole 512-byte rows.  Storing
+//               straight from the thread-per-row registers touched 32 rows
+//               per warp instruction and took ~5800 clk per CTA.
 //
 // Tensor memory: S0, S1 in columns [0,256), O in [256, 256+D), Q in
 // [256+D, 256+D+D/2); all 512 columns are allocated (one CTA per SM:
@@ -66,6 +71,7 @@ struct Bars {
   uint64_t o_full;       // every PV has completed
   uint64_t red_full[2];  // both warpgroups published their row maxima (per tile parity)
   uint64_t lsum_full;    // both warpgroups published their row sums
+  uint64_t o_staged;     // both warpgroups staged their half of o for the row stores
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -192,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     mbar_init(&bars->red_full[0], 2 * BM);
     mbar_init(&bars->red_full[1], 2 * BM);
     mbar_init(&bars->lsum_full, 2 * BM);
+    mbar_init(&bars->o_staged, 2 * BM);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -452,24 +459,48 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-      const int64_t orow = slab_row(gm.qs, a.q_by_pos, q0 + (row_valid ? row : 0));
-      float* op = it.o + b * a.o.b + h * a.o.h + orow * a.o.s + g * (D / 2);
+      // o = O / l staged over the K stages (every QK^T has completed): row r
+      // at r * D * 4 bytes, logical 16-byte chunk q at physical chunk
+      // q ^ (r & 7)
+      constexpr int CH = D / 4;                  // 16-byte chunks per row
+      uint8_t* stg = smem + L::K_OFF;
+      uint8_t* mine = stg + row * (D * 4);
 #pragma unroll 1
       for (int c = 0; c < D / 2; c += 32) {
         uint32_t r[32];
         tmem_ld32(tO + lane_off + g * (D / 2) + c, r);
         tmem_wait_ld32(r);
-        if (row_valid) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 v = make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
-                                         __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
-            *reinterpret_cast<float4*>(op + c + i) = v;
+        for (int j = 0; j < 8; ++j) {
+          const int q = (g * (D / 2) + c) / 4 + j;
+          const uint4 v = make_uint4(__float_as_uint(__uint_as_float(r[4 * j]) * inv),
+                                     __float_as_uint(__uint_as_float(r[4 * j + 1]) * inv),
+                                     __float_as_uint(__uint_as_float(r[4 * j + 2]) * inv),
+                                     __float_as_uint(__uint_as_float(r[4 * j + 3]) * inv));
+          *reinterpret_cast<uint4*>(mine + ((q ^ (row & 7)) << 4)) = v;
+        }
+      }
+      if (row_valid && g == 0) {
+        const int64_t orow = slab_row(gm.qs, a.q_by_pos, q0 + row);
+        it.lse[b * a.lse_b + h * a.lse_h + orow] = l_tot > 0.f ? (m_used + log2f(l_tot)) * kLn2 : -INFINITY;
+      }
+      mbar_arrive(&bars->o_staged);
+      // warp w stores rows [16w, 16w + 16): one whole row (D = 128) or two
+      // (D = 64) per instruction
+      if (__all_sync(0xffffffffu, mbar_wait(&bars->o_staged, 0, abort, status))) {
+        constexpr int RPI = 32 / CH;
+        const int sub = lane / CH, li = lane % CH;
+        float* obase = it.o + b * a.o.b + h * a.o.h;
+#pragma unroll 4
+        for (int i = 0; i < 16; i += RPI) {
+          const int r = 16 * warp + i + sub;
+          if (r < nq) {
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + r * (D * 4) + ((li ^ (r & 7)) << 4));
+            const int64_t orow = slab_row(gm.qs, a.q_by_pos, q0 + r);
+            *reinterpret_cast<uint4*>(obase + orow * a.o.s + 4 * li) = v;
           }
         }
       }
-      if (row_valid && g == 0)
-        it.lse[b * a.lse_b + h * a.lse_h + orow] = l_tot > 0.f ? (m_used + log2f(l_tot)) * kLn2 : -INFINITY;
     }
   }
 
