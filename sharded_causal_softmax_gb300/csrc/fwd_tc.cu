@@ -275,31 +275,36 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     }
   } else if (warp == kMma) {
     // ------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop and its waits, so every operand is
+    // warp-uniform; one elected lane issues each MMA and commit.
+    {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
-      bool ok = mbar_wait(&bars->q_tmem, 0, abort, status);
+      auto wait_all = [&](uint64_t* bar, uint32_t par) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, par, abort, status));
+      };
+      bool ok = wait_all(&bars->q_tmem, 0);
       auto issue_qk = [&](int j) -> bool {   // S[j%2] = Q K_j^T, Q from tensor memory
         const int ks = j % KST;
-        if (!mbar_wait(&bars->k_full[ks], (j / KST) & 1, abort, status)) return false;
+        if (!wait_all(&bars->k_full[ks], (j / KST) & 1)) return false;
         tc_fence_after();
         const uint32_t tS = tmem + (j % SBUF) * 128;
         const uint64_t kd = sdesc_sw128(sK + ks * L::TILE, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;   // K-major: panel, then 32 B steps
-          umma_ts(tS, tQ + kk * 8, sdesc_step(kd, off), idesc_qk, kk > 0 ? 1u : 0u);
+          umma_ts_w(tS, tQ + kk * 8, sdesc_step(kd, off), idesc_qk, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars->s_full[j % SBUF]);
-        umma_commit(&bars->k_empty[ks]);
+        umma_commit_w(&bars->s_full[j % SBUF]);
+        umma_commit_w(&bars->k_empty[ks]);
         return true;
       };
       for (int j = 0; ok && j < n_vis && j < SBUF; ++j) ok = issue_qk(j);
       for (int j = 0; ok && j < n_vis; ++j) {
         // O += P_j V_j  (B = V tile, MN-major: 64-column panels LBO apart, 8-key groups 1024 B apart)
         const int vs = j % VST;
-        if (!mbar_wait(&bars->p_full[j % SBUF], (j / SBUF) & 1, abort, status)) { ok = false; break; }
-        if (!mbar_wait(&bars->v_full[vs], (j / VST) & 1, abort, status)) { ok = false; break; }
+        if (!wait_all(&bars->p_full[j % SBUF], (j / SBUF) & 1)) { ok = false; break; }
+        if (!wait_all(&bars->v_full[vs], (j / VST) & 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tP = tmem + (j % SBUF) * 128;
         const uint64_t vd = sdesc_sw128(sV + vs * L::TILE, PANEL, 1024);
@@ -307,15 +312,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         // keys [16kk, 16kk+16) of P live in warpgroup kk/4's packed columns
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          umma_ts(tO, tP + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_step(vd, kk * 2048), idesc_pv, kk > 0 ? 1u : acc0);
-        umma_commit(&bars->v_empty[vs]);
-        umma_commit(&bars->pv_done[j & 1]);
-        // S[j%3] is free once PV_j has read P_j (MMAs execute in order)
+          umma_ts_w(tO, tP + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_step(vd, kk * 2048), idesc_pv, kk > 0 ? 1u : acc0);
+        umma_commit_w(&bars->v_empty[vs]);
+        umma_commit_w(&bars->pv_done[j & 1]);
+        // S[j%2] is free once PV_j has read P_j (MMAs execute in order)
         if (j + SBUF < n_vis) ok = issue_qk(j + SBUF);
       }
-      if (ok) umma_commit(&bars->o_full);
+      if (ok) umma_commit_w(&bars->o_full);
       if (!ok) {  // make sure no MMA still writes tensor memory
-        umma_commit(&bars->drain);
+        umma_commit_w(&bars->drain);
         mbar_wait_drain(&bars->drain, 0);
       }
     }

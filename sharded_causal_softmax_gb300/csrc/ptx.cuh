@@ -180,6 +180,30 @@ SCA_INLINE void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint3
       : "memory");
 }
 
+// Warp-collective forms: the whole (converged) warp executes them and
+// elect.sync picks one lane (the same lane every time, the warp being full)
+// to issue.  Run from a converged warp the operands stay warp-uniform; the
+// single-lane forms above, called under `if (lane == 0)`, cost ~85 clk of
+// issue per MMA in the forward against 64 clk of tensor-pipe work.
+SCA_INLINE void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+SCA_INLINE void umma_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread
 // has completed.
 SCA_INLINE void umma_commit(uint64_t* bar) {
