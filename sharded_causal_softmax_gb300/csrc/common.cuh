@@ -68,6 +68,32 @@ __host__ __device__ __forceinline__ void tile_pos_range(const Segs& s, int64_t r
   }
 }
 
+// Bits [lo, hi) of a 64-bit word, the bounds clamped to [0, 64].
+__host__ __device__ __forceinline__ uint64_t run_bits(int64_t lo, int64_t hi) {
+  lo = lo < 0 ? 0 : (lo > 64 ? 64 : lo);
+  hi = hi < 0 ? 0 : (hi > 64 ? 64 : hi);
+  if (hi <= lo) return 0;
+  const uint64_t below_hi = hi == 64 ? ~0ull : ((1ull << hi) - 1);
+  return below_hi & ~((1ull << lo) - 1);
+}
+
+// Key columns c0 + j (j < 64) of the tile of slab rows [k0, k0 + nk) that a
+// query at global position qpos (-1: none, under the causal mask) may see:
+// bit j set when c0 + j < nk and, causal, the key's position <= qpos.  The
+// tile's rows in segment part 0 are columns c < cb (position start0 + k0 + c),
+// those in part 1 columns c >= cb (position start1 + k0 + c - len); positions
+// rise within each part, so each part's visible columns form one run.
+__host__ __device__ __forceinline__ uint64_t key_runs(const Segs& ks, int64_t k0, int64_t nk, bool causal,
+                                                      int64_t qpos, int64_t c0) {
+  const int64_t cb = ks.len - k0 < 0 ? 0 : min64(ks.len - k0, nk);
+  int64_t a_hi = cb, b_hi = nk;
+  if (causal) {
+    a_hi = min64(a_hi, qpos - ks.start0 - k0 + 1);
+    b_hi = min64(b_hi, qpos - ks.start1 - k0 + ks.len + 1);
+  }
+  return run_bits(-c0, a_hi - c0) | run_bits(cb - c0, b_hi - c0);
+}
+
 // Walks, in order, the tiles t in [0, n) for which vis(t) holds, testing 32
 // candidates per warp-wide ballot.  All 32 lanes of a warp call next()
 // together with the same arguments; it returns -1 after the last tile.
