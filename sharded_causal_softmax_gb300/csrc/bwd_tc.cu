@@ -346,8 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     }
   } else if (warp == 9) {
     // ------------------------------------------------------ MMA issuer
-    // one thread; it needs only the count of visible tiles, not their rows
-    if (lane == 0) {
+    // The whole warp runs the loop and its waits, so every operand is
+    // warp-uniform; one elected lane issues each MMA and commit.  It needs
+    // only the count of visible tiles, not their rows.
+    {
+      auto wait_all = [&](uint64_t* bar, uint32_t par) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, par, abort, status));
+      };
       constexpr uint32_t idesc_dp = F16PV ? idesc_f16_f32(BN, BM, false, false)    // dP^T: M=keys, N=queries
                                           : idesc_bf16_f32(BN, BM, false, false);
       constexpr uint32_t idesc_s = idesc_f16_f32(BN, BM, false, false);      // S^T (fp16 K, Q)
@@ -357,16 +362,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       constexpr uint32_t idesc_dq = idesc_f16_f32(BM, D, true, true);        // dQ: M=queries, N=D
       const uint32_t sK = smem_u32(smem + L::K_OFF), sV = smem_u32(smem + L::V_OFF);
       const uint32_t sDS = smem_u32(smem + L::DS_OFF);
-      bool ok = mbar_wait(&bars->kv_full, 0, abort, status);
+      bool ok = wait_all(&bars->kv_full, 0);
       for (int n = 0; ok && n < n_vis; ++n) {
         const int st = n & 1;
         const uint32_t sQ = smem_u32(smem + L::Q_OFF + st * L::TILE);
         const uint32_t sO = smem_u32(smem + L::DO_OFF + st * L::TILE);
         // S^T = K Q^T over the S^T columns (the previous dV has read P^T);
         // K and Q must have been converted to fp16
-        if (!mbar_wait(&bars->q_full[st], (n >> 1) & 1, abort, status)) { ok = false; break; }
-        if (n == 0 && !mbar_wait(&bars->k_conv, 0, abort, status)) { ok = false; break; }
-        if (!mbar_wait(&bars->q_conv, n & 1, abort, status)) { ok = false; break; }
+        if (!wait_all(&bars->q_full[st], (n >> 1) & 1)) { ok = false; break; }
+        if (n == 0 && !wait_all(&bars->k_conv, 0)) { ok = false; break; }
+        if (!wait_all(&bars->q_conv, n & 1)) { ok = false; break; }
         tc_fence_after();
         const uint64_t kdk = sdesc_sw128(sK, 16, 1024), qdk = sdesc_sw128(sQ, 16, 1024);
         const uint64_t vdk = sdesc_sw128(sV, 16, 1024), odk = sdesc_sw128(sO, 16, 1024);
@@ -376,14 +381,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;
-          umma_ss(tS, sdesc_step(kdk, off), sdesc_step(qdk, off), idesc_s, kk > 0 ? 1u : 0u);
+          umma_ss_w(tS, sdesc_step(kdk, off), sdesc_step(qdk, off), idesc_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars->s_full);
+        umma_commit_w(&bars->s_full);
         // dP^T = V dO^T over the dP^T columns, which hold the previous dQ
         // until it is read back
-        if (n > 0 && !mbar_wait(&bars->tmem_free, (n - 1) & 1, abort, status)) { ok = false; break; }
-        if (F16PV ? !mbar_wait(&bars->do_conv, n & 1, abort, status)      // V, dO converted to fp16
-                  : !mbar_wait(&bars->do_full[st], (n >> 1) & 1, abort, status)) {
+        if (n > 0 && !wait_all(&bars->tmem_free, (n - 1) & 1)) { ok = false; break; }
+        if (F16PV ? !wait_all(&bars->do_conv, n & 1)      // V, dO converted to fp16
+                  : !wait_all(&bars->do_full[st], (n >> 1) & 1)) {
           ok = false;
           break;
         }
@@ -391,34 +396,34 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;
-          umma_ss(tdP, sdesc_step(vdk, off), sdesc_step(odk, off), idesc_dp, kk > 0 ? 1u : 0u);
+          umma_ss_w(tdP, sdesc_step(vdk, off), sdesc_step(odk, off), idesc_dp, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars->dp_full);
+        umma_commit_w(&bars->dp_full);
         // dV += P^T dO, then dK += dS^T Q (A from tensor memory).  Query
         // K-step kk = 4g + 2c + e lives in warpgroup g's packed columns
         // 64g + 16c + 8e and is ready once chunk c of both warpgroups is:
         // each product runs as two halves, chunk 0's K-steps first.
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          if (!mbar_wait(&bars->p_half[c], n & 1, abort, status)) { ok = false; break; }
+          if (!wait_all(&bars->p_half[c], n & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int kk = 4 * (q >> 1) + 2 * c + (q & 1);
             const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
-            umma_ts(tdV, tS + acol, sdesc_step(odm, kk * 2048), idesc_dv, kk > 0 ? 1u : acc0);
+            umma_ts_w(tdV, tS + acol, sdesc_step(odm, kk * 2048), idesc_dv, kk > 0 ? 1u : acc0);
           }
         }
         if (!ok) break;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          if (!mbar_wait(&bars->ds_half[c], n & 1, abort, status)) { ok = false; break; }
+          if (!wait_all(&bars->ds_half[c], n & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int kk = 4 * (q >> 1) + 2 * c + (q & 1);
             const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
-            umma_ts(tdK, tdP + acol, sdesc_step(qdm, kk * 2048), idesc_dk, kk > 0 ? 1u : acc0);
+            umma_ts_w(tdK, tdP + acol, sdesc_step(qdm, kk * 2048), idesc_dk, kk > 0 ? 1u : acc0);
           }
         }
         if (!ok) break;
@@ -427,13 +432,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         // 64-column panels LBO apart
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          umma_ss(tdP, sdesc_step(sdm, kk * 2048), sdesc_step(kdm, kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
+          umma_ss_w(tdP, sdesc_step(sdm, kk * 2048), sdesc_step(kdm, kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars->q_empty[st]);
-        umma_commit(&bars->dq_full);
+        umma_commit_w(&bars->q_empty[st]);
+        umma_commit_w(&bars->dq_full);
       }
       if (!ok) {
-        umma_commit(&bars->drain);
+        umma_commit_w(&bars->drain);
         mbar_wait_drain(&bars->drain, 0);
       }
     }
@@ -502,15 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         // column 64*wg + j is visible to this thread's key (rows past the slab
         // already have lse = -inf, so P = 0 there)
         uint64_t vis = ~0ull;
-        if (!qt.full) {
-          vis = 0;
-#pragma unroll 1
-          for (int j = 0; j < 64; ++j) {
-            const int qc = 64 * wg + j;
-            const bool v = krow_valid && qc < qt.nq && (!causal || kpos <= seg_pos(gm.qs, qt.q0 + qc));
-            vis |= static_cast<uint64_t>(v) << j;
-          }
-        }
+        if (!qt.full) vis = krow_valid ? query_runs(gm.qs, qt.q0, qt.nq, causal, kpos, 64 * wg) : 0ull;
         tmem_wait_ld32(pr);
         tmem_wait_ld32(pr + 32);
         auto exps = [&](auto masked) {

@@ -94,6 +94,22 @@ __host__ __device__ __forceinline__ uint64_t key_runs(const Segs& ks, int64_t k0
   return run_bits(-c0, a_hi - c0) | run_bits(cb - c0, b_hi - c0);
 }
 
+// Query columns c0 + j (j < 64) of the tile of slab rows [q0, q0 + nq) that
+// a key at global position kpos may be seen by: bit j set when c0 + j < nq
+// and, causal, the query's position >= kpos.  The mirror of key_runs: each
+// segment part's visible columns form one run, here a suffix of the part.
+__host__ __device__ __forceinline__ uint64_t query_runs(const Segs& qs, int64_t q0, int64_t nq, bool causal,
+                                                        int64_t kpos, int64_t c0) {
+  const int64_t cb = qs.len - q0 < 0 ? 0 : min64(qs.len - q0, nq);
+  int64_t a_lo = 0, b_lo = cb;
+  if (causal) {
+    const int64_t a = kpos - qs.start0 - q0, b = kpos - qs.start1 - q0 + qs.len;
+    a_lo = a > a_lo ? a : a_lo;
+    b_lo = b > b_lo ? b : b_lo;
+  }
+  return run_bits(a_lo - c0, cb - c0) | run_bits(b_lo - c0, nq - c0);
+}
+
 // Walks, in order, the tiles t in [0, n) for which vis(t) holds, testing 32
 // candidates per warp-wide ballot.  All 32 lanes of a warp call next()
 // together with the same arguments; it returns -1 after the last tile.

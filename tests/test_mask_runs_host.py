@@ -1,9 +1,11 @@
-"""The forward's per-tile visibility mask (key_runs in common.cuh: at most
-two runs of visible key columns, one per segment part) against the
-definition it replaces, tested column by column on the host: a key column
-is visible when it lies inside the tile and, under the causal mask, its
-global position is at most the query's.  Compiled with nvcc as host code
-(no GPU needed)."""
+"""The per-tile visibility masks of the tensor-core kernels against the
+definitions they replace, tested column by column on the host.  key_runs
+(forward): a key column is visible when it lies inside the tile and, under
+the causal mask, its global position is at most the query's.  query_runs
+(backward): a query column sees the key when it lies inside the tile and,
+causal, its position is at least the key's.  Each is at most two runs of
+columns, one per segment part.  Compiled with nvcc as host code (no GPU
+needed)."""
 import os
 import shutil
 import subprocess
@@ -20,7 +22,7 @@ static uint64_t st = 88172645463325252ull;
 static int64_t rnd(int64_t n) { st ^= st << 13; st ^= st >> 7; st ^= st << 17; return (int64_t)(st % (uint64_t)n); }
 int main() {
   long bad = 0, cases = 0, partial = 0;
-  for (int it = 0; it < 200000; ++it) {
+  for (int it = 0; it < 400000; ++it) {
     Segs s;
     s.n = 1 + (int)rnd(2);
     s.len = 1 + rnd(rnd(4) == 0 ? 2000 : 300);
@@ -33,11 +35,13 @@ int main() {
     const bool causal = rnd(5) != 0;
     const int64_t qpos = rnd(8) == 0 ? -1 : rnd(6000);
     const int64_t c0 = 64 * rnd(2);
-    const uint64_t got = key_runs(s, k0, nk, causal, qpos, c0);
+    const bool fwd = it & 1;
+    const int64_t kpos = rnd(6000);
+    const uint64_t got = fwd ? key_runs(s, k0, nk, causal, qpos, c0) : query_runs(s, k0, nk, causal, kpos, c0);
     uint64_t want = 0;
     for (int j = 0; j < 64; ++j) {
       const int64_t c = c0 + j;
-      const bool v = c < nk && (!causal || seg_pos(s, k0 + c) <= qpos);
+      const bool v = c < nk && (!causal || (fwd ? seg_pos(s, k0 + c) <= qpos : seg_pos(s, k0 + c) >= kpos));
       want |= (uint64_t)v << j;
     }
     ++cases;
@@ -56,7 +60,7 @@ int main() {
 
 
 @pytest.mark.skipif(shutil.which("nvcc") is None, reason="nvcc not found")
-def test_key_runs_matches_per_column_definition(tmp_path):
+def test_key_and_query_runs_match_per_column_definition(tmp_path):
     src = tmp_path / "runs.cu"
     src.write_text(SRC)
     exe = tmp_path / "runs"
