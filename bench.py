@@ -66,12 +66,17 @@ def flops(w, fwd=True, bwd=True):
 
 def workload_config(w, ws: int, visit: str = "ring", inner: int = 0) -> dict:
     """The `config` object both arms print for a workload."""
+    from sharded_causal_softmax_gb300.sharded import AUTO_FUSED_MAX_ROWS, resolve_schedule
+    sched = resolve_schedule(w.schedule, w.S, w.P, visit) if w.method == "softmax" else w.schedule
     cfg = {"workload": w.description, "name": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "P": w.P,
-           "method": w.method, "layout": w.layout, "schedule": w.schedule, "kv_heads": w.kv_heads or w.H,
+           "method": w.method, "layout": w.layout, "schedule": sched, "kv_heads": w.kv_heads or w.H,
            "head_groups": w.head_groups, "step": "fwd+bwd" if w.backward else "fwd", "flops_per_step": flops(w),
            "parallelism": f"{ws} independent replica(s), one per GPU"}
     if visit == "double_ring":
         cfg["visit"] = f"double_ring (inner rings of {inner})"
+    if w.schedule == "auto" and w.method == "softmax":
+        cfg["schedule_choice"] = (f"auto: fused (one launch per direction) up to {AUTO_FUSED_MAX_ROWS} rows per "
+                                  "shard, ring above")
     return cfg
 
 
@@ -711,7 +716,7 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="train_s32k")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--schedule", choices=["ring", "direct", "fused"], default=None,
+    ap.add_argument("--schedule", choices=["auto", "ring", "direct", "fused"], default=None,
                     help="override the workload's schedule")
     ap.add_argument("--addressing", choices=["auto", "position", "permuted"], default="auto")
     ap.add_argument("--visit", choices=["ring", "double_ring"], default="ring",

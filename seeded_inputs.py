@@ -46,7 +46,7 @@ class Workload:
     q_mult: float = 1.0
     head_groups: int = 1  # 2D head x context split
     backward: bool = False
-    schedule: str = "ring"      # "ring" (staged KV blocks) or "direct"
+    schedule: str = "auto"      # "auto", "ring" (staged KV blocks), "direct" or "fused"
     sample_rows: int = 0        # 0: oracle checks every row
     description: str = ""
     kv_heads: int | None = None  # grouped-query attention: key/value heads

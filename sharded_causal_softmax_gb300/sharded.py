@@ -45,6 +45,10 @@ The schedule (host logic only; every byte is moved or computed by libsca):
   its running (m, l, O) over every key/value block, so there are no partials
   and no merge; the backward writes each dK/dV row once.  One GPU holds
   every block, so nothing is staged.
+* "auto" (the default): "fused" when a shard holds at most
+  AUTO_FUSED_MAX_ROWS rows (a ring step's CTAs would then walk at most 32 key
+  tiles each, too few to amortise a CTA's fixed cost of set-up, first loads
+  and epilogue), "ring" otherwise or when the double ring is asked for.
 * Backward: delta = rowsum(dO * O), then the same ring of steps; each step
   recomputes P from the final lse and adds into dQ of the rank's rows and
   into dK/dV of the block's rows (step 0 overwrites, so no zeroing pass is
@@ -125,6 +129,18 @@ def _ptr(t: torch.Tensor) -> int:
     return t.data_ptr()
 
 
+AUTO_FUSED_MAX_ROWS = 4096
+
+
+def resolve_schedule(schedule, S, P, visit="ring"):
+    """The schedule "auto" stands for at these sizes; others unchanged."""
+    if schedule != "auto":
+        return schedule
+    if visit == "ring" and (P == 1 or S // P <= AUTO_FUSED_MAX_ROWS):
+        return "fused"
+    return "ring"
+
+
 class ShardedCausalAttention:
     """Buffers and launch schedule of one sharded attention configuration.
 
@@ -139,12 +155,12 @@ class ShardedCausalAttention:
     """
 
     def __init__(self, B, H, S, D, P, layout="zigzag", dtype=torch.bfloat16, head_groups=1,
-                 schedule="ring", scale=None, causal=True, algo=capi.SCA_ALGO_AUTO, backward=False,
+                 schedule="auto", scale=None, causal=True, algo=capi.SCA_ALGO_AUTO, backward=False,
                  bf16_out=False, device=None, addressing="auto", kv_heads=None, f16_staging=True,
                  visit="ring", inner=None, group_steps=True):
         if layout not in ("zigzag", "contiguous"):
             raise ValueError(f"layout {layout!r}")
-        if schedule not in ("ring", "direct", "fused"):
+        if schedule not in ("auto", "ring", "direct", "fused"):
             raise ValueError(f"schedule {schedule!r}")
         if visit == "ring":
             inner = P
@@ -153,6 +169,8 @@ class ShardedCausalAttention:
                 raise ValueError(f"double_ring needs an inner ring size dividing P={P} (got {inner})")
         else:
             raise ValueError(f"visit {visit!r}")
+        self.schedule_requested = schedule
+        schedule = resolve_schedule(schedule, S, P, visit)
         if addressing not in ("auto", "position", "permuted"):
             raise ValueError(f"addressing {addressing!r}")
         if dtype not in _DT:

@@ -27,7 +27,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(sca):
     # the context still runs kernels, and a fresh status word reads OK
     B, H, S, D, P = 1, 2, 512, 128, 2
     q, k, v = (x.cuda() for x in seeded_inputs.make_inputs(B, H, S, D, "bf16", seed=3))
-    plan = sca.ShardedCausalAttention(B, H, S, D, P)
+    plan = sca.ShardedCausalAttention(B, H, S, D, P, schedule="ring")
     o, lse = plan.forward(q, k, v)
     assert plan.read_status() == 0
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()

@@ -41,7 +41,7 @@ def test_gqa_small_full_oracle(sca, dtype, algo, layout, P, G, H, Hkv, S, kw):
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     a = sca.capi.SCA_ALGO_SIMT if algo == "simt" else sca.capi.SCA_ALGO_AUTO
     plan = sca.ShardedCausalAttention(B, H, S, D, P, layout=layout, dtype=tdt, head_groups=G, backward=True,
-                                      kv_heads=Hkv, algo=a, **kw)
+                                      kv_heads=Hkv, algo=a, **{"schedule": "ring", **kw})
     qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
     o, lse = plan.forward(qd, kd, vd)
     dq, dk, dv = plan.backward(dod)

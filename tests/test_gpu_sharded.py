@@ -81,7 +81,7 @@ def test_forward_sampled_rows_full_size(sca, name, kw):
 def test_forward_small_full_oracle(sca, layout, P, G, kw):
     B, H, S, D = 2, 4, 1024, 128
     q, k, v = seeded_inputs.make_inputs(B, H, S, D, "bf16", seed=100 + P + G)
-    plan = sca.ShardedCausalAttention(B, H, S, D, P, layout=layout, head_groups=G, **kw)
+    plan = sca.ShardedCausalAttention(B, H, S, D, P, layout=layout, head_groups=G, **{"schedule": "ring", **kw})
     o, lse = plan.forward(q.cuda(), k.cuda(), v.cuda())
     ro, rl = oracle.attention(q, k, v, scale_for(D))
     assert_close("o", o, ro, tol_for("bf16"))
@@ -121,7 +121,7 @@ def test_double_ring_partials_are_the_ring_partials(sca):
     w = WORKLOADS["ring_s128k"]
     S, H, P, inner = 16384, 2, w.P, 4
     q, k, v = (x.cuda() for x in seeded_inputs.make_inputs(w.B, H, S, w.D, "bf16", seed=w.seed + 1))
-    ring = sca.ShardedCausalAttention(w.B, H, S, w.D, P)
+    ring = sca.ShardedCausalAttention(w.B, H, S, w.D, P, schedule="ring")
     dbl = sca.ShardedCausalAttention(w.B, H, S, w.D, P, visit="double_ring", inner=inner)
     o1, l1 = ring.forward(q, k, v)
     o2, l2 = dbl.forward(q, k, v)
@@ -140,7 +140,7 @@ def test_double_ring_partials_are_the_ring_partials(sca):
 def test_repeated_calls_are_deterministic(sca):
     B, H, S, D, P = 1, 2, 2048, 128, 4
     q, k, v = seeded_inputs.make_inputs(B, H, S, D, "bf16", seed=3)
-    plan = sca.ShardedCausalAttention(B, H, S, D, P, head_groups=2)
+    plan = sca.ShardedCausalAttention(B, H, S, D, P, head_groups=2, schedule="ring")
     a = [t.clone() for t in plan.forward(q.cuda(), k.cuda(), v.cuda())]
     b = plan.forward(q.cuda(), k.cuda(), v.cuda())
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])

@@ -111,3 +111,19 @@ def test_double_ring_hand_offs(P, inner):
         assert sorted(covered) == sorted(enumerate(senders))
         if t % inner:
             assert len(copy_runs(senders)) == 2 * (P // inner) - (P // inner if inner == 1 else 0)
+
+
+def test_auto_schedule_fuses_short_shards_only():
+    # "auto" fuses when a shard holds at most AUTO_FUSED_MAX_ROWS rows (ring
+    # steps of at most 32 key tiles per CTA) and keeps the ring above, or
+    # whenever the double ring is asked for; explicit schedules pass through
+    from sharded_causal_softmax_gb300.sharded import AUTO_FUSED_MAX_ROWS, resolve_schedule
+    assert AUTO_FUSED_MAX_ROWS == 4096
+    assert resolve_schedule("auto", 8192, 4) == "fused"          # 2048 rows per shard
+    assert resolve_schedule("auto", 16384, 4) == "fused"         # 4096
+    assert resolve_schedule("auto", 32768, 4) == "ring"          # 8192
+    assert resolve_schedule("auto", 131072, 8) == "ring"
+    assert resolve_schedule("auto", 8192, 4, visit="double_ring") == "ring"
+    assert resolve_schedule("auto", 1 << 20, 1) == "fused"       # one shard: nothing to pass around
+    for s in ("ring", "direct", "fused"):
+        assert resolve_schedule(s, 8192, 4) == s
