@@ -67,7 +67,8 @@ def flops(w, fwd=True, bwd=True):
 def workload_config(w, ws: int, visit: str = "ring", inner: int = 0) -> dict:
     """The `config` object both arms print for a workload."""
     from sharded_causal_softmax_gb300.sharded import AUTO_FUSED_MAX_ROWS, resolve_schedule
-    sched = resolve_schedule(w.schedule, w.S, w.P, visit) if w.method == "softmax" else w.schedule
+    sched = (resolve_schedule(w.schedule, w.S, w.P, visit) if w.method == "softmax"
+             else "state passed shard to shard")
     cfg = {"workload": w.description, "name": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "P": w.P,
            "method": w.method, "layout": w.layout, "schedule": sched, "kv_heads": w.kv_heads or w.H,
            "head_groups": w.head_groups, "step": "fwd+bwd" if w.backward else "fwd", "flops_per_step": flops(w),
