@@ -534,11 +534,20 @@ def run_gpu(args):
     if bound == "hbm":
         roofline["bytes_per_launch"] = launch_bytes
         roofline["tflops"] = round(launch_flops / avg_s / 1e12, 2)
+    # the tensor pipe's own dense rate at the clock the region ran at: one
+    # M=128, N=128, K=16 bf16 MMA every 64 clk per SM (measured by a probe),
+    # 8192 FLOP/clk x 152 SMs; the measured cuBLAS peaks above sit below it
+    pipe_mhz = clock_summary.get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
+    pipe_peak = 8192 * 152 * pipe_mhz * 1e6 / 1e12
     if bound == "tensor":
         roofline["peak_regime"] = bf16_regime
         roofline[f"frac_{other_regime}"] = round(achieved / other_peak, 4)
         roofline[f"peak_{other_regime}"] = other_peak
         roofline["sm_mhz_median"] = clock_summary.get("sm_mhz")
+        roofline["frac_of_tensor_pipe"] = round(achieved / pipe_peak, 4)
+        roofline["tensor_pipe_peak"] = round(pipe_peak, 1)
+        roofline["tensor_pipe_peak_source"] = (f"8192 FLOP/clk/SM x 152 SMs x {pipe_mhz:.0f} MHz "
+                                               "(the region's median SM clock, else the maximum)")
     permute_alone = not hbm["zigzag_permute_kernel"] and w.layout == "zigzag"
     if permute_alone:
         # the step addresses rows by position and runs no permute: time the
@@ -592,6 +601,7 @@ def run_gpu(args):
         if plan.uses_tensor_cores(k) and not (bound_of is not None and bound_of(k) == "hbm"):
             other[k][f"frac_{bf16_regime}"] = round(tf / bf16_peak, 4)
             other[k][f"frac_{other_regime}"] = round(tf / other_peak, 4)
+            other[k]["frac_of_tensor_pipe"] = round(tf / pipe_peak, 4)
 
     line = {
         "metric": METRIC,
