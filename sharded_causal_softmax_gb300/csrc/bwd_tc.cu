@@ -27,7 +27,8 @@
 // columns [64g, 64g+64), thread = key row = tensor-memory lane), then read
 // back dQ (thread = query row) and, at the end, dK / dV; warp 8 issues TMA
 // loads (K, V once; Q_i, dO_i double-buffered) and stages lse / delta; warp
-// 9 allocates tensor memory and issues tcgen05.mma from one thread.
+// 9 allocates tensor memory and runs the MMA loop, the whole warp waiting
+// and one elected lane issuing each tcgen05.mma.
 //
 // Tensor memory (512 columns): S^T [0,128), dP^T [128,256), dV [256,256+D),
 // dK [256+D, 256+2D).  Warpgroup g writes its P^T (bf16, 32 columns) over the

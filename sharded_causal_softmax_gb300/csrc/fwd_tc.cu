@@ -5,13 +5,16 @@
 //
 //   warp 8      TMA producer for Q (once) and the K ring (3 stages)
 //   warp 10     TMA producer for the V ring (2 stages)
-//   warp 9      tensor-memory allocation, and one thread issuing tcgen05.mma:
+//   warp 9      tensor-memory allocation, and the MMA loop, run by the
+//               whole warp with one elected lane issuing each tcgen05.mma
+//               (issued under if (lane == 0) the same loop took ~85 clk
+//               per MMA and set the tile period):
 //                 S[n%2] = Q K_n^T           (A = Q from tensor memory)
 //                 O     += P_n V_n           (A = P from tensor memory)
 //               QK^T runs up to two tiles ahead of the softmax.  Keeping Q
 //               in tensor memory halves QK^T's shared-memory operand
 //               traffic (reading Q from shared memory too measured 2%
-//               slower).
+//               slower, and 7% slower even with a third S buffer).
 //   warps 0-7   softmax, two warpgroups: warpgroup g owns columns
 //               [64g, 64g+64) of every S row, thread t of the warpgroup owns
 //               query row t (tensor-memory lane t).  The row maximum is
@@ -33,8 +36,9 @@
 //
 // Tensor memory: S0, S1 in columns [0,256), O in [256, 256+D), Q in
 // [256+D, 256+D+D/2); all 512 columns are allocated (one CTA per SM:
-// shared memory use is above half the SM).  Tiles with no visible (query, key) pair are skipped; tiles that
-// may hold masked pairs or ragged rows are masked elementwise.  Every
+// shared memory use is above half the SM).  Tiles with no visible (query,
+// key) pair are skipped; in tiles that may hold masked pairs or ragged rows
+// each query's visible columns (at most two runs) are masked by key_runs.  Every
 // mbarrier wait is bounded (ptx.cuh); on expiry the CTA records
 // SCA_ERR_TIMEOUT, drains its in-flight copies and MMAs (bounded), frees
 // its tensor memory and exits.
