@@ -129,6 +129,7 @@ struct Bars {
   uint64_t state_full;   // A1 of sub-block c in tensor memory
   uint64_t t1u_done;     // state term and U of sub-block c done: X, Y free, U over A1
   uint64_t m_full;       // masked product of sub-block c in X, Y
+  uint64_t u_read;       // every converter warp has read U (phase per sub-block with a U)
   uint64_t o_full[2], o_free[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_kernel(const __grid_constan
     mbar_init(&bars->state_full, kConv);
     mbar_init(&bars->t1u_done, 1);
     mbar_init(&bars->m_full, kConv);
+    mbar_init(&bars->u_read, kConv);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -315,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_kernel(const __grid_constan
     };
     float run[64];
     bool ok = true;
+    int n_u = 0;   // sub-blocks so far whose U was read (phase of u_read)
     if (n_sub > 0) {
       load_block_state(0, run);
       put_state(run, tA_hi + lane_off, tA_lo + lane_off, half);
@@ -367,9 +370,14 @@ __global__ void __launch_bounds__(kThreads, 1) block_kernel(const __grid_constan
 #pragma unroll
           for (int e = 0; e < 32; ++e) run[32 * cc + e] += __uint_as_float(w[e]);
         }
-        // every warp has read its part of U before any overwrites it
+        // every warp has read its part of U before any overwrites it (a
+        // bounded mbarrier: a warp that gave up on an earlier wait must not
+        // leave the others in a hardware barrier)
         tc_fence_before();
-        asm volatile("bar.sync 1, %0;" ::"n"(kConv) : "memory");
+        mbar_arrive(&bars->u_read);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->u_read, n_u & 1, abort, status));
+        ++n_u;
+        if (!ok) break;
         tc_fence_after();
       } else if (c + 1 < n_sub) {
         load_block_state(c / nsub + 1, run);
